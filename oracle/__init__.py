@@ -1,0 +1,207 @@
+"""Paged-KV exact attention oracle (fp64, CPU).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  The product path (the
+CUDA library and its Python binding) never imports, links or runs it, and the
+two share no code.
+
+``oracle.c`` holds the plain C implementation (see its header for the passages
+of "Transformer inference kernels: GEMM·Attention·FlashAttention·Fusion (3/10)"
+and "code-series sgl-project mini-sglang 07" each function follows); this
+module compiles it with gcc and wraps it for numpy arrays.  ``online.py`` holds
+the online-softmax block merge and the split-KV merge written from sections 12
+and 16 of the first page; ``brute.py`` a tiny pure-Python brute force.
+
+All bf16 tensors cross this interface as ``numpy.uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``_oracle.so`` (gcc, -O2, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    # -O2 without fast-math: every operation stays IEEE double.
+    cmd = ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp", "-fPIC",
+           "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    lib.oracle_store_kv.argtypes = [P, P, P, i64, P, P, i64, i64]
+    lib.oracle_store_kv.restype = ctypes.c_int
+    lib.oracle_page_table_from_token_table.argtypes = [P, i64, P, i32, i32, i32, P, i64]
+    lib.oracle_page_table_from_token_table.restype = ctypes.c_int
+    lib.oracle_seqlens.argtypes = [P, P, i32, P, P, P, P, P]
+    lib.oracle_seqlens.restype = ctypes.c_int
+    lib.oracle_attention.argtypes = [P, P, P, P, i64, P, P, i32, i32, i32, i32, i32,
+                                     i64, ctypes.c_int, dbl, P, i64, P, P]
+    lib.oracle_attention.restype = ctypes.c_int
+    lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    return lib
+
+
+def load_variant(so_path: str):
+    """Load another build of the oracle's C source (the tests compile
+    deliberately broken copies to show that the pins catch each mistake)."""
+    return _bind(ctypes.CDLL(os.path.abspath(so_path)))
+
+
+def _load(lib=None):
+    global _lib
+    if lib is not None:
+        return lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise OracleError(f"{what} failed with oracle status {status}")
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to float64."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def store_kv(k, v, slot_mapping, k_cache, v_cache, *, lib=None) -> None:
+    """KV-cache store into ``k_cache``/``v_cache`` in place (uint16 arrays,
+    first axis = slot, the rest = one token's row)."""
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    sm = _c(slot_mapping, np.int32)
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous
+    assert v_cache.dtype == np.uint16 and v_cache.flags.c_contiguous
+    T = sm.shape[0]
+    row = int(np.prod(k_cache.shape[1:])) if k_cache.ndim > 1 else 1
+    slots = k_cache.shape[0]
+    assert k.size == T * row and v.size == T * row
+    _check(_load(lib).oracle_store_kv(_ptr(k), _ptr(v), _ptr(sm), T, _ptr(k_cache), _ptr(v_cache),
+                                   slots, row), "oracle_store_kv")
+
+
+def page_table_from_token_table(token_table, table_idx, max_seqlen_k: int, page_size: int,
+                                out_cols: int | None = None, *, lib=None) -> np.ndarray:
+    tt = _c(token_table, np.int32)
+    ti = _c(table_idx, np.int32)
+    cols = -(-int(max_seqlen_k) // int(page_size))
+    out_cols = cols if out_cols is None else int(out_cols)
+    out = np.zeros((ti.shape[0], out_cols), dtype=np.int32)
+    _check(_load(lib).oracle_page_table_from_token_table(
+        _ptr(tt), tt.shape[1], _ptr(ti), ti.shape[0], int(max_seqlen_k), int(page_size),
+        _ptr(out), out_cols), "oracle_page_table_from_token_table")
+    return out
+
+
+def seqlens(cached_len, extend_len, *, lib=None):
+    """(cu_seqlens_q, cu_seqlens_k, cache_seqlens, max_seqlen_q, max_seqlen_k)."""
+    c = _c(cached_len, np.int32)
+    e = _c(extend_len, np.int32)
+    B = c.shape[0]
+    cu_q = np.zeros(B + 1, np.int32)
+    cu_k = np.zeros(B + 1, np.int32)
+    cs = np.zeros(max(B, 1), np.int32)
+    mq = np.zeros(1, np.int32)
+    mk = np.zeros(1, np.int32)
+    _check(_load(lib).oracle_seqlens(_ptr(c), _ptr(e), B, _ptr(cu_q), _ptr(cu_k), _ptr(cs),
+                                     _ptr(mq), _ptr(mk)), "oracle_seqlens")
+    return cu_q, cu_k, cs[:B], int(mq[0]), int(mk[0])
+
+
+def attention(q, k_cache, v_cache, page_table, cu_seqlens_q, cu_seqlens_k, *,
+              num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+              causal: bool, scale: float, rows=None, lib=None):
+    """fp64 attention over paged K/V.
+
+    q: uint16 [Tq, Hq, d]; caches: uint16 [num_pages*page_size, Hkv, d] (any
+    shape with that element order); page_table int32 [B, stride].
+    Returns (out, lse): float64 [Tq, Hq, d] and [Tq, Hq], or, when ``rows`` (an
+    int64 [n, 2] array of (token, head)) is given, [n, d] and [n].
+    """
+    q = _c(q, np.uint16)
+    kc = k_cache if (k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous) else _c(k_cache, np.uint16)
+    vc = v_cache if (v_cache.dtype == np.uint16 and v_cache.flags.c_contiguous) else _c(v_cache, np.uint16)
+    pt = _c(page_table, np.int32)
+    if pt.ndim == 1:
+        pt = pt.reshape(-1, 1)
+    cq = _c(cu_seqlens_q, np.int32)
+    ck = _c(cu_seqlens_k, np.int32)
+    B = cq.shape[0] - 1
+    Hq, Hkv, d, P = int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size)
+    num_pages = kc.size // (P * Hkv * d)
+    Tq = int(cq[-1]) if B > 0 else 0
+    if rows is None:
+        out = np.zeros((Tq, Hq, d), dtype=np.float64)
+        lse = np.zeros((Tq, Hq), dtype=np.float64)
+        rp, nr = None, 0
+    else:
+        rws = _c(rows, np.int64).reshape(-1, 2)
+        out = np.zeros((rws.shape[0], d), dtype=np.float64)
+        lse = np.zeros((rws.shape[0],), dtype=np.float64)
+        rp, nr = _ptr(rws), rws.shape[0]
+    _check(_load(lib).oracle_attention(
+        _ptr(q), _ptr(kc), _ptr(vc), _ptr(pt), pt.shape[1], _ptr(cq), _ptr(ck), B,
+        Hq, Hkv, d, P, num_pages, int(bool(causal)), float(scale), rp, nr,
+        _ptr(out), _ptr(lse)), "oracle_attention")
+    return out, lse
+
+
+def decode(q, k_cache, v_cache, page_table, cache_seqlens, *, num_q_heads: int,
+           num_kv_heads: int, head_dim: int, page_size: int, scale: float, rows=None, lib=None):
+    """Decode attention: one query token per sequence attending to all
+    cache_seqlens[b] keys (the new token already stored).  q: [B, Hq, d]."""
+    cs = np.asarray(cache_seqlens, dtype=np.int64)
+    B = cs.shape[0]
+    cu_q = np.arange(B + 1, dtype=np.int32)
+    cu_k = np.zeros(B + 1, dtype=np.int64)
+    cu_k[1:] = np.cumsum(cs)
+    return attention(q, k_cache, v_cache, page_table, cu_q, cu_k.astype(np.int32),
+                     num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                     page_size=page_size, causal=False, scale=scale, rows=rows, lib=lib)
+
+
+from . import online  # noqa: E402,F401  (re-export)

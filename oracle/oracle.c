@@ -1,0 +1,265 @@
+/*
+ * Paged-KV exact attention: the plain, slow fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes, and where the pages define it:
+ *
+ *  - oracle_store_kv: the KV-cache store step, "RoPE + KV cache store" in the
+ *    layer graph of "Transformer inference kernels: GEMM·Attention·
+ *    FlashAttention·Fusion (3/10)", sections 1-2.  Token t's K and V rows are
+ *    copied bit for bit into cache row slot_mapping[t]; a negative slot is a
+ *    padding token and is skipped.
+ *
+ *  - oracle_attention: scaled dot-product attention, same page, section 10
+ *    ("O = softmax(QK^T/sqrt(d) + mask) V"), computed the naive way: the score
+ *    row S is materialised in full, then a two-pass softmax (max, then
+ *    exponentials and their sum), then P.V.  Keys and values are read through
+ *    the page table exactly as section 14 of the same page describes the
+ *    address translation: logical position j -> page_table[b, j / P] ->
+ *    physical page -> row page*P + j % P of the pool.  Query head h reads KV
+ *    head h / (Hq/Hkv), the consecutive grouping of section 15 (32 q heads on
+ *    8 KV heads, group size 4).  Request boundaries come from cu_seqlens_q and
+ *    cu_seqlens_k (exclusive prefix sums of extend_len and device_len), as in
+ *    "code-series sgl-project mini-sglang 07", "from ledger to tensors".  The
+ *    causal mask is aligned to the END of each request's keys: query i of a
+ *    request with Lq queries and Lk keys sits at absolute position
+ *    Lk - Lq + i and sees keys 0 .. Lk - Lq + i (a cached prefix of Lk - Lq
+ *    tokens followed by the Lq extend tokens).  A query row with no visible
+ *    key returns O = 0 and lse = -inf (the "KV: empty" edge case of section
+ *    24 of the first page).
+ *
+ *  - oracle_page_table_from_token_table: the metadata step of the
+ *    mini-sglang page, "from ledger to tensors": the global table is token
+ *    granular (page size 1); a request's row is sliced with step P up to
+ *    max_seqlen_k and, for P > 1, floor-divided by P to turn the slot of each
+ *    page's first token into that page's id.
+ *
+ * All arithmetic on floating point is IEEE double.  bf16 inputs are widened
+ * exactly (a bf16 value is the top 16 bits of an IEEE single).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL -1
+#define ORACLE_ERANGE -2
+#define ORACLE_ENOMEM -3
+
+static double widen_bf16(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* KV store.  k, v: [T, row_elems] bf16 bits; caches: [num_slots, row_elems]. */
+int oracle_store_kv(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
+                    int64_t num_tokens, uint16_t *k_cache, uint16_t *v_cache,
+                    int64_t num_slots, int64_t row_elems)
+{
+    if (num_tokens < 0 || num_slots < 0 || row_elems <= 0) return ORACLE_EINVAL;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) return ORACLE_ERANGE;
+        memcpy(k_cache + slot * row_elems, k + t * row_elems, (size_t)row_elems * 2);
+        memcpy(v_cache + slot * row_elems, v + t * row_elems, (size_t)row_elems * 2);
+    }
+    return ORACLE_OK;
+}
+
+/* Metadata: page table [B, out_cols] from the token-granular global table.
+ * token_table: [num_rows, tt_stride]; table_idx[b] selects request b's row.
+ * Column c of the result is token_table[table_idx[b], c * P] / P (floor). */
+int oracle_page_table_from_token_table(const int32_t *token_table, int64_t tt_stride,
+                                       const int32_t *table_idx, int32_t num_seqs,
+                                       int32_t max_seqlen_k, int32_t page_size,
+                                       int32_t *out, int64_t out_cols)
+{
+    if (page_size <= 0 || num_seqs < 0 || max_seqlen_k < 0) return ORACLE_EINVAL;
+    int64_t cols = ((int64_t)max_seqlen_k + page_size - 1) / page_size;
+    if (cols > out_cols) return ORACLE_EINVAL;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        const int32_t *row = token_table + (int64_t)table_idx[b] * tt_stride;
+        for (int64_t c = 0; c < cols; ++c) {
+            int64_t slot = row[c * page_size];
+            /* floor division; slots are non-negative for real tokens */
+            int64_t q = slot / page_size;
+            if (slot < 0 && q * page_size != slot) q -= 1;
+            out[(int64_t)b * out_cols + c] = (int32_t)q;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Metadata: per-request boundaries from the three lengths.  extend_len is the
+ * query length and device_len = cached_len + extend_len the key length of each
+ * request; cu_q / cu_k are their exclusive prefix sums starting at 0 and
+ * cache_seqlens is device_len itself ("from ledger to tensors"). */
+int oracle_seqlens(const int32_t *cached_len, const int32_t *extend_len, int32_t num_seqs,
+                   int32_t *cu_q, int32_t *cu_k, int32_t *cache_seqlens,
+                   int32_t *max_seqlen_q, int32_t *max_seqlen_k)
+{
+    if (num_seqs < 0) return ORACLE_EINVAL;
+    int64_t sq = 0, sk = 0;
+    int32_t mq = 0, mk = 0;
+    cu_q[0] = 0;
+    cu_k[0] = 0;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        int64_t lq = extend_len[b];
+        int64_t lk = (int64_t)cached_len[b] + extend_len[b];
+        if (lq < 0 || cached_len[b] < 0) return ORACLE_EINVAL;
+        sq += lq;
+        sk += lk;
+        if (sq > INT32_MAX || sk > INT32_MAX) return ORACLE_ERANGE;
+        cu_q[b + 1] = (int32_t)sq;
+        cu_k[b + 1] = (int32_t)sk;
+        cache_seqlens[b] = (int32_t)lk;
+        if (lq > mq) mq = (int32_t)lq;
+        if (lk > mk) mk = (int32_t)lk;
+    }
+    *max_seqlen_q = mq;
+    *max_seqlen_k = mk;
+    return ORACLE_OK;
+}
+
+/* One attention row: query token t (global index into q), query head h.
+ * Writes d doubles to o and one to *lse.  scratch holds >= Lk doubles. */
+static int attention_row(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *page_table, int64_t pt_stride,
+                         const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
+                         int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
+                         int causal, double scale, int64_t t, int32_t h,
+                         double *o, double *lse, double *s_row)
+{
+    /* request b owning query token t */
+    int32_t b = -1;
+    for (int32_t i = 0; i < num_seqs; ++i) {
+        if (cu_q[i] <= t && t < cu_q[i + 1]) { b = i; break; }
+    }
+    if (b < 0) return ORACLE_EINVAL;
+    int64_t Lq = cu_q[b + 1] - cu_q[b];
+    int64_t Lk = cu_k[b + 1] - cu_k[b];
+    int64_t i = t - cu_q[b];
+    int64_t off = Lk - Lq;                 /* cached prefix length */
+    int64_t n_vis = Lk;
+    if (causal) {
+        int64_t lim = off + i + 1;         /* keys 0 .. off+i are visible */
+        if (lim < n_vis) n_vis = lim;
+        if (n_vis < 0) n_vis = 0;
+    }
+    int32_t g = Hq / Hkv;
+    int32_t kvh = h / g;
+    const uint16_t *qrow = q + (t * Hq + h) * (int64_t)d;
+
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    if (n_vis <= 0) { *lse = -INFINITY; return ORACLE_OK; }
+
+    /* pass 0: materialise the score row S[j] = scale * q . K_j */
+    for (int64_t j = 0; j < n_vis; ++j) {
+        int64_t page = page_table[b * pt_stride + j / P];
+        if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+        int64_t row = page * P + j % P;
+        const uint16_t *krow = k_cache + (row * Hkv + kvh) * (int64_t)d;
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += widen_bf16(qrow[c]) * widen_bf16(krow[c]);
+        s_row[j] = scale * acc;
+    }
+    /* pass 1: row maximum */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n_vis; ++j) if (s_row[j] > m) m = s_row[j];
+    /* pass 2: exponentials, their sum, and P.V */
+    double l = 0.0;
+    for (int64_t j = 0; j < n_vis; ++j) {
+        double p = exp(s_row[j] - m);
+        l += p;
+        int64_t page = page_table[b * pt_stride + j / P];
+        int64_t row = page * P + j % P;
+        const uint16_t *vrow = v_cache + (row * Hkv + kvh) * (int64_t)d;
+        for (int c = 0; c < d; ++c) o[c] += p * widen_bf16(vrow[c]);
+    }
+    for (int c = 0; c < d; ++c) o[c] /= l;
+    *lse = m + log(l);
+    return ORACLE_OK;
+}
+
+/* Attention over paged K/V.
+ * q: [Tq, Hq, d] bf16 bits; k_cache, v_cache: [num_pages*P, Hkv, d] bf16 bits;
+ * page_table: [num_seqs, pt_stride] int32; cu_q, cu_k: [num_seqs+1] int32.
+ * rows == NULL: every (token, head) row; out [Tq, Hq, d], lse [Tq, Hq].
+ * rows != NULL: nrows pairs (token, head) as int64; out [nrows, d], lse [nrows]. */
+int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                     const int32_t *page_table, int64_t pt_stride,
+                     const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
+                     int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
+                     int causal, double scale, const int64_t *rows, int64_t nrows,
+                     double *out, double *lse)
+{
+    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || P <= 0 || Hq % Hkv) return ORACLE_EINVAL;
+    int64_t Tq = num_seqs > 0 ? cu_q[num_seqs] : 0;
+    int64_t max_lk = 0;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        int64_t Lq = cu_q[b + 1] - cu_q[b], Lk = cu_k[b + 1] - cu_k[b];
+        /* more queries than keys is malformed, except over an empty KV
+         * range (a padded or dummy request): then every row sees nothing */
+        if (Lq < 0 || Lk < 0 || (Lq > Lk && Lk > 0)) return ORACLE_EINVAL;
+        if (Lk > max_lk) max_lk = Lk;
+    }
+    int64_t n = rows ? nrows : Tq * Hq;
+    int status = ORACLE_OK;
+#pragma omp parallel
+    {
+        double *s_row = (double *)malloc(sizeof(double) * (size_t)(max_lk > 0 ? max_lk : 1));
+        if (!s_row) {
+#pragma omp atomic write
+            status = ORACLE_ENOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < n; ++r) {
+                int64_t t = rows ? rows[2 * r] : r / Hq;
+                int32_t h = (int32_t)(rows ? rows[2 * r + 1] : r % Hq);
+                if (t < 0 || t >= Tq || h < 0 || h >= Hq) {
+#pragma omp atomic write
+                    status = ORACLE_EINVAL;
+                    continue;
+                }
+                int st = attention_row(q, k_cache, v_cache, page_table, pt_stride, cu_q, cu_k,
+                                       num_seqs, Hq, Hkv, d, P, num_pages, causal, scale, t, h,
+                                       out + r * (int64_t)d, lse + r, s_row);
+                if (st != ORACLE_OK) {
+#pragma omp atomic write
+                    status = st;
+                }
+            }
+            free(s_row);
+        }
+    }
+    return status;
+}

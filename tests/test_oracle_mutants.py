@@ -1,0 +1,55 @@
+"""Plant plausible mistakes in copies of the oracle's C source and show that
+the pins catch every one (CPU only; the real oracle is never modified)."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_CHECKS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text in oracle.c, replacement, replace-count)
+MUTANTS = [
+    ("causal_top_left", "int64_t lim = off + i + 1;", "int64_t lim = i + 1;", 1),
+    ("causal_off_by_one", "int64_t lim = off + i + 1;", "int64_t lim = off + i;", 1),
+    ("no_causal_mask", "if (causal) {", "if (0) {", 1),
+    ("gqa_modulo_heads", "int32_t kvh = h / g;", "int32_t kvh = h % Hkv;", 1),
+    ("scale_dropped", "s_row[j] = scale * acc;", "s_row[j] = acc;", 1),
+    ("page_offset_swapped", "int64_t row = page * P + j % P;", "int64_t row = page * P + j / P;", 1),
+    ("page_index_transposed", "page_table[b * pt_stride + j / P]", "page_table[b * pt_stride + j % P]", 1),
+    ("no_normalisation", "for (int c = 0; c < d; ++c) o[c] /= l;", "", 1),
+    ("lse_missing_max", "*lse = m + log(l);", "*lse = log(l);", 1),
+    ("values_from_k_cache", "const uint16_t *vrow = v_cache +", "const uint16_t *vrow = k_cache +", 1),
+    ("exp_sign_flipped", "double p = exp(s_row[j] - m);", "double p = exp(m - s_row[j]);", 1),
+    ("last_key_dropped", "for (int64_t j = 0; j < n_vis; ++j) {\n        double p", "for (int64_t j = 0; j + 1 < n_vis; ++j) {\n        double p", 1),
+    ("cu_k_prefix_wrong", "cu_k[b + 1] = (int32_t)sk;", "cu_k[b + 1] = (int32_t)sq;", 1),
+    ("page_table_no_divide", "int64_t q = slot / page_size;", "int64_t q = slot;", 1),
+    ("store_swaps_k_v", "memcpy(k_cache + slot * row_elems, k + t * row_elems", "memcpy(k_cache + slot * row_elems, v + t * row_elems", 1),
+]
+
+
+def _build_mutant(tmp_path, name, old, new, count):
+    src = open(SRC).read()
+    assert src.count(old) >= count, f"mutation anchor for {name} not found"
+    mutated = src.replace(old, new, count)
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"{name}.so"
+    c.write_text(mutated)
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", str(c), "-o", str(so), "-lm"],
+                   check=True)
+    return oracle.load_variant(str(so))
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=lambda m: m[0])
+def test_pins_catch_mutant(tmp_path, mutant):
+    name, old, new, count = mutant
+    lib = _build_mutant(tmp_path, name, old, new, count)
+    caught = []
+    for check in ALL_CHECKS:
+        try:
+            check(lib=lib)
+        except (AssertionError, oracle.OracleError):
+            caught.append(check.__name__)
+    assert caught, f"no pin caught the planted mistake '{name}'"
