@@ -1,0 +1,224 @@
+/*
+ * pa.h - C ABI of the paged-KV attention library (libpa.so, sm_103a).
+ *
+ * Exact attention over a paged KV cache, as a serving engine runs it:
+ *   pa_store_kv          write the new tokens' K/V rows into the paged pool
+ *   pa_build_seqlens     per-request boundaries from the three lengths (host)
+ *   pa_build_page_table  per-request page table from the token-granular table
+ *   pa_prefill           varlen causal prefill / extend attention
+ *   pa_decode            one-query-per-sequence split-KV decode attention
+ *   pa_lse_combine       merge of split partial results by log-sum-exp
+ *
+ * Sources (web pages; section names as printed on them):
+ *  [T] "Transformer inference kernels: GEMM·Attention·FlashAttention·Fusion
+ *      (3/10)": s.1-2 layer graph (RoPE + KV cache store, then attention),
+ *      s.10 scaled dot-product attention, s.11 tiled exact attention, s.12
+ *      online softmax, s.13 prefill vs decode, s.14 paged-KV address
+ *      translation, s.15 GQA head mapping, s.16 split-KV with stable merge,
+ *      s.24 edge-case matrix.
+ *  [M] "code-series sgl-project mini-sglang 07": "from ledger to tensors"
+ *      (extend_len / device_len / cached_len, cu_seqlens_q, cu_seqlens_k,
+ *      cache_seqlens, the page-size-1 global table sliced with step P and
+ *      floor-divided by P), "the layer does not know the backend" (q viewed
+ *      as [-1, Hq, d]).
+ *
+ * Conventions shared by every call
+ *  - bf16 tensors are IEEE bfloat16; all metadata is int32; device offsets
+ *    are computed in 64 bits (pools larger than 2^31 bytes are fine).
+ *  - KV pool layout (K and V alike): [num_pages, page_size, Hkv, d], row
+ *    major.  The physical row of logical key j of request b is
+ *    page_table[b * page_table_stride + j / page_size] * page_size
+ *    + j % page_size  ([T] s.14).  With page_size 1 the table holds slots.
+ *  - GQA: query head h reads KV head h / (Hq / Hkv)  ([T] s.15).
+ *  - Causal masks are aligned to the END of each request's keys: query i of
+ *    a request with Lq queries and Lk keys sees keys 0 .. Lk - Lq + i
+ *    (cached prefix, then the extend tokens; [M]).
+ *  - A query row that sees no key yields O = 0 and lse = -inf.
+ *  - Supported: head_dim 64 or 128; page_size 1 or 16; Hq % Hkv == 0 with
+ *    group size Hq / Hkv in {1, 2, 4, 8}; Hkv * head_dim <= 4096.
+ *  - Every device pointer must be 16-byte aligned.  The library allocates
+ *    no memory: the caller owns every buffer, including the decode workspace.
+ *  - Calls are asynchronous on the given CUDA stream (a cudaStream_t passed
+ *    as void*; NULL = legacy default stream) and never synchronise it.
+ *  - Errors: arguments are validated on the host before any launch; a
+ *    rejected call launches nothing and returns PA_ERR_INVALID or
+ *    PA_ERR_UNSUPPORTED.  A failed launch returns PA_ERR_CUDA.  The text of
+ *    the last failure on the calling thread is pa_last_error().  Values that
+ *    live on the device (page ids, slots, cu_seqlens) cannot be checked
+ *    before launch; kernels skip any access outside the pool and raise the
+ *    device error word instead, which pa_device_error() reads.  There is no
+ *    fallback path of any kind.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,      /* malformed arguments */
+    PA_ERR_UNSUPPORTED = 2,  /* well-formed but outside the supported set */
+    PA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+    PA_ERR_DEVICE = 4        /* a kernel flagged bad device-side metadata */
+} pa_status;
+
+/* Device error bits (pa_device_error). */
+#define PA_DEVERR_PAGE_RANGE 1   /* a page id / slot outside the pool was skipped */
+#define PA_DEVERR_SEQLENS 2      /* cu_seqlens / cache_seqlens inconsistent */
+#define PA_DEVERR_TIMEOUT 4      /* a bounded wait in a kernel gave up */
+
+int pa_abi_version(void);
+const char *pa_status_string(int status);
+/* Message of the last failed call on this thread ("" if none). */
+const char *pa_last_error(void);
+
+/* Read and clear the device error word of the current device.  Synchronises
+ * `stream` first.  *bits receives an OR of PA_DEVERR_* (0 = clean). */
+pa_status pa_device_error(int32_t *bits, void *stream);
+
+/*
+ * pa_store_kv - KV-cache store ([T] s.1-2, "RoPE + KV cache store"):
+ *   for t in [0, num_tokens): s = slot_mapping[t];
+ *     if s >= 0: k_cache_row[s] = k[t]; v_cache_row[s] = v[t]   (bit copy)
+ * k, v:          device bf16 [num_tokens, Hkv, head_dim]
+ * slot_mapping:  device int32 [num_tokens]; slot = page * page_size + offset;
+ *                a negative slot marks a padding token and is skipped;
+ *                a slot >= num_slots is skipped and raises PA_DEVERR_PAGE_RANGE.
+ *                Two tokens with the same slot are a caller error.
+ * k_cache, v_cache: device bf16 [num_slots, Hkv, head_dim] (a pool
+ *                [num_pages, page_size, Hkv, d] has num_slots = pages * size).
+ */
+pa_status pa_store_kv(const void *k, const void *v, const int32_t *slot_mapping,
+                      int64_t num_tokens, void *k_cache, void *v_cache, int64_t num_slots,
+                      int32_t num_kv_heads, int32_t head_dim, void *stream);
+
+/*
+ * pa_build_seqlens - host-side metadata ([M], "from ledger to tensors").
+ * All pointers are HOST memory.  From cached_len[b] and extend_len[b]:
+ *   cu_seqlens_q  [num_seqs+1] = exclusive prefix sum of extend_len
+ *   cu_seqlens_k  [num_seqs+1] = exclusive prefix sum of device_len
+ *   cache_seqlens [num_seqs]   = device_len = cached_len + extend_len
+ *   *max_seqlen_q, *max_seqlen_k = the maxima.
+ * Negative lengths or sums beyond INT32_MAX are PA_ERR_INVALID.
+ */
+pa_status pa_build_seqlens(const int32_t *cached_len, const int32_t *extend_len,
+                           int32_t num_seqs, int32_t *cu_seqlens_q, int32_t *cu_seqlens_k,
+                           int32_t *cache_seqlens, int32_t *max_seqlen_q,
+                           int32_t *max_seqlen_k);
+
+/*
+ * pa_build_page_table - device-side metadata ([M]): the global table is token
+ * granular (page size 1, one slot per position); request b's row
+ * token_table[table_idx[b], :] is sliced with step page_size up to
+ * max_seqlen_k and floor-divided by page_size:
+ *   page_table[b * page_table_stride + c] =
+ *       floor(token_table[table_idx[b] * token_table_stride + c * page_size] / page_size)
+ *   for c < ceil(max_seqlen_k / page_size).
+ * token_table, table_idx, page_table: device int32.  Columns at and beyond
+ * ceil(max_seqlen_k / page_size) are not written.
+ */
+pa_status pa_build_page_table(const int32_t *token_table, int64_t token_table_stride,
+                              const int32_t *table_idx, int32_t num_seqs,
+                              int32_t max_seqlen_k, int32_t page_size, int32_t *page_table,
+                              int32_t page_table_stride, void *stream);
+
+/*
+ * pa_prefill - varlen prefill / extend attention ([T] s.10-15, [M]).
+ * For request b: Lq = cu_seqlens_q[b+1] - cu_seqlens_q[b] queries (the extend
+ * tokens, rows cu_seqlens_q[b].. of q and out), Lk = cu_seqlens_k[b+1] -
+ * cu_seqlens_k[b] keys read through page_table row b (Lk >= Lq unless Lk = 0).
+ *   out[t, h, :] = softmax_j(scale * q[t,h,:] . K_j) V_j over the visible keys,
+ *   lse[h * lse_stride + t] = ln sum_j exp(scale * q . K_j)   (optional)
+ * The score matrix never leaves the chip (tiled, online softmax; [T] s.11-12).
+ * max_seqlen_q / max_seqlen_k must bound every request's Lq / Lk.
+ */
+typedef struct {
+    const void *q;               /* bf16 [total_q, Hq, d] */
+    const void *k_cache;         /* bf16 [num_pages, page_size, Hkv, d] */
+    const void *v_cache;
+    const int32_t *page_table;   /* int32 [num_seqs, page_table_stride] */
+    int32_t page_table_stride;
+    const int32_t *cu_seqlens_q; /* int32 [num_seqs + 1] */
+    const int32_t *cu_seqlens_k; /* int32 [num_seqs + 1] */
+    int32_t num_seqs;
+    int32_t max_seqlen_q;
+    int32_t max_seqlen_k;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t page_size;
+    int64_t num_pages;
+    int32_t causal;              /* 0 or 1 */
+    float scale;                 /* usually 1/sqrt(head_dim) */
+    void *out;                   /* bf16 [total_q, Hq, d] */
+    float *lse;                  /* optional fp32 [Hq, lse_stride]; NULL = not written */
+    int64_t lse_stride;          /* >= total_q when lse != NULL */
+} pa_prefill_params;
+
+pa_status pa_prefill(const pa_prefill_params *p, void *stream);
+
+/*
+ * pa_decode - decode attention ([T] s.13 and s.16): one query token per
+ * sequence (q row b) attends to all cache_seqlens[b] keys of its page-table
+ * row (the new token already stored).  The key range is cut into splits of
+ * kv_chunk keys; each split yields a partial (O_s, lse_s) in the workspace
+ * and a log-sum-exp combine pass merges them.  When every sequence fits one
+ * split the first pass writes `out` directly and no combine runs.
+ */
+typedef struct {
+    const void *q;               /* bf16 [num_seqs, Hq, d] */
+    const void *k_cache;         /* bf16 [num_pages, page_size, Hkv, d] */
+    const void *v_cache;
+    const int32_t *page_table;   /* int32 [num_seqs, page_table_stride] */
+    int32_t page_table_stride;
+    const int32_t *cache_seqlens;/* int32 [num_seqs] */
+    int32_t num_seqs;
+    int32_t max_seqlen_k;        /* >= every cache_seqlens[b] */
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t page_size;
+    int64_t num_pages;
+    float scale;
+    void *out;                   /* bf16 [num_seqs, Hq, d] */
+    float *lse;                  /* optional fp32 [num_seqs, Hq]; NULL = not written */
+    void *workspace;             /* device, >= pa_decode_workspace_size(p) bytes */
+    size_t workspace_bytes;
+    int32_t kv_chunk;            /* keys per split, multiple of 16; 0 = automatic */
+} pa_decode_params;
+
+/* Bytes of workspace pa_decode needs for these parameters (0 when a single
+ * split covers max_seqlen_k).  Reads only host fields of *p. */
+size_t pa_decode_workspace_size(const pa_decode_params *p);
+/* The split size pa_decode will use for these parameters. */
+int32_t pa_decode_kv_chunk(const pa_decode_params *p);
+
+pa_status pa_decode(const pa_decode_params *p, void *stream);
+
+/*
+ * pa_lse_combine - stable merge of split partials ([T] s.12 and s.16):
+ * for each row r (a (sequence, head) pair) and its n_r = num_splits_of_row
+ * splits: M = max_s lse_s, w_s = exp(lse_s - M),
+ *   out[r, :] = sum_s w_s O_s[r, :] / sum_s w_s,  lse[r] = M + ln sum_s w_s.
+ * o_partial:   device fp32 [num_rows, max_splits, head_dim] (normalised O_s)
+ * lse_partial: device fp32 [num_rows, max_splits] (natural log; -inf = empty)
+ * splits_per_row: device int32 [num_rows] or NULL (= max_splits for all)
+ * out: device bf16 [num_rows, head_dim]; lse_out: device fp32 [num_rows] or NULL.
+ * A row with no split, or only empty splits, gives zeros and -inf.
+ */
+pa_status pa_lse_combine(const float *o_partial, const float *lse_partial,
+                         const int32_t *splits_per_row, int32_t num_rows, int32_t max_splits,
+                         int32_t head_dim, void *out, float *lse_out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

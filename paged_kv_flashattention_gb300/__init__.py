@@ -1,0 +1,17 @@
+"""Paged-KV exact attention for GB300 (sm_103a).
+
+A small C-ABI library (``libpa.so``, declared in ``include/pa.h``) with
+hand-written CUDA kernels for the KV-cache store, varlen causal prefill /
+extend attention over a page table, split-KV decode and the log-sum-exp
+combine; this package is its thin torch binding.  PyTorch provides device
+memory and streams only.
+"""
+from .api import (PagedAttentionError, abi_version, build_page_table, build_seqlens, decode,
+                  decode_kv_chunk, decode_workspace_size, device_error, lse_combine, prefill,
+                  store_kv)
+
+__all__ = [
+    "PagedAttentionError", "abi_version", "build_page_table", "build_seqlens", "decode",
+    "decode_kv_chunk", "decode_workspace_size", "device_error", "lse_combine", "prefill",
+    "store_kv",
+]

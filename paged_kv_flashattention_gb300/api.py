@@ -1,0 +1,268 @@
+"""Thin torch binding of the C ABI (argument marshalling only).
+
+Every function checks dtypes, devices and contiguity, passes raw pointers and
+the current CUDA stream to libpa, and raises ``PagedAttentionError`` on a
+non-zero status.  No arithmetic of the attention path happens here.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import numpy as np
+import torch
+
+from . import _lib
+
+PA_OK = 0
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def _check(status: int, lib=None):
+    if status != PA_OK:
+        lib = lib or _lib.load()
+        msg = lib.pa_last_error().decode(errors="replace")
+        name = lib.pa_status_string(status).decode()
+        raise PagedAttentionError(status, f"{name}: {msg}")
+
+
+def _stream(t: torch.Tensor | None = None) -> int:
+    dev = t.device if t is not None else None
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype, device=None, contiguous=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def abi_version() -> int:
+    return int(_lib.load().pa_abi_version())
+
+
+def device_error() -> int:
+    """Read and clear the device error word (synchronises the current stream)."""
+    lib = _lib.load()
+    bits = ctypes.c_int32(0)
+    _check(lib.pa_device_error(ctypes.byref(bits), _stream()), lib)
+    return int(bits.value)
+
+
+def store_kv(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+             k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    """Write token t's K/V rows into row slot_mapping[t] of the pools.
+    k, v: bf16 [T, Hkv, d]; caches: bf16 [num_pages, page_size, Hkv, d] or
+    [num_slots, Hkv, d]; slot_mapping: int32 [T] (negative = skip)."""
+    dev = k_cache.device
+    for t, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, dev)
+    _need(slot_mapping, "slot_mapping", torch.int32, dev)
+    Hkv, d = k_cache.shape[-2], k_cache.shape[-1]
+    T = slot_mapping.numel()
+    if k.numel() != T * Hkv * d or v.numel() != T * Hkv * d:
+        raise ValueError("k/v must hold num_tokens rows of Hkv*d")
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    num_slots = k_cache.numel() // (Hkv * d)
+    lib = _lib.load()
+    _check(lib.pa_store_kv(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
+                           num_slots, Hkv, d, _stream(k_cache)), lib)
+
+
+def build_seqlens(cached_len, extend_len):
+    """Host metadata: (cu_seqlens_q, cu_seqlens_k, cache_seqlens, max_q, max_k)
+    as int32 numpy arrays (the C entry point does the arithmetic)."""
+    c = np.ascontiguousarray(cached_len, dtype=np.int32)
+    e = np.ascontiguousarray(extend_len, dtype=np.int32)
+    B = c.shape[0]
+    cu_q = np.zeros(B + 1, np.int32)
+    cu_k = np.zeros(B + 1, np.int32)
+    cs = np.zeros(max(B, 1), np.int32)
+    mq = ctypes.c_int32(0)
+    mk = ctypes.c_int32(0)
+    lib = _lib.load()
+    _check(lib.pa_build_seqlens(c.ctypes.data, e.ctypes.data, B, cu_q.ctypes.data,
+                                cu_k.ctypes.data, cs.ctypes.data, ctypes.byref(mq),
+                                ctypes.byref(mk)), lib)
+    return cu_q, cu_k, cs[:B], int(mq.value), int(mk.value)
+
+
+def build_page_table(token_table: torch.Tensor, table_idx: torch.Tensor, max_seqlen_k: int,
+                     page_size: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Device metadata: page table [B, ceil(max_seqlen_k / page_size)] from the
+    token-granular global table (sliced with step page_size, floor-divided)."""
+    dev = token_table.device
+    _need(token_table, "token_table", torch.int32, dev)
+    _need(table_idx, "table_idx", torch.int32, dev)
+    B = table_idx.numel()
+    ncols = -(-int(max_seqlen_k) // int(page_size))
+    if out is None:
+        out = torch.empty((B, max(ncols, 1)), dtype=torch.int32, device=dev)
+    _need(out, "out", torch.int32, dev)
+    lib = _lib.load()
+    _check(lib.pa_build_page_table(_ptr(token_table), token_table.stride(0), _ptr(table_idx), B,
+                                   int(max_seqlen_k), int(page_size), _ptr(out), out.stride(0),
+                                   _stream(token_table)), lib)
+    return out
+
+
+def _pool_geometry(k_cache: torch.Tensor, v_cache: torch.Tensor, page_size: int | None):
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    if k_cache.dim() == 4:
+        num_pages, P, Hkv, d = k_cache.shape
+        if page_size is not None and page_size != P:
+            raise ValueError("page_size does not match the pool shape")
+    elif k_cache.dim() == 3:
+        if page_size is None:
+            raise ValueError("page_size is required for a [slots, Hkv, d] pool")
+        slots, Hkv, d = k_cache.shape
+        P = page_size
+        num_pages = slots // P
+    else:
+        raise ValueError("pool must be [pages, page_size, Hkv, d] or [slots, Hkv, d]")
+    return int(num_pages), int(P), int(Hkv), int(d)
+
+
+def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
+            cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int,
+            max_seqlen_k: int, *, causal: bool = True, scale: float | None = None,
+            page_size: int | None = None, out: torch.Tensor | None = None,
+            lse: torch.Tensor | None = None) -> torch.Tensor:
+    """Varlen prefill / extend attention.  q: bf16 [total_q, Hq, d];
+    returns out bf16 [total_q, Hq, d]; lse (optional) fp32 [Hq, total_q]."""
+    dev = q.device
+    num_pages, P, Hkv, d = _pool_geometry(k_cache, v_cache, page_size)
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, dev)
+    for t, n in ((page_table, "page_table"), (cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        _need(t, n, torch.int32, dev, contiguous=(n != "page_table"))
+    if page_table.dim() != 2 or page_table.stride(1) != 1:
+        raise ValueError("page_table must be 2-D with unit column stride")
+    total_q, Hq, dq = q.shape
+    if dq != d:
+        raise ValueError("head_dim of q and the pool differ")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev, contiguous=False)
+        if lse.dim() != 2 or lse.shape[0] != Hq or lse.stride(1) != 1:
+            raise ValueError("lse must be [Hq, >= total_q] with unit inner stride")
+    p = _lib.PrefillParams(
+        q=_ptr(q), k_cache=_ptr(k_cache), v_cache=_ptr(v_cache), page_table=_ptr(page_table),
+        page_table_stride=page_table.stride(0), cu_seqlens_q=_ptr(cu_seqlens_q),
+        cu_seqlens_k=_ptr(cu_seqlens_k), num_seqs=cu_seqlens_q.numel() - 1,
+        max_seqlen_q=int(max_seqlen_q), max_seqlen_k=int(max_seqlen_k), num_q_heads=Hq,
+        num_kv_heads=Hkv, head_dim=d, page_size=P, num_pages=num_pages, causal=int(bool(causal)),
+        scale=float(1.0 / math.sqrt(d) if scale is None else scale), out=_ptr(out),
+        lse=_ptr(lse), lse_stride=(lse.stride(0) if lse is not None else 0))
+    lib = _lib.load()
+    _check(lib.pa_prefill(ctypes.byref(p), _stream(q)), lib)
+    return out
+
+
+def _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k, scale, page_size,
+                   out, lse, workspace, kv_chunk):
+    num_pages, P, Hkv, d = _pool_geometry(k_cache, v_cache, page_size)
+    B, Hq, dq = q.shape
+    if dq != d:
+        raise ValueError("head_dim of q and the pool differ")
+    return _lib.DecodeParams(
+        q=_ptr(q), k_cache=_ptr(k_cache), v_cache=_ptr(v_cache), page_table=_ptr(page_table),
+        page_table_stride=page_table.stride(0) if page_table is not None else 0,
+        cache_seqlens=_ptr(cache_seqlens), num_seqs=B, max_seqlen_k=int(max_seqlen_k),
+        num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, page_size=P, num_pages=num_pages,
+        scale=float(1.0 / math.sqrt(d) if scale is None else scale), out=_ptr(out), lse=_ptr(lse),
+        workspace=_ptr(workspace), workspace_bytes=(workspace.numel() * workspace.element_size()
+                                                    if workspace is not None else 0),
+        kv_chunk=int(kv_chunk))
+
+
+def decode_workspace_size(q_shape, k_cache: torch.Tensor, max_seqlen_k: int, *,
+                          page_size: int | None = None, kv_chunk: int = 0) -> int:
+    """Workspace bytes pa_decode needs (0 when a single split suffices)."""
+    B, Hq, d = q_shape
+    num_pages, P, Hkv, dk = _pool_geometry(k_cache, k_cache, page_size)
+    p = _lib.DecodeParams(num_seqs=B, max_seqlen_k=int(max_seqlen_k), num_q_heads=Hq,
+                          num_kv_heads=Hkv, head_dim=d, page_size=P, num_pages=num_pages,
+                          scale=1.0, kv_chunk=int(kv_chunk))
+    return int(_lib.load().pa_decode_workspace_size(ctypes.byref(p)))
+
+
+def decode_kv_chunk(q_shape, k_cache: torch.Tensor, max_seqlen_k: int, *,
+                    page_size: int | None = None, kv_chunk: int = 0) -> int:
+    B, Hq, d = q_shape
+    num_pages, P, Hkv, dk = _pool_geometry(k_cache, k_cache, page_size)
+    p = _lib.DecodeParams(num_seqs=B, max_seqlen_k=int(max_seqlen_k), num_q_heads=Hq,
+                          num_kv_heads=Hkv, head_dim=d, page_size=P, num_pages=num_pages,
+                          scale=1.0, kv_chunk=int(kv_chunk))
+    return int(_lib.load().pa_decode_kv_chunk(ctypes.byref(p)))
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
+           cache_seqlens: torch.Tensor, max_seqlen_k: int, *, scale: float | None = None,
+           page_size: int | None = None, out: torch.Tensor | None = None,
+           lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+           kv_chunk: int = 0) -> torch.Tensor:
+    """Split-KV decode: q bf16 [B, Hq, d] -> out bf16 [B, Hq, d]; lse fp32 [B, Hq].
+    ``workspace`` (a uint8 CUDA tensor) is allocated here when not given."""
+    dev = q.device
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, dev)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, dev)
+    _need(page_table, "page_table", torch.int32, dev, contiguous=False)
+    if page_table.dim() != 2 or page_table.stride(1) != 1:
+        raise ValueError("page_table must be 2-D with unit column stride")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    need = decode_workspace_size(q.shape, k_cache, max_seqlen_k, page_size=page_size, kv_chunk=kv_chunk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    p = _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k, scale, page_size,
+                       out, lse, workspace, kv_chunk)
+    lib = _lib.load()
+    _check(lib.pa_decode(ctypes.byref(p), _stream(q)), lib)
+    return out
+
+
+def lse_combine(o_partial: torch.Tensor, lse_partial: torch.Tensor,
+                splits_per_row: torch.Tensor | None = None, *, out: torch.Tensor | None = None,
+                lse: torch.Tensor | None = None) -> torch.Tensor:
+    """Merge split partials: o_partial fp32 [R, S, d], lse_partial fp32 [R, S]
+    -> out bf16 [R, d] (and lse fp32 [R] if given)."""
+    dev = o_partial.device
+    _need(o_partial, "o_partial", torch.float32, dev)
+    _need(lse_partial, "lse_partial", torch.float32, dev)
+    R, S, d = o_partial.shape
+    if lse_partial.shape != (R, S):
+        raise ValueError("lse_partial must be [R, S]")
+    if splits_per_row is not None:
+        _need(splits_per_row, "splits_per_row", torch.int32, dev)
+    if out is None:
+        out = torch.empty((R, d), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    lib = _lib.load()
+    _check(lib.pa_lse_combine(_ptr(o_partial), _ptr(lse_partial), _ptr(splits_per_row), R, S, d,
+                              _ptr(out), _ptr(lse), _stream(o_partial)), lib)
+    return out

@@ -1,0 +1,264 @@
+// The C ABI of libpa (declared in include/pa.h): argument validation on the
+// host, error reporting, and dispatch to the kernels.  Nothing here touches
+// device memory except pa_device_error (which reads the error words) and no
+// call allocates memory.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+thread_local char g_last_error[512] = "";
+
+pa_status fail(pa_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+pa_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int g_sms[64] = {0};
+std::mutex g_sms_lock;
+
+// Shared checks of the head geometry.
+pa_status check_heads(int32_t hq, int32_t hkv, int32_t d, int32_t page_size) {
+    if (hq <= 0 || hkv <= 0) return fail(PA_ERR_INVALID, "head counts must be positive (Hq=%d, Hkv=%d)", hq, hkv);
+    if (hq % hkv != 0) return fail(PA_ERR_INVALID, "num_q_heads %% num_kv_heads != 0 (Hq=%d, Hkv=%d)", hq, hkv);
+    const int g = hq / hkv;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return fail(PA_ERR_UNSUPPORTED, "GQA group size %d not in {1,2,4,8}", g);
+    if (d != 64 && d != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64,128}", d);
+    if (page_size != 1 && page_size != 16)
+        return fail(PA_ERR_UNSUPPORTED, "page_size %d not in {1,16}", page_size);
+    if ((int64_t)hkv * d > 4096) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads * head_dim > 4096");
+    return PA_OK;
+}
+}  // namespace
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
+    std::lock_guard<std::mutex> lk(g_sms_lock);
+    if (g_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 132;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_abi_version(void) { return PA_ABI_VERSION; }
+
+const char *pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_DEVICE: return "device-side metadata error";
+        default: return "unknown status";
+    }
+}
+
+const char *pa_last_error(void) { return pa::g_last_error; }
+
+pa_status pa_device_error(int32_t *bits, void *stream) {
+    if (bits == nullptr) return fail(PA_ERR_INVALID, "bits is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t (*getters[])(int **) = {error_word_store, error_word_decode, error_word_prefill};
+    int32_t acc = 0;
+    for (auto get : getters) {
+        int *addr = nullptr;
+        cudaError_t e = get(&addr);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        int32_t v = 0;
+        e = cudaMemcpyAsync(&v, addr, sizeof v, cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(addr, 0, sizeof(int), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+        acc |= v;
+    }
+    *bits = acc;
+    return PA_OK;
+}
+
+pa_status pa_store_kv(const void *k, const void *v, const int32_t *slot_mapping, int64_t num_tokens,
+                      void *k_cache, void *v_cache, int64_t num_slots, int32_t num_kv_heads,
+                      int32_t head_dim, void *stream) {
+    g_last_error[0] = 0;
+    if (num_tokens < 0 || num_slots < 0) return fail(PA_ERR_INVALID, "negative num_tokens or num_slots");
+    if (num_kv_heads <= 0 || head_dim <= 0) return fail(PA_ERR_INVALID, "num_kv_heads and head_dim must be positive");
+    const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * 2;
+    if (row_bytes % 16 != 0) return fail(PA_ERR_UNSUPPORTED, "K/V row of %lld bytes is not a multiple of 16", (long long)row_bytes);
+    if (row_bytes > (1 << 20)) return fail(PA_ERR_UNSUPPORTED, "K/V row too large");
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return fail(PA_ERR_INVALID, "NULL pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID, "K/V pointers must be 16-byte aligned");
+    cudaError_t e = launch_store_kv(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_slots,
+                                    (int32_t)row_bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "store_kv launch");
+}
+
+pa_status pa_build_seqlens(const int32_t *cached_len, const int32_t *extend_len, int32_t num_seqs,
+                           int32_t *cu_seqlens_q, int32_t *cu_seqlens_k, int32_t *cache_seqlens,
+                           int32_t *max_seqlen_q, int32_t *max_seqlen_k) {
+    g_last_error[0] = 0;
+    if (num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs < 0");
+    if (!cu_seqlens_q || !cu_seqlens_k || !max_seqlen_q || !max_seqlen_k || (num_seqs > 0 && (!cached_len || !extend_len || !cache_seqlens)))
+        return fail(PA_ERR_INVALID, "NULL pointer");
+    int64_t sq = 0, sk = 0;
+    int32_t mq = 0, mk = 0;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        if (cached_len[b] < 0 || extend_len[b] < 0) return fail(PA_ERR_INVALID, "negative length at request %d", b);
+        const int64_t lk = (int64_t)cached_len[b] + extend_len[b];
+        if (lk > INT32_MAX) return fail(PA_ERR_INVALID, "device_len overflows int32 at request %d", b);
+        if (extend_len[b] > mq) mq = extend_len[b];
+        if (lk > mk) mk = (int32_t)lk;
+        sq += extend_len[b];
+        sk += lk;
+        if (sq > INT32_MAX || sk > INT32_MAX) return fail(PA_ERR_INVALID, "cumulative length overflows int32");
+    }
+    // write only after validation succeeded
+    int64_t aq = 0, ak = 0;
+    cu_seqlens_q[0] = 0;
+    cu_seqlens_k[0] = 0;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        const int32_t lk = cached_len[b] + extend_len[b];
+        aq += extend_len[b];
+        ak += lk;
+        cu_seqlens_q[b + 1] = (int32_t)aq;
+        cu_seqlens_k[b + 1] = (int32_t)ak;
+        cache_seqlens[b] = lk;
+    }
+    *max_seqlen_q = mq;
+    *max_seqlen_k = mk;
+    return PA_OK;
+}
+
+pa_status pa_build_page_table(const int32_t *token_table, int64_t token_table_stride,
+                              const int32_t *table_idx, int32_t num_seqs, int32_t max_seqlen_k,
+                              int32_t page_size, int32_t *page_table, int32_t page_table_stride,
+                              void *stream) {
+    g_last_error[0] = 0;
+    if (num_seqs < 0 || max_seqlen_k < 0) return fail(PA_ERR_INVALID, "negative num_seqs or max_seqlen_k");
+    if (page_size <= 0) return fail(PA_ERR_INVALID, "page_size must be positive");
+    const int64_t ncols = ((int64_t)max_seqlen_k + page_size - 1) / page_size;
+    if (ncols > page_table_stride) return fail(PA_ERR_INVALID, "page_table_stride %d < %lld columns", page_table_stride, (long long)ncols);
+    if ((int64_t)(ncols - 1) * page_size >= token_table_stride && ncols > 0)
+        return fail(PA_ERR_INVALID, "token_table_stride %lld too small for max_seqlen_k %d", (long long)token_table_stride, max_seqlen_k);
+    if (num_seqs == 0 || ncols == 0) return PA_OK;
+    if (!token_table || !table_idx || !page_table) return fail(PA_ERR_INVALID, "NULL pointer");
+    cudaError_t e = launch_build_page_table(token_table, token_table_stride, table_idx, num_seqs,
+                                            (int32_t)ncols, page_size, page_table, page_table_stride,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "build_page_table launch");
+}
+
+pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
+    g_last_error[0] = 0;
+    if (p == nullptr) return fail(PA_ERR_INVALID, "params is NULL");
+    pa_status st = check_heads(p->num_q_heads, p->num_kv_heads, p->head_dim, p->page_size);
+    if (st != PA_OK) return st;
+    if (p->head_dim != 128 && p->head_dim != 64) return fail(PA_ERR_UNSUPPORTED, "prefill head_dim");
+    if (p->num_seqs < 0 || p->max_seqlen_q < 0 || p->max_seqlen_k < 0 || p->num_pages <= 0)
+        return fail(PA_ERR_INVALID, "negative sizes or empty pool");
+    if (p->max_seqlen_q > p->max_seqlen_k && p->max_seqlen_k > 0)
+        return fail(PA_ERR_INVALID, "max_seqlen_q %d > max_seqlen_k %d", p->max_seqlen_q, p->max_seqlen_k);
+    if (p->causal != 0 && p->causal != 1) return fail(PA_ERR_INVALID, "causal must be 0 or 1");
+    if (!(p->scale == p->scale)) return fail(PA_ERR_INVALID, "scale is NaN");
+    if (p->num_seqs == 0 || p->max_seqlen_q == 0) return PA_OK;
+    const int64_t ncols = ((int64_t)p->max_seqlen_k + p->page_size - 1) / p->page_size;
+    if (p->page_table_stride < ncols) return fail(PA_ERR_INVALID, "page_table_stride too small for max_seqlen_k");
+    if (!p->q || !p->k_cache || !p->v_cache || !p->page_table || !p->cu_seqlens_q || !p->cu_seqlens_k || !p->out)
+        return fail(PA_ERR_INVALID, "NULL pointer");
+    if (!aligned16(p->q) || !aligned16(p->k_cache) || !aligned16(p->v_cache) || !aligned16(p->out))
+        return fail(PA_ERR_INVALID, "q, caches and out must be 16-byte aligned");
+    if (p->lse != nullptr && p->lse_stride <= 0) return fail(PA_ERR_INVALID, "lse_stride must be positive");
+    if (p->num_pages > (int64_t)INT32_MAX / p->page_size)
+        return fail(PA_ERR_UNSUPPORTED, "pool larger than 2^31 slots");
+    cudaError_t e = launch_prefill(*p, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "prefill configuration not supported by this build");
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "prefill launch");
+}
+
+static pa_status check_decode(const pa_decode_params *p) {
+    if (p == nullptr) return fail(PA_ERR_INVALID, "params is NULL");
+    pa_status st = check_heads(p->num_q_heads, p->num_kv_heads, p->head_dim, p->page_size);
+    if (st != PA_OK) return st;
+    if (p->num_seqs < 0 || p->max_seqlen_k < 0 || p->num_pages <= 0)
+        return fail(PA_ERR_INVALID, "negative sizes or empty pool");
+    if (p->num_seqs > 16384) return fail(PA_ERR_UNSUPPORTED, "more than 16384 sequences in one decode call");
+    if (p->kv_chunk < 0 || p->kv_chunk % 16 != 0) return fail(PA_ERR_INVALID, "kv_chunk must be a non-negative multiple of 16");
+    if (!(p->scale == p->scale)) return fail(PA_ERR_INVALID, "scale is NaN");
+    if (p->num_pages > (int64_t)INT32_MAX / p->page_size)
+        return fail(PA_ERR_UNSUPPORTED, "pool larger than 2^31 slots");
+    return PA_OK;
+}
+
+size_t pa_decode_workspace_size(const pa_decode_params *p) {
+    if (check_decode(p) != PA_OK) return 0;
+    return plan_decode(*p).workspace_bytes;
+}
+
+int32_t pa_decode_kv_chunk(const pa_decode_params *p) {
+    if (check_decode(p) != PA_OK) return 0;
+    return plan_decode(*p).kv_chunk;
+}
+
+pa_status pa_decode(const pa_decode_params *p, void *stream) {
+    g_last_error[0] = 0;
+    pa_status st = check_decode(p);
+    if (st != PA_OK) return st;
+    if (p->num_seqs == 0) return PA_OK;
+    const int64_t ncols = ((int64_t)p->max_seqlen_k + p->page_size - 1) / p->page_size;
+    if (p->page_table_stride < ncols) return fail(PA_ERR_INVALID, "page_table_stride too small for max_seqlen_k");
+    if (!p->q || !p->k_cache || !p->v_cache || !p->page_table || !p->cache_seqlens || !p->out)
+        return fail(PA_ERR_INVALID, "NULL pointer");
+    if (!aligned16(p->q) || !aligned16(p->k_cache) || !aligned16(p->v_cache) || !aligned16(p->out))
+        return fail(PA_ERR_INVALID, "q, caches and out must be 16-byte aligned");
+    const DecodePlan plan = plan_decode(*p);
+    if (plan.workspace_bytes > 0) {
+        if (p->workspace == nullptr || p->workspace_bytes < plan.workspace_bytes)
+            return fail(PA_ERR_INVALID, "workspace of %zu bytes needed, %zu given", plan.workspace_bytes, p->workspace_bytes);
+        if (!aligned16(p->workspace)) return fail(PA_ERR_INVALID, "workspace must be 16-byte aligned");
+    }
+    cudaError_t e = launch_decode(*p, plan, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "decode launch");
+}
+
+pa_status pa_lse_combine(const float *o_partial, const float *lse_partial, const int32_t *splits_per_row,
+                         int32_t num_rows, int32_t max_splits, int32_t head_dim, void *out, float *lse_out,
+                         void *stream) {
+    g_last_error[0] = 0;
+    if (num_rows < 0 || max_splits < 0) return fail(PA_ERR_INVALID, "negative num_rows or max_splits");
+    if (head_dim != 64 && head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64,128}", head_dim);
+    if (num_rows == 0) return PA_OK;
+    if (!out || (max_splits > 0 && (!o_partial || !lse_partial))) return fail(PA_ERR_INVALID, "NULL pointer");
+    if (!aligned16(o_partial) || !aligned16(out)) return fail(PA_ERR_INVALID, "o_partial and out must be 16-byte aligned");
+    cudaError_t e = launch_lse_combine(o_partial, lse_partial, splits_per_row, nullptr, 1, 1, num_rows,
+                                       max_splits, head_dim, out, lse_out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "lse_combine launch");
+}
+
+}  // extern "C"

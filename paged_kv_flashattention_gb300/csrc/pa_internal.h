@@ -1,0 +1,46 @@
+// Host-side launch functions behind the C ABI (validated arguments only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+cudaError_t launch_store_kv(const void *k, const void *v, const int32_t *slot_mapping,
+                            int64_t num_tokens, void *k_cache, void *v_cache, int64_t num_slots,
+                            int32_t row_bytes, cudaStream_t stream);
+
+cudaError_t launch_build_page_table(const int32_t *token_table, int64_t tt_stride,
+                                    const int32_t *table_idx, int32_t num_seqs, int32_t ncols,
+                                    int32_t page_size, int32_t *page_table, int32_t pt_stride,
+                                    cudaStream_t stream);
+
+// Decode plan: keys per split, splits of the longest sequence, KV heads per CTA.
+struct DecodePlan {
+    int32_t kv_chunk;
+    int32_t max_splits;
+    int32_t heads_per_cta;
+    size_t workspace_bytes;
+};
+DecodePlan plan_decode(const pa_decode_params &p);
+cudaError_t launch_decode(const pa_decode_params &p, const DecodePlan &plan, cudaStream_t stream);
+
+cudaError_t launch_lse_combine(const float *o_partial, const float *lse_partial,
+                               const int32_t *splits_per_row, const int32_t *cache_seqlens,
+                               int32_t kv_chunk, int32_t heads_per_seq, int32_t num_rows,
+                               int32_t max_splits, int32_t head_dim, void *out, float *lse_out,
+                               cudaStream_t stream);
+
+cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream);
+
+int num_sms();
+
+// Device addresses of each translation unit's error word.
+cudaError_t error_word_store(int **addr);
+cudaError_t error_word_decode(int **addr);
+cudaError_t error_word_prefill(int **addr);
+
+}  // namespace pa
