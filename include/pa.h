@@ -145,6 +145,7 @@ typedef struct {
     const void *v_cache;
     const int32_t *page_table;   /* int32 [num_seqs, page_table_stride] */
     int32_t page_table_stride;
+    int32_t total_q;             /* rows of q and out (>= cu_seqlens_q[num_seqs]) */
     const int32_t *cu_seqlens_q; /* int32 [num_seqs + 1] */
     const int32_t *cu_seqlens_k; /* int32 [num_seqs + 1] */
     int32_t num_seqs;

@@ -26,7 +26,7 @@ c_size = ctypes.c_size_t
 class PrefillParams(ctypes.Structure):
     _fields_ = [
         ("q", c_p), ("k_cache", c_p), ("v_cache", c_p),
-        ("page_table", c_p), ("page_table_stride", c_i32),
+        ("page_table", c_p), ("page_table_stride", c_i32), ("total_q", c_i32),
         ("cu_seqlens_q", c_p), ("cu_seqlens_k", c_p),
         ("num_seqs", c_i32), ("max_seqlen_q", c_i32), ("max_seqlen_k", c_i32),
         ("num_q_heads", c_i32), ("num_kv_heads", c_i32), ("head_dim", c_i32),

@@ -166,7 +166,7 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
             raise ValueError("lse must be [Hq, >= total_q] with unit inner stride")
     p = _lib.PrefillParams(
         q=_ptr(q), k_cache=_ptr(k_cache), v_cache=_ptr(v_cache), page_table=_ptr(page_table),
-        page_table_stride=page_table.stride(0), cu_seqlens_q=_ptr(cu_seqlens_q),
+        page_table_stride=page_table.stride(0), total_q=total_q, cu_seqlens_q=_ptr(cu_seqlens_q),
         cu_seqlens_k=_ptr(cu_seqlens_k), num_seqs=cu_seqlens_q.numel() - 1,
         max_seqlen_q=int(max_seqlen_q), max_seqlen_k=int(max_seqlen_k), num_q_heads=Hq,
         num_kv_heads=Hkv, head_dim=d, page_size=P, num_pages=num_pages, causal=int(bool(causal)),

@@ -187,9 +187,11 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
         return fail(PA_ERR_INVALID, "max_seqlen_q %d > max_seqlen_k %d", p->max_seqlen_q, p->max_seqlen_k);
     if (p->causal != 0 && p->causal != 1) return fail(PA_ERR_INVALID, "causal must be 0 or 1");
     if (!(p->scale == p->scale)) return fail(PA_ERR_INVALID, "scale is NaN");
-    if (p->num_seqs == 0 || p->max_seqlen_q == 0) return PA_OK;
+    if (p->total_q < 0) return fail(PA_ERR_INVALID, "total_q < 0");
+    if (p->num_seqs == 0 || p->max_seqlen_q == 0 || p->total_q == 0) return PA_OK;
     const int64_t ncols = ((int64_t)p->max_seqlen_k + p->page_size - 1) / p->page_size;
     if (p->page_table_stride < ncols) return fail(PA_ERR_INVALID, "page_table_stride too small for max_seqlen_k");
+    if (p->lse != nullptr && p->lse_stride < p->total_q) return fail(PA_ERR_INVALID, "lse_stride < total_q");
     if (!p->q || !p->k_cache || !p->v_cache || !p->page_table || !p->cu_seqlens_q || !p->cu_seqlens_k || !p->out)
         return fail(PA_ERR_INVALID, "NULL pointer");
     if (!aligned16(p->q) || !aligned16(p->k_cache) || !aligned16(p->v_cache) || !aligned16(p->out))

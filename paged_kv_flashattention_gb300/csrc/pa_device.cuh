@@ -1,7 +1,8 @@
 // Device-side helpers shared by the kernels of libpa: bf16 packing, the
 // device error word, mbarrier / bulk-copy / TMA / tcgen05 wrappers written as
-// inline PTX for sm_103a.  Every wait here is bounded: after kSpinLimit polls
-// it raises PA_DEVERR_TIMEOUT and returns false so the kernel can unwind.
+// inline PTX for sm_103a.  Every wait here is bounded (about one second of
+// wall time): it then raises PA_DEVERR_TIMEOUT and returns false so the
+// kernel can unwind.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -22,8 +23,7 @@ static __device__ int g_device_error = 0;
 
 __device__ __forceinline__ void raise_error(int bits) { atomicOr(&g_device_error, bits); }
 
-// Bounded spin: ~2^26 polls of a try_wait (each may itself block for a
-// hardware-chosen interval) is far beyond any legitimate wait.
+// Hard cap on polls, a second guard behind the wall-time limit below.
 constexpr uint32_t kSpinLimit = 1u << 26;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -90,10 +90,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 // Wait for the phase with the given parity to complete; false on timeout.
+// The limit is wall time (kWaitLimitNs of the global timer), checked every
+// 256 polls, so a wait that can never finish ends within about a second.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) break;
+    }
     raise_error(PA_DEVERR_TIMEOUT);
     return false;
 }

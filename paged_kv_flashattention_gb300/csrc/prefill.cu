@@ -1,4 +1,40 @@
-// Varlen prefill / extend attention (tcgen05 + TMEM).  Placeholder.
+// Varlen causal prefill / extend attention over a paged KV cache on the
+// 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// "Transformer inference kernels: GEMM·Attention·FlashAttention·Fusion
+// (3/10)": attention is computed tile by tile so the score matrix never
+// reaches HBM (section 11), with the online softmax merge of section 12; keys
+// are read through the page table (section 14), several query heads share a
+// KV head (section 15), and the causal window of a request with a cached
+// prefix is aligned to the end of its keys ("code-series sgl-project
+// mini-sglang 07": seqlens_q = extend_len, seqlens_k = device_len).
+//
+// GB300 design (prior art on the pages is Hopper/Ampere; this is not it):
+// one CTA = one 128-row query tile of one query head of one request.
+//   warp 4 (producer): TMA loads the Q tile once (two 64-column halves,
+//     128-byte swizzle, K-major), then per 128-key step the K and V tiles:
+//     page size 16 -> one 3-D TMA box of 16 tokens per page and half;
+//     page size 1  -> cp.async 16-byte rows placed in the same swizzled
+//     layout.  A two-stage ring; pages past the request's keys are filled
+//     with zeros by out-of-range TMA coordinates.
+//   warp 5 (MMA): one thread issues tcgen05.mma.  S_j = Q K_j^T (SS form,
+//     both K-major) into one of two 128-column TMEM buffers, so S_{j+1} is
+//     computed while the softmax works on S_j; then O += P_j V_j with P_j
+//     read from TMEM (TS form) and V_j MN-major in shared memory.
+//   warps 0-3 (softmax): thread r owns query row r = TMEM lane r.  It loads
+//     its S row with tcgen05.ld, applies scale * log2(e), the causal and
+//     length masks, updates the running maximum lazily (only when the tile
+//     maximum exceeds it by more than 8, i.e. 2^8 headroom; then O in TMEM is
+//     rescaled by exp2(m_old - m_new)), writes P as bf16 back over its S
+//     columns with tcgen05.st, and finally normalises O and writes bf16
+//     output and the natural-log LSE.
+// TMEM: S0 = columns [0,128), S1 = [128,256), O = [256, 256 + d).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -6,6 +42,406 @@ namespace pa {
 
 PA_ERROR_WORD_ACCESSOR(error_word_prefill)
 
-cudaError_t launch_prefill(const pa_prefill_params &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kBM = 128;          // query rows per tile
+constexpr int kBN = 128;          // keys per step
+constexpr int kKVStages = 2;
+constexpr int kThreads = 192;     // 4 softmax warps + producer + MMA
+constexpr float kLazy = 8.0f;
+
+struct PrefillArgs {
+    CUtensorMap qmap;             // bf16 (d, Hq, total_q), box (64, 1, 128)
+    CUtensorMap kmap;             // bf16 (d, Hkv, num_slots), box (64, 1, 16)
+    CUtensorMap vmap;
+    const uint8_t *k_cache;       // for page size 1 (row gathers)
+    const uint8_t *v_cache;
+    const int32_t *page_table;
+    int64_t pt_stride;
+    const int32_t *cu_q;
+    const int32_t *cu_k;
+    __nv_bfloat16 *out;
+    float *lse;
+    int64_t lse_stride;
+    int32_t num_seqs;
+    int32_t total_q;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t page_size;
+    int32_t num_slots;
+    int32_t causal;
+    float scale_log2;
+};
+
+template <int D>
+struct PrefillSmem {
+    static constexpr int kHalves = D / 64;                 // 64-column (128-byte) halves
+    static constexpr int kTileBytes = kHalves * 128 * 128; // 128 rows x D bf16
+    static constexpr int kQ = 0;
+    static constexpr int kKV = kTileBytes;                  // stage s: K at kKV + s*2*tile, V after
+    static constexpr int kBars = kKV + kKVStages * 2 * kTileBytes;
+    static constexpr int kTotal = kBars + 256;
+};
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
+    using S = PrefillSmem<D>;
+    constexpr int H = S::kHalves;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int tile = blockIdx.x;
+    const int h = blockIdx.y;
+    const int b = blockIdx.z;
+    const int q0 = a.cu_q[b];
+    const int Lq = a.cu_q[b + 1] - q0;
+    const int Lk = a.cu_k[b + 1] - a.cu_k[b];
+    if (tile * kBM >= Lq) return;                     // uniform per CTA
+    const int kvh = h / (a.num_q_heads / a.num_kv_heads);
+    const int off = Lk - Lq;                          // cached prefix length
+    const int rows_here = min(kBM, Lq - tile * kBM);
+    // keys this tile can see
+    int kv_end = Lk;
+    if (a.causal) kv_end = min(Lk, off + tile * kBM + rows_here);
+    if (kv_end < 0) kv_end = 0;
+    const int n_kv = (kv_end + kBN - 1) / kBN;
+
+    uint8_t *sQ = smem + S::kQ;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBars);
+    uint64_t *q_full = bars;                 // 1
+    uint64_t *kv_full = bars + 1;            // kKVStages
+    uint64_t *kv_empty = bars + 3;           // kKVStages
+    uint64_t *s_full = bars + 5;             // 2
+    uint64_t *p_full = bars + 7;             // 2
+    uint64_t *pv_done = bars + 9;            // 1: one phase per P.V step
+    uint64_t *o_final = bars + 10;           // 1: the last P.V (and all before it) done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const bool paged16 = (a.page_size == 16);
+
+    if (warp == 5) tmem_alloc(tmem_slot, 512);
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kKVStages; ++s) {
+            mbar_init(&kv_full[s], paged16 ? 1 : 32);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_full[s], 128);
+        }
+        mbar_init(pv_done, 1);
+        mbar_init(o_final, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tO = tmem + 256;
+
+    if (warp == 4) {
+        // ----------------------------------------------------- producer ----
+        const int32_t *pt = a.page_table + (int64_t)b * a.pt_stride;
+        if (lane == 0) {
+            prefetch_tmap(&a.qmap);
+            if (paged16) { prefetch_tmap(&a.kmap); prefetch_tmap(&a.vmap); }
+            mbar_arrive_expect_tx(q_full, S::kTileBytes);
+            for (int hh = 0; hh < H; ++hh)
+                tma_load_3d(sQ + hh * 16384, &a.qmap, hh * 64, h, q0 + tile * kBM, q_full);
+        }
+        for (int j = 0; j < n_kv; ++j) {
+            const int st = j % kKVStages;
+            if (j >= kKVStages && !mbar_wait(&kv_empty[st], ((j / kKVStages) - 1) & 1)) break;
+            uint8_t *sK = smem + S::kKV + st * 2 * S::kTileBytes;
+            uint8_t *sV = sK + S::kTileBytes;
+            const int key0 = j * kBN;
+            if (paged16) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&kv_full[st], 2 * S::kTileBytes);
+                    for (int pg = 0; pg < kBN / 16; ++pg) {
+                        const int kk = key0 + pg * 16;
+                        int slot0 = a.num_slots;            // out of range: zero fill
+                        if (kk < kv_end) {
+                            const int page = pt[kk / 16];
+                            if (page >= 0 && (int64_t)page * 16 < a.num_slots) slot0 = page * 16;
+                            else raise_error(PA_DEVERR_PAGE_RANGE);
+                        }
+                        for (int hh = 0; hh < H; ++hh) {
+                            tma_load_3d(sK + hh * 16384 + pg * 2048, &a.kmap, hh * 64, kvh, slot0, &kv_full[st]);
+                            tma_load_3d(sV + hh * 16384 + pg * 2048, &a.vmap, hh * 64, kvh, slot0, &kv_full[st]);
+                        }
+                    }
+                }
+            } else {
+                // page size 1: each lane gathers 4 key rows with cp.async,
+                // writing the 128-byte-swizzled layout TMA would produce
+                for (int rr = 0; rr < kBN / 32; ++rr) {
+                    const int r = rr * 32 + lane;
+                    const int key = key0 + r;
+                    int64_t slot = -1;
+                    if (key < kv_end) {
+                        slot = pt[key];
+                        if (slot < 0 || slot >= a.num_slots) { raise_error(PA_DEVERR_PAGE_RANGE); slot = -1; }
+                    }
+                    for (int hh = 0; hh < H; ++hh) {
+                        for (int c = 0; c < 8; ++c) {
+                            const int so = hh * 16384 + r * 128 + ((c ^ (r & 7)) * 16);
+                            if (slot >= 0) {
+                                const int64_t go = (slot * a.num_kv_heads + kvh) * (int64_t)D * 2 + hh * 128 + c * 16;
+                                cp_async16(sK + so, a.k_cache + go);
+                                cp_async16(sV + so, a.v_cache + go);
+                            } else {
+                                *reinterpret_cast<uint4 *>(sK + so) = make_uint4(0, 0, 0, 0);
+                                *reinterpret_cast<uint4 *>(sV + so) = make_uint4(0, 0, 0, 0);
+                            }
+                        }
+                    }
+                }
+                cp_async_commit();
+                cp_async_wait_all();
+                fence_proxy_async_smem();      // make generic-proxy writes visible to the MMA
+                mbar_arrive(&kv_full[st]);
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------------------------------------------------- MMA ----
+        if (lane == 0 && n_kv > 0) {
+            constexpr uint32_t idesc_s = umma_idesc_bf16(kBM, kBN, false);
+            constexpr uint32_t idesc_o = umma_idesc_bf16(kBM, D, true);
+            bool ok = mbar_wait(q_full, 0);
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % kKVStages;
+                if (!mbar_wait(&kv_full[st], (j / kKVStages) & 1)) return false;
+                tc_fence_after();
+                const uint8_t *sK = smem + S::kKV + st * 2 * S::kTileBytes;
+                const uint32_t dst = tmem + (j & 1) * 128;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t qa = smem_u32(sQ + (k / 4) * 16384 + (k % 4) * 32);
+                    const uint32_t ka = smem_u32(sK + (k / 4) * 16384 + (k % 4) * 32);
+                    umma_ss(dst, umma_desc_sw128(qa, 16, 1024), umma_desc_sw128(ka, 16, 1024), idesc_s, k > 0);
+                }
+                umma_commit(&s_full[j & 1]);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                if (j + 1 < n_kv) {
+                    // S buffer (j+1)&1 held P_{j-1}: its PV must have finished
+                    if (j >= 1 && !mbar_wait(pv_done, (j - 1) & 1)) { ok = false; break; }
+                    if (!issue_s(j + 1)) { ok = false; break; }
+                }
+                if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const int st = j % kKVStages;
+                const uint8_t *sV = smem + S::kKV + st * 2 * S::kTileBytes + S::kTileBytes;
+                const uint32_t pa_tm = tmem + (j & 1) * 128;
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k) {
+                    const uint32_t va = smem_u32(sV + k * 16 * 128);
+                    umma_ts(tO, pa_tm + k * 8, umma_desc_sw128(va, 16384, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+                }
+                umma_commit(pv_done);
+                umma_commit(&kv_empty[st]);
+                if (j == n_kv - 1) umma_commit(o_final);
+            }
+        }
+    } else {
+        // ------------------------------------------------------ softmax ----
+        const int r = threadIdx.x;                    // row within the tile = TMEM lane
+        const int qi = tile * kBM + r;                // query index within the request
+        const bool row_valid = r < rows_here;
+        const int vis_end = a.causal ? min(Lk, off + qi + 1) : Lk;   // keys [0, vis_end)
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        float m_run = -INFINITY;
+        float l_run = 0.f;
+        bool ok = true;
+        // tcgen05.ld / st are warp-collective (.sync.aligned): every branch
+        // that encloses one is made warp-uniform, and the warp reconverges
+        // after each (per-lane) barrier wait.
+        for (int j = 0; j < n_kv; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t sb = tmem + lane_base + (j & 1) * 128;
+            uint32_t sr[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) tmem_ld32(sb + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+            tmem_wait_ld();
+            const int kbase = j * kBN;
+            const int lim = row_valid ? vis_end - kbase : 0;   // columns < lim are visible
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) {
+                float x = __uint_as_float(sr[c]) * a.scale_log2;
+                x = (c < lim) ? x : -INFINITY;
+                sr[c] = __float_as_uint(x);
+                mt = fmaxf(mt, x);
+            }
+            // lazy maximum: move it only when the tile maximum exceeds it by
+            // more than kLazy; then O (after P.V_{j-1}) and l are rescaled
+            const bool need = mt > m_run + kLazy;
+            const float alpha = need ? fast_exp2(m_run - mt) : 1.f;
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(tO + lane_base + c * 32, orr);
+                    tmem_wait_ld();
+                    uint32_t w0[16], w1[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        w0[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                        w1[e] = __float_as_uint(__uint_as_float(orr[16 + e]) * alpha);
+                    }
+                    tmem_st16(tO + lane_base + c * 32, w0);
+                    tmem_st16(tO + lane_base + c * 32 + 16, w1);
+                }
+            }
+            if (need) {
+                l_run *= alpha;
+                m_run = mt;
+            }
+            const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+            float psum = 0.f;
+            uint32_t pk[kBN / 2];
+#pragma unroll
+            for (int c = 0; c < kBN / 2; ++c) {
+                const float p0 = fast_exp2(__uint_as_float(sr[2 * c]) - m_use);
+                const float p1 = fast_exp2(__uint_as_float(sr[2 * c + 1]) - m_use);
+                psum += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l_run += psum;
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c)
+                tmem_st16(sb + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[j & 1]);
+        }
+        // ---- epilogue: O / l -> bf16, lse.  Up to two P.V phases may still
+        // be pending here, which one parity bit cannot tell apart, so the
+        // last P.V signals its own barrier.
+        if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0));
+        tc_fence_after();
+        if (ok) {
+            const int64_t tok = (int64_t)q0 + qi;
+            __nv_bfloat16 *orow = a.out + (tok * a.num_q_heads + h) * D;
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t orr[32];
+                if (n_kv > 0) {                       // CTA-uniform
+                    tmem_ld32(tO + lane_base + c * 32, orr);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) orr[e] = 0u;
+                }
+                if (row_valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
+                        dst[v] = w;
+                    }
+                }
+            }
+            if (row_valid && a.lse != nullptr)
+                a.lse[(int64_t)h * a.lse_stride + tok] =
+                    l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        __syncwarp();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 map (d, heads, rows) with a (64, 1, box_rows) box, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, int d, int heads, int64_t rows, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_t(const PrefillArgs &a, dim3 grid, cudaStream_t stream) {
+    using S = PrefillSmem<D>;
+    // Reserve enough shared memory that one CTA holds an SM (TMEM: 512 columns).
+    const int smem = (S::kTotal + 1024) > 120 * 1024 ? (S::kTotal + 1024) : 120 * 1024;
+    auto kern = prefill_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
+    PrefillArgs a{};
+    const int64_t num_slots = p.num_pages * p.page_size;
+    if (!make_map(&a.qmap, p.q, p.head_dim, p.num_q_heads, p.total_q, kBM)) return cudaErrorNotSupported;
+    if (p.page_size == 16) {
+        if (!make_map(&a.kmap, p.k_cache, p.head_dim, p.num_kv_heads, num_slots, 16)) return cudaErrorNotSupported;
+        if (!make_map(&a.vmap, p.v_cache, p.head_dim, p.num_kv_heads, num_slots, 16)) return cudaErrorNotSupported;
+    }
+    a.k_cache = static_cast<const uint8_t *>(p.k_cache);
+    a.v_cache = static_cast<const uint8_t *>(p.v_cache);
+    a.page_table = p.page_table;
+    a.pt_stride = p.page_table_stride;
+    a.cu_q = p.cu_seqlens_q;
+    a.cu_k = p.cu_seqlens_k;
+    a.out = static_cast<__nv_bfloat16 *>(p.out);
+    a.lse = p.lse;
+    a.lse_stride = p.lse_stride;
+    a.num_seqs = p.num_seqs;
+    a.total_q = p.total_q;
+    a.num_q_heads = p.num_q_heads;
+    a.num_kv_heads = p.num_kv_heads;
+    a.page_size = p.page_size;
+    a.num_slots = (int32_t)num_slots;
+    a.causal = p.causal;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    dim3 grid((p.max_seqlen_q + kBM - 1) / kBM, p.num_q_heads, p.num_seqs);
+    if (grid.y > 65535 || grid.z > 65535) return cudaErrorNotSupported;
+    return p.head_dim == 128 ? launch_t<128>(a, grid, stream) : launch_t<64>(a, grid, stream);
+}
 
 }  // namespace pa

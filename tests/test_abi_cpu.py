@@ -70,7 +70,7 @@ def test_build_seqlens_edges(lib):
 def _prefill(lib, **kw):
     from paged_kv_flashattention_gb300 import _lib
     base = dict(q=0x1000, k_cache=0x2000, v_cache=0x3000, page_table=0x4000, page_table_stride=64,
-                cu_seqlens_q=0x5000, cu_seqlens_k=0x6000, num_seqs=2, max_seqlen_q=16,
+                total_q=64, cu_seqlens_q=0x5000, cu_seqlens_k=0x6000, num_seqs=2, max_seqlen_q=16,
                 max_seqlen_k=32, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
                 num_pages=100, causal=1, scale=0.1, out=0x7000, lse=None, lse_stride=0)
     base.update(kw)
