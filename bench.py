@@ -1,0 +1,453 @@
+"""Benchmark of the paged-KV attention path on one mixed continuous batch.
+
+One STEP is one pass of the whole path over one batch: the KV store of every
+new token (256 decode tokens + 2 x 2048 prefill tokens), the metadata of both
+sub-batches (host seqlens -> pinned, non-blocking H2D; page tables sliced on
+the device), causal prefill of the two 2048-token chunks, and split-KV decode
+(+ LSE combine) of 256 sequences with contexts log-uniform in [512, 32768]
+over a ~40 GB bf16 KV pool (Hq 32 / Hkv 8, d 128, page 16).
+
+value    = algorithmic bytes of the step (decode K/V + q/o, prefill Q/K/V/O,
+           store read+write) / device step time, in GB/s.  Inputs are resident
+           in HBM; the step's decode reads ~8 GB, far larger than L2.
+e2e      = the same bytes / step time through the public API with HOST
+           buffers: q, new K/V and slot mapping copied H2D from pinned memory
+           and both outputs copied back D2H inside the timed region.
+roofline = the decode pass (split kernel + combine) against measured HBM
+           bandwidth; prefill TFLOP/s against the measured bf16 peak is
+           reported beside it.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged-attn decode HBM GB/s; prefill TFLOP/s; fraction of GB300 roofline"
+WORKLOAD = ("mixed_batch_llama3_8b: 256 decode seqs (context log-uniform [512, 32768]) + "
+            "2 prefill chunks x 2048 (no cache hit), Hq 32 / Hkv 8, head_dim 128, page 16, "
+            "bf16 KV pool 2 x 20 GB, seeded permuted page tables")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def ncu_traffic(kernel_file: str, summary: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source changed since the capture (the summary records its hash)."""
+    try:
+        text = open(os.path.join(ROOT, "profiles", summary)).read()
+        want = re.search(r"source_sha256:\s*([0-9a-f]{64})", text).group(1)
+        bytes_ = float(re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", text).group(1))
+        src = open(os.path.join(ROOT, "paged_kv_flashattention_gb300", "csrc", kernel_file), "rb").read()
+        return bytes_ if hashlib.sha256(src).hexdigest() == want else None
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+class MixedBatch:
+    """Device state of the mixed-batch workload (pool, inputs, buffers)."""
+
+    def __init__(self, dev, seed_offset: int = 0):
+        import torch
+        import paged_kv_flashattention_gb300 as pa
+        self.torch, self.pa, self.dev = torch, pa, dev
+        cfg = W.config(5, with_data=False)
+        self.dec, self.pre = cfg["decode"], cfg["prefill"]
+        d, p = self.dec, self.pre
+        self.Hq, self.Hkv, self.D, self.P = d.num_q_heads, d.num_kv_heads, d.head_dim, d.page_size
+        shape = (d.num_pages, self.P, self.Hkv, self.D)
+        self.k_cache = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        self.v_cache = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        W.fill_normal_device(self.k_cache, W.SEED_BASE + 50 + seed_offset)
+        W.fill_normal_device(self.v_cache, W.SEED_BASE + 51 + seed_offset)
+        g = torch.Generator(device=dev)
+        g.manual_seed(W.SEED_BASE + 52 + seed_offset)
+        Tn = d.num_new_tokens + p.num_new_tokens
+        self.q_dec = torch.randn((d.num_seqs, self.Hq, self.D), generator=g, device=dev).to(torch.bfloat16)
+        self.q_pre = torch.randn((p.num_new_tokens, self.Hq, self.D), generator=g, device=dev).to(torch.bfloat16)
+        self.k_new = torch.randn((Tn, self.Hkv, self.D), generator=g, device=dev).to(torch.bfloat16)
+        self.v_new = torch.randn((Tn, self.Hkv, self.D), generator=g, device=dev).to(torch.bfloat16)
+        self.slot_mapping = torch.from_numpy(np.concatenate([d.slot_mapping, p.slot_mapping])).to(dev)
+        # global token-granular table: decode requests, then the prefill chunks
+        width = max(d.token_table.shape[1], p.token_table.shape[1])
+        tt = np.full((d.num_seqs + p.num_seqs, width), (d.num_pages - 1) * self.P, np.int32)
+        tt[:d.num_seqs, :d.token_table.shape[1]] = d.token_table
+        tt[d.num_seqs:, :p.token_table.shape[1]] = p.token_table
+        self.token_table = torch.from_numpy(tt).to(dev)
+        self.idx_dec = torch.arange(d.num_seqs, dtype=torch.int32, device=dev)
+        self.idx_pre = torch.arange(d.num_seqs, d.num_seqs + p.num_seqs, dtype=torch.int32, device=dev)
+        self.max_dec = int(d.device_len.max())
+        self.out_dec = torch.empty_like(self.q_dec)
+        self.out_pre = torch.empty_like(self.q_pre)
+        ws = pa.decode_workspace_size(self.q_dec.shape, self.k_cache, self.max_dec)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.pt_dec = torch.empty((d.num_seqs, -(-self.max_dec // self.P)), dtype=torch.int32, device=dev)
+        self.pt_pre = torch.empty((p.num_seqs, -(-int(p.device_len.max()) // self.P)), dtype=torch.int32,
+                                  device=dev)
+        # algorithmic work of one step
+        ctx = d.device_len.astype(np.int64)
+        self.decode_bytes = int(ctx.sum()) * self.Hkv * self.D * 2 * 2 + 2 * self.q_dec.numel() * 2
+        pairs = sum(int(L) * (int(L) + 1) // 2 for L in p.extend_len)
+        self.prefill_flops = 4 * self.D * self.Hq * pairs
+        self.prefill_bytes = 2 * self.q_pre.numel() * 2 + 2 * p.num_new_tokens * self.Hkv * self.D * 2
+        self.store_bytes = 2 * 2 * Tn * self.Hkv * self.D * 2
+        self.step_bytes = self.decode_bytes + self.prefill_bytes + self.store_bytes
+        self.launches_per_step = 6   # store, 2 page tables, prefill, decode split + combine
+        from paged_kv_flashattention_gb300.metadata import MetadataBuilder
+        self.meta_dec = MetadataBuilder(dev, d.num_seqs)
+        self.meta_pre = MetadataBuilder(dev, p.num_seqs)
+
+    def step(self, timing: bool = False):
+        torch, pa = self.torch, self.pa
+        ev = None
+        if timing:
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev[0].record()
+        pa.store_kv(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache)
+        md = self.meta_dec.prepare(self.dec.cached_len, self.dec.extend_len, self.token_table,
+                                   self.idx_dec, self.P, page_table_out=self.pt_dec)
+        mp = self.meta_pre.prepare(self.pre.cached_len, self.pre.extend_len, self.token_table,
+                                   self.idx_pre, self.P, page_table_out=self.pt_pre)
+        if timing:
+            ev[1].record()
+        pa.prefill(self.q_pre, self.k_cache, self.v_cache, mp.page_table, mp.cu_seqlens_q, mp.cu_seqlens_k,
+                   mp.max_seqlen_q, mp.max_seqlen_k, causal=True, out=self.out_pre)
+        if timing:
+            ev[2].record()
+        pa.decode(self.q_dec, self.k_cache, self.v_cache, md.page_table, md.cache_seqlens, md.max_seqlen_k,
+                  out=self.out_dec, workspace=self.workspace)
+        if timing:
+            ev[3].record()
+        self._keep = (md, mp)
+        return ev
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+
+    mb = MixedBatch(dev)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        mb.step()
+    barrier()
+    # ---- timed device steps (per-phase events recorded on the same stream)
+    phase = {"store_meta": [], "prefill": [], "decode": []}
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = []
+    with ClockSampler(local) as clk:
+        start.record()
+        for _ in range(args.steps):
+            evs.append(mb.step(timing=True))
+        end.record()
+        torch.cuda.synchronize()
+    barrier()
+    total_ms = start.elapsed_time(end)
+    for e in evs:
+        phase["store_meta"].append(e[0].elapsed_time(e[1]))
+        phase["prefill"].append(e[1].elapsed_time(e[2]))
+        phase["decode"].append(e[2].elapsed_time(e[3]))
+    t = torch.tensor([total_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step = float(t.item()) / args.steps
+    from paged_kv_flashattention_gb300 import device_error
+    dev_err = device_error()
+
+    # ---- end-to-end through the public API with host buffers
+    pin = lambda x: torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x.cpu())
+    h_qd, h_qp, h_k, h_v, h_sm = pin(mb.q_dec), pin(mb.q_pre), pin(mb.k_new), pin(mb.v_new), pin(mb.slot_mapping)
+    h_od = torch.empty(mb.out_dec.shape, dtype=mb.out_dec.dtype, pin_memory=True)
+    h_op = torch.empty(mb.out_pre.shape, dtype=mb.out_pre.dtype, pin_memory=True)
+    h2d = sum(x.numel() * x.element_size() for x in (h_qd, h_qp, h_k, h_v, h_sm))
+    d2h = h_od.numel() * h_od.element_size() + h_op.numel() * h_op.element_size()
+
+    def e2e_step():
+        mb.q_dec.copy_(h_qd, non_blocking=True)
+        mb.q_pre.copy_(h_qp, non_blocking=True)
+        mb.k_new.copy_(h_k, non_blocking=True)
+        mb.v_new.copy_(h_v, non_blocking=True)
+        mb.slot_mapping.copy_(h_sm, non_blocking=True)
+        mb.step()
+        h_od.copy_(mb.out_dec, non_blocking=True)
+        h_op.copy_(mb.out_pre, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    t2 = torch.tensor([s2.elapsed_time(e2)], device=dev)
+    if world > 1:
+        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
+    ms_e2e = float(t2.item()) / args.steps
+    h2d += 3 * 4 * (mb.dec.num_seqs + 1 + mb.pre.num_seqs + 1)   # metadata copies of both batches
+
+    dec_ms = statistics.mean(phase["decode"])
+    pre_ms = statistics.mean(phase["prefill"])
+    dec_gbs = mb.decode_bytes / (dec_ms * 1e-3) / 1e9
+    pre_tflops = mb.prefill_flops / (pre_ms * 1e-3) / 1e12
+    value = world * mb.step_bytes / (ms_step * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (decode reads "
+                   f"{mb.decode_bytes / 1e9:.2f} GB per step; no flush)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "step": "store_kv + metadata (2 batches) + prefill + decode(split+combine)",
+                   "step_bytes": mb.step_bytes},
+        "roofline": {"bound": "hbm", "kernel": "decode pass (split-KV kernel + LSE combine)",
+                     "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "peak_source": peak_src,
+                     "bytes_per_launch": mb.decode_bytes,
+                     "traffic": ncu_traffic("decode.cu", "decode_mixed_batch.md")},
+        "decode": {"ms": round(dec_ms, 4), "gbs": round(dec_gbs, 1),
+                   "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4),
+                   "frac_hbm_spec_8tbs": round(dec_gbs / 8000.0, 4),
+                   "seqs_per_s": round(mb.dec.num_seqs / (dec_ms * 1e-3), 1)},
+        "prefill": {"ms": round(pre_ms, 4), "tflops": round(pre_tflops, 1),
+                    "frac_bf16": round(pre_tflops / peaks["bf16_tflops"], 4),
+                    "frac_bf16_sustained": round(pre_tflops / peaks["bf16_tflops_sustained"], 4),
+                    "frac_bf16_spec_2250": round(pre_tflops / 2250.0, 4),
+                    "tokens_per_s": round(mb.pre.num_new_tokens / (pre_ms * 1e-3), 1)},
+        "store_meta_ms": round(statistics.mean(phase["store_meta"]), 4),
+        "e2e": {"value": round(world * mb.step_bytes / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": mb.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "device_error": dev_err,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(mb, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+def oracle_decode_sample(dec: W.Problem, seqs, fetch_pages, q_rows):
+    """Run the oracle on decode sequences `seqs` of the mixed batch.  The
+    pages those sequences use are packed into a compact host pool (the
+    oracle's result does not depend on physical placement) and the K/V rows
+    of the new tokens are already in them.  Returns (seconds, bytes)."""
+    import oracle
+    pages = sorted(set(p for b in seqs for p in dec.meta["page_lists"][b]))
+    remap = {p: i for i, p in enumerate(pages)}
+    kc, vc = fetch_pages(pages)
+    L = dec.device_len[seqs].astype(np.int64)
+    width = max(1, int(max(len(dec.meta["page_lists"][b]) for b in seqs)))
+    pt = np.zeros((len(seqs), width), np.int32)
+    for i, b in enumerate(seqs):
+        pl = [remap[p] for p in dec.meta["page_lists"][b]]
+        pt[i, :len(pl)] = pl
+    t0 = time.perf_counter()
+    oracle.decode(q_rows, kc, vc, pt, L, num_q_heads=dec.num_q_heads, num_kv_heads=dec.num_kv_heads,
+                  head_dim=dec.head_dim, page_size=dec.page_size, scale=dec.scale)
+    dt = time.perf_counter() - t0
+    return dt, int(L.sum()) * dec.num_kv_heads * dec.head_dim * 2 * 2
+
+
+def cpu_baseline(mb: MixedBatch, target_s: float):
+    """The fp64 oracle on the host cores, on a bounded sample of the decode
+    batch (the step's dominant work), in the same unit (GB/s of K/V)."""
+    import oracle
+    torch = mb.torch
+    dec = mb.dec
+
+    def fetch(pages):
+        idx = torch.tensor(pages, dtype=torch.long, device=mb.dev)
+        k = mb.k_cache.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+        v = mb.v_cache.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+        return k, v
+
+    order = np.random.default_rng(5).permutation(dec.num_seqs)
+    qh = mb.q_dec.view(torch.int16).cpu().numpy().view(np.uint16)
+    # a fixed sample of the decode batch (~2 GB of K/V), run repeatedly until
+    # about target_s seconds of oracle time have been spent
+    seqs, acc = [], 0
+    for b in order:
+        nb = int(dec.device_len[b]) * dec.num_kv_heads * dec.head_dim * 4
+        if seqs and acc + nb > 2e9:
+            break
+        seqs.append(int(b))
+        acc += nb
+    total_t, total_b, reps = 0.0, 0, 0
+    while total_t < target_s and reps < 100:
+        dt, by = oracle_decode_sample(dec, seqs, fetch, qh[seqs])
+        total_t += dt
+        total_b += by
+        reps += 1
+    return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle decode of {len(seqs)} of the 256 decode sequences "
+                      f"({total_b / reps / 1e9:.2f} GB of K/V) x {reps} repetitions, {total_t:.1f} s"}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle, each step a bounded sample of the
+    workload's decode batch (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    cfg = W.config(5, with_data=False)
+    dec = cfg["decode"]
+    rng = np.random.default_rng(W.SEED_BASE + 60)
+    # host pool holding only the sampled sequences' pages (seeded N(0,1) values)
+    seqs = [int(b) for b in np.argsort(dec.device_len)[:args.ref_seqs]]
+    pages = sorted(set(p for b in seqs for p in dec.meta["page_lists"][b]))
+    shape = (len(pages), dec.page_size, dec.num_kv_heads, dec.head_dim)
+    kc, vc = W.normal_bf16(rng, shape), W.normal_bf16(rng, shape)
+    q = W.normal_bf16(rng, (len(seqs), dec.num_q_heads, dec.head_dim))
+
+    def fetch(_pages):
+        return kc, vc
+
+    for _ in range(args.warmup):
+        oracle_decode_sample(dec, seqs, fetch, q)
+    times, nbytes = [], 0
+    for _ in range(args.steps):
+        dt, nbytes = oracle_decode_sample(dec, seqs, fetch, q)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = nbytes / (ms * 1e-3) / 1e9
+    sample = (f"fp64 oracle decode of the {len(seqs)} shortest of the 256 decode sequences "
+              f"({nbytes / 1e9:.3f} GB of K/V per step)")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target wall time of the CPU-oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seqs", type=int, default=24, help="decode sequences per reference step")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
