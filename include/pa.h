@@ -7,6 +7,7 @@
  *   pa_build_page_table  per-request page table from the token-granular table
  *   pa_prefill           varlen causal prefill / extend attention
  *   pa_decode            one-query-per-sequence split-KV decode attention
+ *   pa_decode_noalloc    the same, with fixed library-owned split scratch
  *   pa_lse_combine       merge of split partial results by log-sum-exp
  *
  * Sources (web pages; section names as printed on them):
@@ -202,6 +203,33 @@ size_t pa_decode_workspace_size(const pa_decode_params *p);
 int32_t pa_decode_kv_chunk(const pa_decode_params *p);
 
 pa_status pa_decode(const pa_decode_params *p, void *stream);
+
+/*
+ * pa_decode_noalloc - pa_decode for callers that cannot allocate device
+ * memory.  The paper has no counterpart for this entry point; it exists for
+ * deployment.  Some callers may not call cudaMalloc at all: code
+ * that runs while a CUDA graph is being captured, plug-ins whose host
+ * application owns every byte of device memory through its own arena,
+ * latency-critical loops where an allocation could synchronise the device,
+ * or runtimes with a hard memory budget.  This call takes the same
+ * parameters as pa_decode except that p->workspace and p->workspace_bytes
+ * are ignored: the split partials go to a fixed scratch array that is part
+ * of the library image (a file-scope __device__ array of
+ * PA_DECODE_NOALLOC_SCRATCH_BYTES = 32 MiB, held on every GPU that loads the
+ * library until the process exits).  The caller still passes q, the pools,
+ * the metadata and out/lse.
+ *  - Sizes whose split scratch (pa_decode_workspace_size) exceeds 32 MiB are
+ *    rejected with PA_ERR_UNSUPPORTED and a message; nothing is launched.
+ *  - The first call on a device (with that device current) looks up the
+ *    scratch address with cudaGetSymbolAddress; make that first call before
+ *    any stream capture.  No call allocates or frees memory.
+ *  - All calls on a device share the one scratch array, which keeps the last
+ *    call's partials (nothing in it needs to start at zero).  Calls whose
+ *    kernels overlap on the GPU (other streams, other threads) race on it:
+ *    serialise them.
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+pa_status pa_decode_noalloc(const pa_decode_params *p, void *stream);
 
 /*
  * pa_lse_combine - stable merge of split partials ([T] s.12 and s.16):

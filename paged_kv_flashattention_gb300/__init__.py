@@ -7,11 +7,12 @@ combine; this package is its thin torch binding.  PyTorch provides device
 memory and streams only.
 """
 from .api import (PagedAttentionError, abi_version, build_page_table, build_seqlens, decode,
-                  decode_kv_chunk, decode_workspace_size, device_error, lse_combine, prefill,
+                  decode_noalloc, decode_kv_chunk, decode_workspace_size, device_error, lse_combine, prefill,
                   store_kv)
 
 __all__ = [
     "PagedAttentionError", "abi_version", "build_page_table", "build_seqlens", "decode",
+    "decode_noalloc",
     "decode_kv_chunk", "decode_workspace_size", "device_error", "lse_combine", "prefill",
     "store_kv",
 ]

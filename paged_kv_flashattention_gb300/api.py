@@ -244,6 +244,36 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_t
     return out
 
 
+def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   page_table: torch.Tensor, cache_seqlens: torch.Tensor, max_seqlen_k: int, *,
+                   scale: float | None = None, page_size: int | None = None,
+                   out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                   kv_chunk: int = 0) -> torch.Tensor:
+    """Split-KV decode through ``pa_decode_noalloc``: the split partials go to
+    the library's fixed 32 MiB device scratch, so no workspace is allocated
+    (for callers that may not allocate device memory).  Calls on one device
+    must not overlap on the GPU; sizes whose scratch would exceed 32 MiB raise
+    PagedAttentionError.  ``out`` (and ``lse``) must be given by a caller that
+    cannot allocate; they are created here only for convenience."""
+    dev = q.device
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, dev)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, dev)
+    _need(page_table, "page_table", torch.int32, dev, contiguous=False)
+    if page_table.dim() != 2 or page_table.stride(1) != 1:
+        raise ValueError("page_table must be 2-D with unit column stride")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    p = _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k, scale, page_size,
+                       out, lse, None, kv_chunk)
+    lib = _lib.load()
+    _check(lib.pa_decode_noalloc(ctypes.byref(p), _stream(q)), lib)
+    return out
+
+
 def lse_combine(o_partial: torch.Tensor, lse_partial: torch.Tensor,
                 splits_per_row: torch.Tensor | None = None, *, out: torch.Tensor | None = None,
                 lse: torch.Tensor | None = None) -> torch.Tensor:

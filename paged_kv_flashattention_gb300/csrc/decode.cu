@@ -30,6 +30,8 @@
 // The whole kernel is bound by HBM: every K/V byte is read once.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -547,6 +549,33 @@ cudaError_t launch_lse_combine(const float *o_partial, const float *lse_partial,
             o_partial, lse_partial, splits_per_row, cache_seqlens, kv_chunk, heads_per_seq,
             num_rows, max_splits, o, lse_out);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Scratch for pa_decode_noalloc: a file-scope device array, so a caller that
+// cannot allocate device memory still gets split-KV decode.  Every GPU that
+// loads this library holds these bytes until the process exits.  Host code
+// must not pass the symbol itself to a kernel (on the host it is only a
+// stand-in, not a device address): the device address is looked up once per
+// device with cudaGetSymbolAddress, with that device current.
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[kDecodeNoAllocScratchBytes];
+
+cudaError_t decode_noalloc_scratch(void **ptr) {
+    static std::mutex lock;
+    static void *addr[kMaxDevices] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(lock);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace pa

@@ -249,6 +249,29 @@ pa_status pa_decode(const pa_decode_params *p, void *stream) {
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "decode launch");
 }
 
+pa_status pa_decode_noalloc(const pa_decode_params *p, void *stream) {
+    g_last_error[0] = 0;
+    pa_status st = check_decode(p);
+    if (st != PA_OK) return st;
+    if (p->num_seqs == 0) return PA_OK;
+    const DecodePlan plan = plan_decode(*p);
+    if (plan.workspace_bytes > kDecodeNoAllocScratchBytes)
+        return fail(PA_ERR_UNSUPPORTED,
+                    "pa_decode_noalloc: these sizes need %zu bytes of split scratch, more than its fixed "
+                    "%zu bytes; use pa_decode with a caller-allocated workspace, or a larger kv_chunk",
+                    plan.workspace_bytes, (size_t)kDecodeNoAllocScratchBytes);
+    void *scratch = nullptr;
+    if (plan.workspace_bytes > 0) {
+        cudaError_t e = decode_noalloc_scratch(&scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "pa_decode_noalloc: cudaGetSymbolAddress(scratch)");
+    }
+    // The existing decode path, with the fixed scratch as its workspace.
+    pa_decode_params q = *p;
+    q.workspace = scratch;
+    q.workspace_bytes = scratch ? kDecodeNoAllocScratchBytes : 0;
+    return pa_decode(&q, stream);
+}
+
 pa_status pa_lse_combine(const float *o_partial, const float *lse_partial, const int32_t *splits_per_row,
                          int32_t num_rows, int32_t max_splits, int32_t head_dim, void *out, float *lse_out,
                          void *stream) {

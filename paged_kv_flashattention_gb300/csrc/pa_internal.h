@@ -38,6 +38,13 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream);
 
 int num_sms();
 
+// Fixed-size scratch behind pa_decode_noalloc (a file-scope device array in
+// decode.cu).  decode_noalloc_scratch returns its device address on the
+// current device, looking it up on the first call per device.
+constexpr size_t kDecodeNoAllocScratchBytes = size_t(32) << 20;
+constexpr int kMaxDevices = 64;
+cudaError_t decode_noalloc_scratch(void **ptr);
+
 // Device addresses of each translation unit's error word.
 cudaError_t error_word_store(int **addr);
 cudaError_t error_word_decode(int **addr);
