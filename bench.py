@@ -430,6 +430,86 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+MICRO_CASES = {
+    # name: (config, variant, kernel)
+    "tiny_decode": (1, None, "decode"),
+    "llama32_1b_decode": (2, None, "decode"),
+    "varlen_prefill_16x512": (3, None, "prefill"),
+    "extend_partial_hit_p16": (4, None, "prefill"),
+    "extend_partial_hit_p1": (4, "p1", "prefill"),
+    "store_16x512": (3, None, "store"),
+    # a smaller mixed-batch decode: 64 sequences, contexts log-uniform
+    # [512, 32768], ~2 GB pool (inputs still far larger than L2)
+    "decode_64seq_logu": (None, None, "decode"),
+}
+
+
+def micro_problem(name):
+    cfg, variant, kernel = MICRO_CASES[name]
+    if cfg is not None:
+        return W.config(cfg, variant), kernel
+    rng = np.random.default_rng(W.SEED_BASE + 70)
+    Lk = np.exp(rng.uniform(math.log(512), math.log(32768), size=64)).astype(np.int32)
+    p = W.build(name, cached_len=Lk - 1, extend_len=np.ones(64, np.int32), num_q_heads=32,
+                num_kv_heads=8, head_dim=128, page_size=16, seed=W.SEED_BASE + 71, pool_factor=1.1)
+    return p, kernel
+
+
+def run_micro(args):
+    """One kernel on one workload, as in a microbenchmark manifest: warm-up,
+    then `steps` launches timed one by one with CUDA events (median, p95)."""
+    import torch
+    import paged_kv_flashattention_gb300 as pa
+    from paged_kv_flashattention_gb300 import metadata
+    dev = torch.device("cuda", 0)
+    p, kernel = micro_problem(args.micro)
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    kc, vc, q = to(p.k_cache), to(p.v_cache), to(p.q)
+    kn, vn = to(p.k_new), to(p.v_new)
+    sm = torch.from_numpy(p.slot_mapping).to(dev)
+    pa.store_kv(kn, vn, sm, kc, vc)
+    m = metadata.prepare(p.cached_len, p.extend_len, torch.from_numpy(p.token_table).to(dev),
+                         torch.from_numpy(p.table_idx).to(dev), p.page_size)
+    Hkv, D, Hq = p.num_kv_heads, p.head_dim, p.num_q_heads
+    out = torch.empty_like(q)
+    if kernel == "decode":
+        ws = torch.empty(max(16, pa.decode_workspace_size(q.shape, kc, m.max_seqlen_k)),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: pa.decode(q, kc, vc, m.page_table, m.cache_seqlens, m.max_seqlen_k,
+                               scale=p.scale, out=out, workspace=ws)
+        work = int(p.device_len.astype(np.int64).sum()) * Hkv * D * 4 + 2 * q.numel() * 2
+        unit = "GB/s"
+    elif kernel == "prefill":
+        fn = lambda: pa.prefill(q, kc, vc, m.page_table, m.cu_seqlens_q, m.cu_seqlens_k,
+                                m.max_seqlen_q, m.max_seqlen_k, causal=p.causal, scale=p.scale, out=out)
+        off = p.cached_len.astype(np.int64)
+        E = p.extend_len.astype(np.int64)
+        work = 4 * D * Hq * int(np.sum(E * off + E * (E + 1) // 2))
+        unit = "TFLOP/s"
+    else:
+        fn = lambda: pa.store_kv(kn, vn, sm, kc, vc)
+        work = 2 * 2 * kn.numel() * 2
+        unit = "GB/s"
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in ts)
+    med = us[len(us) // 2]
+    p95 = us[min(len(us) - 1, int(0.95 * len(us)))]
+    rate = work / (med * 1e-6) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(json.dumps({"micro": args.micro, "kernel": kernel, "us_median": round(med, 2),
+                      "us_p95": round(p95, 2), "rate": round(rate, 1), "unit": unit,
+                      "work": work, "iters": args.steps, "warmup": args.warmup}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -440,10 +520,14 @@ def main(argv=None):
                     help="target wall time of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seqs", type=int, default=24, help="decode sequences per reference step")
+    ap.add_argument("--micro", choices=sorted(MICRO_CASES), default=None,
+                    help="time one kernel on one workload instead of the full step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.micro:
+        run_micro(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
