@@ -246,6 +246,16 @@ pa_status pa_lse_combine(const float *o_partial, const float *lse_partial,
                          const int32_t *splits_per_row, int32_t num_rows, int32_t max_splits,
                          int32_t head_dim, void *out, float *lse_out, void *stream);
 
+/*
+ * pa_selftest_exp2 - evaluate, on the device, the 2^x approximation the
+ * prefill softmax uses for a quarter of its exponentials (2^round(x) times a
+ * cubic fitted to 2^f on [-1/2, 1/2], relative error < 8e-5 for x >= -125),
+ * so tests can compare it with CUDA's exp2f.  ([T] s.12 defines the
+ * exponentials; the approximation is this library's.)
+ * x, y: device fp32 [n]; y[i] = approximation of 2^x[i].
+ */
+pa_status pa_selftest_exp2(const float *x, float *y, int64_t n, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -62,6 +62,7 @@ SIGNATURES = {
     "pa_decode": (ctypes.c_int, [ctypes.POINTER(DecodeParams), c_p]),
     "pa_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(DecodeParams), c_p]),
     "pa_lse_combine": (ctypes.c_int, [c_p, c_p, c_p, c_i32, c_i32, c_i32, c_p, c_p, c_p]),
+    "pa_selftest_exp2": (ctypes.c_int, [c_p, c_p, c_i64, c_p]),
 }
 
 

@@ -272,6 +272,15 @@ pa_status pa_decode_noalloc(const pa_decode_params *p, void *stream) {
     return pa_decode(&q, stream);
 }
 
+pa_status pa_selftest_exp2(const float *x, float *y, int64_t n, void *stream) {
+    g_last_error[0] = 0;
+    if (n < 0) return fail(PA_ERR_INVALID, "n < 0");
+    if (n == 0) return PA_OK;
+    if (!x || !y) return fail(PA_ERR_INVALID, "NULL pointer");
+    cudaError_t e = launch_exp2_selftest(x, y, n, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "exp2 self-test launch");
+}
+
 pa_status pa_lse_combine(const float *o_partial, const float *lse_partial, const int32_t *splits_per_row,
                          int32_t num_rows, int32_t max_splits, int32_t head_dim, void *out, float *lse_out,
                          void *stream) {

@@ -9,26 +9,32 @@
 // prefix is aligned to the end of its keys ("code-series sgl-project
 // mini-sglang 07": seqlens_q = extend_len, seqlens_k = device_len).
 //
-// GB300 design (prior art on the pages is Hopper/Ampere; this is not it):
-// one CTA = one 128-row query tile of one query head of one request.
-//   warp 4 (producer): TMA loads the Q tile once (two 64-column halves,
+// GB300 design (the pages' prior art is Ampere/Hopper; this is not it).
+// One CTA = one 128-row query tile of T query heads that share a KV head
+// (T = 2 when the GQA group allows it), so every K/V tile feeds 2T MMAs.
+//   warp 4T (producer): TMA loads the T Q tiles once (64-column halves,
 //     128-byte swizzle, K-major), then per 128-key step the K and V tiles:
 //     page size 16 -> one 3-D TMA box of 16 tokens per page and half;
 //     page size 1  -> cp.async 16-byte rows placed in the same swizzled
-//     layout.  A two-stage ring; pages past the request's keys are filled
-//     with zeros by out-of-range TMA coordinates.
-//   warp 5 (MMA): one thread issues tcgen05.mma.  S_j = Q K_j^T (SS form,
-//     both K-major) into one of two 128-column TMEM buffers, so S_{j+1} is
-//     computed while the softmax works on S_j; then O += P_j V_j with P_j
-//     read from TMEM (TS form) and V_j MN-major in shared memory.
-//   warps 0-3 (softmax): thread r owns query row r = TMEM lane r.  It loads
-//     its S row with tcgen05.ld, applies scale * log2(e), the causal and
-//     length masks, updates the running maximum lazily (only when the tile
-//     maximum exceeds it by more than 8, i.e. 2^8 headroom; then O in TMEM is
-//     rescaled by exp2(m_old - m_new)), writes P as bf16 back over its S
-//     columns with tcgen05.st, and finally normalises O and writes bf16
-//     output and the natural-log LSE.
-// TMEM: S0 = columns [0,128), S1 = [128,256), O = [256, 256 + d).
+//     layout.  A two-stage ring; pages past the visible keys are filled with
+//     zeros by out-of-range TMA coordinates.
+//   warp 4T+1 (MMA): one thread issues tcgen05.mma.  Order per step j:
+//     PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...: S_k(j+1) overwrites the TMEM
+//     columns that PV_k(j) reads P from, which relies on tcgen05.mma ops of
+//     one thread executing in issue order; and because a tcgen05.commit
+//     tracks every earlier MMA of the thread, the arrival of S_k(j+1) also
+//     tells the softmax that PV_k(j) has finished (O_k may be rescaled).
+//   warps 4k..4k+3 (softmax of tile k): thread r owns query row r = TMEM
+//     lane r.  It loads its S row with tcgen05.ld, masks only on tiles that
+//     reach the causal diagonal or the end of the keys, takes the row maximum
+//     with a tree of independent maxima, updates the running maximum lazily
+//     (only when the tile maximum exceeds it by more than 8 in log2 units;
+//     then O_k in TMEM is rescaled), computes p = 2^(s*scale*log2 e - m) with
+//     packed f32x2 FMAs -- three quarters of the exponentials on the MUFU
+//     unit, one quarter as a cubic on the FMA pipe so the two units share the
+//     load -- writes P as bf16 over its S columns with tcgen05.st, and at the
+//     end normalises O and writes bf16 output and the natural-log LSE.
+// TMEM (512 columns): S_k at [128k, 128k+128), O_k at [256 + 128k, +d).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -47,8 +53,37 @@ namespace {
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per step
 constexpr int kKVStages = 2;
-constexpr int kThreads = 192;     // 4 softmax warps + producer + MMA
 constexpr float kLazy = 8.0f;
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    uint64_t ai = *reinterpret_cast<uint64_t *>(&a), bi = *reinterpret_cast<uint64_t *>(&b), r;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ai), "l"(bi));
+    return *reinterpret_cast<float2 *>(&r);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// 2^x on the FMA pipe for two values: 2^x = 2^n * p(x - n), n = round(x).
+// round() adds 1.5 * 2^23 in fp32 (the sum's low mantissa bits hold n) and
+// 2^n is applied by adding n << 23 to p's bits.  p is a cubic fitted to 2^f
+// on [-1/2, 1/2] (relative error < 8e-5; exp2_poly_fit.py).  x is clamped at
+// -125 so the result stays a normal float (2^-125 is zero for bf16 P).
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+    x.x = fmaxf(x.x, -125.f);
+    x.y = fmaxf(x.y, -125.f);
+    const float2 t = add2(x, make_float2(12582912.f, 12582912.f));
+    const float2 n = add2(t, make_float2(-12582912.f, -12582912.f));
+    const float2 f = add2(x, make_float2(-n.x, -n.y));
+    float2 p = ffma2(make_float2(0.0551705262f, 0.0551705262f), f, make_float2(0.24260831f, 0.24260831f));
+    p = ffma2(p, f, make_float2(0.69326092f, 0.69326092f));
+    p = ffma2(p, f, make_float2(0.999928252f, 0.999928252f));
+    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
+}
 
 struct PrefillArgs {
     CUtensorMap qmap;             // bf16 (d, Hq, total_q), box (64, 1, 128)
@@ -73,12 +108,12 @@ struct PrefillArgs {
     float scale_log2;
 };
 
-template <int D>
+template <int D, int T>
 struct PrefillSmem {
     static constexpr int kHalves = D / 64;                 // 64-column (128-byte) halves
     static constexpr int kTileBytes = kHalves * 128 * 128; // 128 rows x D bf16
-    static constexpr int kQ = 0;
-    static constexpr int kKV = kTileBytes;                  // stage s: K at kKV + s*2*tile, V after
+    static constexpr int kQ = 0;                           // T query tiles
+    static constexpr int kKV = T * kTileBytes;             // stage s: K at kKV + s*2*tile, V after
     static constexpr int kBars = kKV + kKVStages * 2 * kTileBytes;
     static constexpr int kTotal = kBars + 256;
 };
@@ -86,56 +121,59 @@ struct PrefillSmem {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
-    using S = PrefillSmem<D>;
+template <int D, int T>
+__global__ void __launch_bounds__(32 * (4 * T + 2), 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
+    using S = PrefillSmem<D, T>;
     constexpr int H = S::kHalves;
+    constexpr int kProducer = 4 * T;
+    constexpr int kMma = 4 * T + 1;
+    constexpr int kOCols = D == 128 ? 128 : 64;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int tile = blockIdx.x;
-    const int h = blockIdx.y;
     const int b = blockIdx.z;
     const int q0 = a.cu_q[b];
     const int Lq = a.cu_q[b + 1] - q0;
     const int Lk = a.cu_k[b + 1] - a.cu_k[b];
-    if (tile * kBM >= Lq) return;                     // uniform per CTA
-    const int kvh = h / (a.num_q_heads / a.num_kv_heads);
-    const int off = Lk - Lq;                          // cached prefix length
+    const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;     // later (heavier) tiles launch first
+    if (tile * kBM >= Lq) return;                               // uniform per CTA
+    const int h0 = blockIdx.y * T;                              // query heads h0 .. h0+T-1
+    const int kvh = h0 / (a.num_q_heads / a.num_kv_heads);
+    const int off = Lk - Lq;                                    // cached prefix length
     const int rows_here = min(kBM, Lq - tile * kBM);
-    // keys this tile can see
-    int kv_end = Lk;
+    int kv_end = Lk;                                            // keys the tile's last row sees
     if (a.causal) kv_end = min(Lk, off + tile * kBM + rows_here);
     if (kv_end < 0) kv_end = 0;
     const int n_kv = (kv_end + kBN - 1) / kBN;
+    // keys every row of the tile sees: steps entirely below this need no mask
+    int min_vis = a.causal ? min(Lk, off + tile * kBM + 1) : Lk;
+    if (min_vis < 0) min_vis = 0;
 
     uint8_t *sQ = smem + S::kQ;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBars);
     uint64_t *q_full = bars;                 // 1
     uint64_t *kv_full = bars + 1;            // kKVStages
     uint64_t *kv_empty = bars + 3;           // kKVStages
-    uint64_t *s_full = bars + 5;             // 2
-    uint64_t *p_full = bars + 7;             // 2
-    uint64_t *pv_done = bars + 9;            // 1: one phase per P.V step
-    uint64_t *o_final = bars + 10;           // 1: the last P.V (and all before it) done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+    uint64_t *s_full = bars + 5;             // T
+    uint64_t *p_full = bars + 7;             // T
+    uint64_t *o_final = bars + 9;            // 1: every MMA of the CTA done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const bool paged16 = (a.page_size == 16);
 
-    if (warp == 5) tmem_alloc(tmem_slot, 512);
+    if (warp == kMma) tmem_alloc(tmem_slot, 512);
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < kKVStages; ++s) {
             mbar_init(&kv_full[s], paged16 ? 1 : 32);
             mbar_init(&kv_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&s_full[s], 1);
-            mbar_init(&p_full[s], 128);
+        for (int k = 0; k < T; ++k) {
+            mbar_init(&s_full[k], 1);
+            mbar_init(&p_full[k], 128);
         }
-        mbar_init(pv_done, 1);
         mbar_init(o_final, 1);
         fence_mbar_init();
     }
@@ -143,17 +181,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 256;
 
-    if (warp == 4) {
+    if (warp == kProducer) {
         // ----------------------------------------------------- producer ----
         const int32_t *pt = a.page_table + (int64_t)b * a.pt_stride;
         if (lane == 0) {
             prefetch_tmap(&a.qmap);
             if (paged16) { prefetch_tmap(&a.kmap); prefetch_tmap(&a.vmap); }
-            mbar_arrive_expect_tx(q_full, S::kTileBytes);
-            for (int hh = 0; hh < H; ++hh)
-                tma_load_3d(sQ + hh * 16384, &a.qmap, hh * 64, h, q0 + tile * kBM, q_full);
+            mbar_arrive_expect_tx(q_full, T * S::kTileBytes);
+            for (int k = 0; k < T; ++k)
+                for (int hh = 0; hh < H; ++hh)
+                    tma_load_3d(sQ + k * S::kTileBytes + hh * 16384, &a.qmap, hh * 64, h0 + k,
+                                q0 + tile * kBM, q_full);
         }
         for (int j = 0; j < n_kv; ++j) {
             const int st = j % kKVStages;
@@ -205,97 +244,112 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
                 cp_async_commit();
                 cp_async_wait_all();
-                fence_proxy_async_smem();      // make generic-proxy writes visible to the MMA
+                fence_proxy_async_smem();      // generic-proxy writes -> visible to the MMA
                 mbar_arrive(&kv_full[st]);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMma) {
         // ---------------------------------------------------------- MMA ----
         if (lane == 0 && n_kv > 0) {
             constexpr uint32_t idesc_s = umma_idesc_bf16(kBM, kBN, false);
             constexpr uint32_t idesc_o = umma_idesc_bf16(kBM, D, true);
-            bool ok = mbar_wait(q_full, 0);
-            auto issue_s = [&](int j) -> bool {
-                const int st = j % kKVStages;
-                if (!mbar_wait(&kv_full[st], (j / kKVStages) & 1)) return false;
-                tc_fence_after();
-                const uint8_t *sK = smem + S::kKV + st * 2 * S::kTileBytes;
-                const uint32_t dst = tmem + (j & 1) * 128;
+            auto issue_s = [&](int k, int j) {
+                const uint8_t *sK = smem + S::kKV + (j % kKVStages) * 2 * S::kTileBytes;
+                const uint8_t *sQk = sQ + k * S::kTileBytes;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t qa = smem_u32(sQ + (k / 4) * 16384 + (k % 4) * 32);
-                    const uint32_t ka = smem_u32(sK + (k / 4) * 16384 + (k % 4) * 32);
-                    umma_ss(dst, umma_desc_sw128(qa, 16, 1024), umma_desc_sw128(ka, 16, 1024), idesc_s, k > 0);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qa = smem_u32(sQk + (kk / 4) * 16384 + (kk % 4) * 32);
+                    const uint32_t ka = smem_u32(sK + (kk / 4) * 16384 + (kk % 4) * 32);
+                    umma_ss(tmem + 128 * k, umma_desc_sw128(qa, 16, 1024), umma_desc_sw128(ka, 16, 1024),
+                            idesc_s, kk > 0);
                 }
-                umma_commit(&s_full[j & 1]);
-                return true;
+                umma_commit(&s_full[k]);
             };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv) {
-                    // S buffer (j+1)&1 held P_{j-1}: its PV must have finished
-                    if (j >= 1 && !mbar_wait(pv_done, (j - 1) & 1)) { ok = false; break; }
-                    if (!issue_s(j + 1)) { ok = false; break; }
-                }
-                if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
+            bool ok = mbar_wait(q_full, 0) && mbar_wait(&kv_full[0], 0);
+            if (ok) {
                 tc_fence_after();
+                for (int k = 0; k < T; ++k) issue_s(k, 0);
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
                 const int st = j % kKVStages;
                 const uint8_t *sV = smem + S::kKV + st * 2 * S::kTileBytes + S::kTileBytes;
-                const uint32_t pa_tm = tmem + (j & 1) * 128;
+                for (int k = 0; k < T; ++k) {
+                    if (!mbar_wait(&p_full[k], j & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t o_tm = tmem + 256 + kOCols * k;
 #pragma unroll
-                for (int k = 0; k < kBN / 16; ++k) {
-                    const uint32_t va = smem_u32(sV + k * 16 * 128);
-                    umma_ts(tO, pa_tm + k * 8, umma_desc_sw128(va, 16384, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        const uint32_t va = smem_u32(sV + kk * 16 * 128);
+                        umma_ts(o_tm, tmem + 128 * k + kk * 8, umma_desc_sw128(va, 16384, 1024), idesc_o,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (k == T - 1) umma_commit(&kv_empty[st]);
+                    if (j + 1 < n_kv) {
+                        if (k == 0) {
+                            if (!mbar_wait(&kv_full[(j + 1) % kKVStages], ((j + 1) / kKVStages) & 1)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        issue_s(k, j + 1);
+                    }
                 }
-                umma_commit(pv_done);
-                umma_commit(&kv_empty[st]);
-                if (j == n_kv - 1) umma_commit(o_final);
             }
+            umma_commit(o_final);
         }
     } else {
         // ------------------------------------------------------ softmax ----
-        const int r = threadIdx.x;                    // row within the tile = TMEM lane
+        const int k = warp >> 2;                      // query tile (head h0 + k)
+        const int r = threadIdx.x & 127;              // row within the tile = TMEM lane
         const int qi = tile * kBM + r;                // query index within the request
         const bool row_valid = r < rows_here;
         const int vis_end = a.causal ? min(Lk, off + qi + 1) : Lk;   // keys [0, vis_end)
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t s_tm = tmem + lane_base + 128 * k;
+        const uint32_t o_tm = tmem + lane_base + 256 + kOCols * k;
+        const float2 c2 = make_float2(a.scale_log2, a.scale_log2);
         float m_run = -INFINITY;
         float l_run = 0.f;
         bool ok = true;
         // tcgen05.ld / st are warp-collective (.sync.aligned): every branch
-        // that encloses one is made warp-uniform, and the warp reconverges
-        // after each (per-lane) barrier wait.
+        // that encloses one is warp-uniform, and the warp reconverges after
+        // each (per-lane) barrier wait.
         for (int j = 0; j < n_kv; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[k], j & 1));
             if (!ok) break;
             tc_fence_after();
-            const uint32_t sb = tmem + lane_base + (j & 1) * 128;
             uint32_t sr[kBN];
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) tmem_ld32(sb + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+            for (int c = 0; c < kBN / 32; ++c) tmem_ld32(s_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
             tmem_wait_ld();
             const int kbase = j * kBN;
-            const int lim = row_valid ? vis_end - kbase : 0;   // columns < lim are visible
-            float mt = -INFINITY;
+            if (kbase + kBN > min_vis) {                // tile reaches the diagonal / end: mask
+                const int lim = row_valid ? vis_end - kbase : kBN;
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                float x = __uint_as_float(sr[c]) * a.scale_log2;
-                x = (c < lim) ? x : -INFINITY;
-                sr[c] = __float_as_uint(x);
-                mt = fmaxf(mt, x);
+                for (int c = 0; c < kBN; ++c)
+                    if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
             }
+            // row maximum of the raw scores (scale > 0 commutes with max)
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i]);
+#pragma unroll
+            for (int c = 8; c < kBN; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+            const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            const float m_cand = mt * a.scale_log2;
             // lazy maximum: move it only when the tile maximum exceeds it by
-            // more than kLazy; then O (after P.V_{j-1}) and l are rescaled
-            const bool need = mt > m_run + kLazy;
-            const float alpha = need ? fast_exp2(m_run - mt) : 1.f;
+            // more than kLazy; then O_k (PV_k(j-1) is complete: the commit of
+            // S_k(j) tracks it) and l are rescaled
+            const bool need = m_cand > m_run + kLazy;
+            const float alpha = need ? fast_exp2(m_run - m_cand) : 1.f;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t orr[32];
-                    tmem_ld32(tO + lane_base + c * 32, orr);
+                    tmem_ld32(o_tm + c * 32, orr);
                     tmem_wait_ld();
                     uint32_t w0[16], w1[16];
 #pragma unroll
@@ -303,46 +357,53 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         w0[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
                         w1[e] = __float_as_uint(__uint_as_float(orr[16 + e]) * alpha);
                     }
-                    tmem_st16(tO + lane_base + c * 32, w0);
-                    tmem_st16(tO + lane_base + c * 32 + 16, w1);
+                    tmem_st16(o_tm + c * 32, w0);
+                    tmem_st16(o_tm + c * 32 + 16, w1);
                 }
             }
             if (need) {
                 l_run *= alpha;
-                m_run = mt;
+                m_run = m_cand;
             }
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            float psum = 0.f;
+            const float2 nm2 = make_float2(-m_use, -m_use);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
             uint32_t pk[kBN / 2];
 #pragma unroll
             for (int c = 0; c < kBN / 2; ++c) {
-                const float p0 = fast_exp2(__uint_as_float(sr[2 * c]) - m_use);
-                const float p1 = fast_exp2(__uint_as_float(sr[2 * c + 1]) - m_use);
-                psum += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
+                const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), c2, nm2);
+                float2 p;
+                if ((c & 3) == 3) {
+                    p = exp2_poly2(x);
+                } else {
+                    p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                }
+                acc[c & 3] = add2(acc[c & 3], p);
+                pk[c] = pack_bf16x2(p.x, p.y);
             }
-            l_run += psum;
+            const float2 s01 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+            l_run += s01.x + s01.y;
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c)
-                tmem_st16(sb + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
+                tmem_st16(s_tm + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&p_full[j & 1]);
+            mbar_arrive(&p_full[k]);
         }
-        // ---- epilogue: O / l -> bf16, lse.  Up to two P.V phases may still
-        // be pending here, which one parity bit cannot tell apart, so the
-        // last P.V signals its own barrier.
+        // ---- epilogue: O / l -> bf16, lse
         if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0));
         tc_fence_after();
         if (ok) {
             const int64_t tok = (int64_t)q0 + qi;
+            const int h = h0 + k;
             __nv_bfloat16 *orow = a.out + (tok * a.num_q_heads + h) * D;
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t orr[32];
                 if (n_kv > 0) {                       // CTA-uniform
-                    tmem_ld32(tO + lane_base + c * 32, orr);
+                    tmem_ld32(o_tm + c * 32, orr);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -368,9 +429,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMma) {
         __syncwarp();
         tmem_dealloc(tmem, 512);
+    }
+}
+
+__global__ void exp2_selftest_kernel(const float *__restrict__ x, float *__restrict__ y, int64_t n) {
+    const int64_t i = 2 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+    if (i + 1 < n) {
+        const float2 r = exp2_poly2(make_float2(x[i], x[i + 1]));
+        y[i] = r.x;
+        y[i + 1] = r.y;
+    } else if (i < n) {
+        y[i] = exp2_poly2(make_float2(x[i], x[i])).x;
     }
 }
 
@@ -400,15 +472,15 @@ bool make_map(CUtensorMap *m, const void *base, int d, int heads, int64_t rows, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int T>
 cudaError_t launch_t(const PrefillArgs &a, dim3 grid, cudaStream_t stream) {
-    using S = PrefillSmem<D>;
-    // Reserve enough shared memory that one CTA holds an SM (TMEM: 512 columns).
+    using S = PrefillSmem<D, T>;
+    // One CTA per SM (it allocates all 512 TMEM columns).
     const int smem = (S::kTotal + 1024) > 120 * 1024 ? (S::kTotal + 1024) : 120 * 1024;
-    auto kern = prefill_kernel<D>;
+    auto kern = prefill_kernel<D, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, stream>>>(a);
+    kern<<<grid, 32 * (4 * T + 2), smem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -439,9 +511,21 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     a.num_slots = (int32_t)num_slots;
     a.causal = p.causal;
     a.scale_log2 = p.scale * 1.4426950408889634f;
-    dim3 grid((p.max_seqlen_q + kBM - 1) / kBM, p.num_q_heads, p.num_seqs);
+    // two query heads per CTA whenever they share a KV head
+    const int group = p.num_q_heads / p.num_kv_heads;
+    const int T = (group % 2 == 0) ? 2 : 1;
+    dim3 grid((p.max_seqlen_q + kBM - 1) / kBM, p.num_q_heads / T, p.num_seqs);
     if (grid.y > 65535 || grid.z > 65535) return cudaErrorNotSupported;
-    return p.head_dim == 128 ? launch_t<128>(a, grid, stream) : launch_t<64>(a, grid, stream);
+    if (p.head_dim == 128)
+        return T == 2 ? launch_t<128, 2>(a, grid, stream) : launch_t<128, 1>(a, grid, stream);
+    return T == 2 ? launch_t<64, 2>(a, grid, stream) : launch_t<64, 1>(a, grid, stream);
+}
+
+cudaError_t launch_exp2_selftest(const float *x, float *y, int64_t n, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t threads = (n + 1) / 2;
+    exp2_selftest_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(x, y, n);
+    return cudaGetLastError();
 }
 
 }  // namespace pa

@@ -103,3 +103,23 @@ def test_decode_via_prefill_matches_decode(cuda_device):
     compare(o_pre, ref, "decode through prefill", lse_gpu=l_pre.T.contiguous(), lse_ref=ref_lse)
     diff = (o_dec.float() - o_pre.float()).abs().max().item()
     assert diff <= 2e-2
+
+
+def test_exp2_polynomial_against_cuda_exp2(cuda_device):
+    """The softmax's FMA-pipe 2^x (cubic on the reduced argument) against
+    CUDA's exp2f (torch.exp2 on the device): relative error < 1e-4 over the
+    range the softmax feeds it, and exact powers of two at integers."""
+    from paged_kv_flashattention_gb300 import _lib
+    lib = _lib.load()
+    x = torch.cat([torch.linspace(-125.0, 8.0, 1 << 20, device=cuda_device),
+                   torch.arange(-125, 9, device=cuda_device, dtype=torch.float32)])
+    y = torch.empty_like(x)
+    assert lib.pa_selftest_exp2(x.data_ptr(), y.data_ptr(), x.numel(),
+                                torch.cuda.current_stream().cuda_stream) == 0
+    ref = torch.exp2(x)
+    rel = ((y - ref).abs() / ref).max().item()
+    assert rel < 1e-4, rel
+    xi = torch.arange(-125, 9, device=cuda_device, dtype=torch.float32)
+    yi = y[-xi.numel():]
+    # at integers the reduced argument is 0 and the cubic's constant term is within 8e-5 of 1
+    assert ((yi / torch.exp2(xi)) - 1).abs().max().item() < 8e-5
