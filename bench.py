@@ -493,15 +493,33 @@ def run_micro(args):
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
+    # Replay the call from a captured CUDA graph so host launch overhead does
+    # not sit between the events; each replay is timed on its own.
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    # back-to-back replays between two events (mean), in groups of 10 so a
+    # median and p95 over groups can be reported as well
+    groups = max(1, args.steps // 10)
     ts = []
-    for _ in range(args.steps):
+    for _ in range(groups):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        fn()
+        for _ in range(10):
+            graph.replay()
         b.record()
         ts.append((a, b))
     torch.cuda.synchronize()
-    us = sorted(a.elapsed_time(b) * 1e3 for a, b in ts)
+    us = sorted(a.elapsed_time(b) * 1e3 / 10 for a, b in ts)
     med = us[len(us) // 2]
     p95 = us[min(len(us) - 1, int(0.95 * len(us)))]
     rate = work / (med * 1e-6) / (1e12 if unit == "TFLOP/s" else 1e9)

@@ -121,8 +121,14 @@ struct PrefillSmem {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Register split (T = 2): 384 threads launch with 168 registers each
+// (64,512 in all); the softmax warpgroups raise theirs to 184 and the
+// producer/MMA warpgroup lowers its to 128: 256 * 184 + 128 * 128 = 63,488.
+constexpr int kSoftmaxRegs = 184;
+constexpr int kControlRegs = 128;
+
 template <int D, int T>
-__global__ void __launch_bounds__(32 * (4 * T + 2), 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
+__global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
     using S = PrefillSmem<D, T>;
     constexpr int H = S::kHalves;
     constexpr int kProducer = 4 * T;
@@ -182,7 +188,10 @@ __global__ void __launch_bounds__(32 * (4 * T + 2), 1) prefill_kernel(const __gr
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kProducer) {
+    if (warp >= kProducer) {
+        // ------------------------------------- producer / MMA warpgroup ----
+        if (T == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+      if (warp == kProducer) {
         // ----------------------------------------------------- producer ----
         const int32_t *pt = a.page_table + (int64_t)b * a.pt_stride;
         if (lane == 0) {
@@ -201,25 +210,28 @@ __global__ void __launch_bounds__(32 * (4 * T + 2), 1) prefill_kernel(const __gr
             uint8_t *sV = sK + S::kTileBytes;
             const int key0 = j * kBN;
             if (paged16) {
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&kv_full[st], 2 * S::kTileBytes);
-                    for (int pg = 0; pg < kBN / 16; ++pg) {
-                        const int kk = key0 + pg * 16;
-                        int slot0 = a.num_slots;            // out of range: zero fill
-                        if (kk < kv_end) {
-                            const int page = pt[kk / 16];
-                            if (page >= 0 && (int64_t)page * 16 < a.num_slots) slot0 = page * 16;
-                            else raise_error(PA_DEVERR_PAGE_RANGE);
-                        }
-                        for (int hh = 0; hh < H; ++hh) {
-                            tma_load_3d(sK + hh * 16384 + pg * 2048, &a.kmap, hh * 64, kvh, slot0, &kv_full[st]);
-                            tma_load_3d(sV + hh * 16384 + pg * 2048, &a.vmap, hh * 64, kvh, slot0, &kv_full[st]);
-                        }
+                // lanes 0..7 each own one 16-token page of the step: one
+                // page-table read per lane, then that page's TMA boxes
+                if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], 2 * S::kTileBytes);
+                __syncwarp();
+                if (lane < kBN / 16) {
+                    const int kk = key0 + lane * 16;
+                    int slot0 = a.num_slots;                // out of range: zero fill
+                    if (kk < kv_end) {
+                        const int page = pt[kk / 16];
+                        if (page >= 0 && (int64_t)page * 16 < a.num_slots) slot0 = page * 16;
+                        else raise_error(PA_DEVERR_PAGE_RANGE);
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < H; ++hh) {
+                        tma_load_3d(sK + hh * 16384 + lane * 2048, &a.kmap, hh * 64, kvh, slot0, &kv_full[st]);
+                        tma_load_3d(sV + hh * 16384 + lane * 2048, &a.vmap, hh * 64, kvh, slot0, &kv_full[st]);
                     }
                 }
             } else {
                 // page size 1: each lane gathers 4 key rows with cp.async,
                 // writing the 128-byte-swizzled layout TMA would produce
+#pragma unroll
                 for (int rr = 0; rr < kBN / 32; ++rr) {
                     const int r = rr * 32 + lane;
                     const int key = key0 + r;
@@ -248,20 +260,23 @@ __global__ void __launch_bounds__(32 * (4 * T + 2), 1) prefill_kernel(const __gr
                 mbar_arrive(&kv_full[st]);
             }
         }
-    } else if (warp == kMma) {
+      } else if (warp == kMma) {
         // ---------------------------------------------------------- MMA ----
         if (lane == 0 && n_kv > 0) {
             constexpr uint32_t idesc_s = umma_idesc_bf16(kBM, kBN, false);
             constexpr uint32_t idesc_o = umma_idesc_bf16(kBM, D, true);
+            // Descriptors are built once; a k-step adds its byte offset >> 4 to
+            // the 14-bit start-address field (shared addresses stay < 2^18).
+            const uint64_t dq0 = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dkv0 = umma_desc_sw128(smem_u32(smem + S::kKV), 16, 1024);
+            const uint64_t dv0 = umma_desc_sw128(smem_u32(smem + S::kKV + S::kTileBytes), 16384, 1024);
             auto issue_s = [&](int k, int j) {
-                const uint8_t *sK = smem + S::kKV + (j % kKVStages) * 2 * S::kTileBytes;
-                const uint8_t *sQk = sQ + k * S::kTileBytes;
+                const uint64_t dq = dq0 + (uint64_t)((k * S::kTileBytes) >> 4);
+                const uint64_t dk = dkv0 + (uint64_t)(((j % kKVStages) * 2 * S::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qa = smem_u32(sQk + (kk / 4) * 16384 + (kk % 4) * 32);
-                    const uint32_t ka = smem_u32(sK + (kk / 4) * 16384 + (kk % 4) * 32);
-                    umma_ss(tmem + 128 * k, umma_desc_sw128(qa, 16, 1024), umma_desc_sw128(ka, 16, 1024),
-                            idesc_s, kk > 0);
+                    const uint64_t o = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
+                    umma_ss(tmem + 128 * k, dq + o, dk + o, idesc_s, kk > 0);
                 }
                 umma_commit(&s_full[k]);
             };
@@ -272,17 +287,15 @@ __global__ void __launch_bounds__(32 * (4 * T + 2), 1) prefill_kernel(const __gr
             }
             for (int j = 0; ok && j < n_kv; ++j) {
                 const int st = j % kKVStages;
-                const uint8_t *sV = smem + S::kKV + st * 2 * S::kTileBytes + S::kTileBytes;
+                const uint64_t dv = dv0 + (uint64_t)((st * 2 * S::kTileBytes) >> 4);
                 for (int k = 0; k < T; ++k) {
                     if (!mbar_wait(&p_full[k], j & 1)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t o_tm = tmem + 256 + kOCols * k;
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint32_t va = smem_u32(sV + kk * 16 * 128);
-                        umma_ts(o_tm, tmem + 128 * k + kk * 8, umma_desc_sw128(va, 16384, 1024), idesc_o,
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        umma_ts(o_tm, tmem + 128 * k + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                                 (j > 0 || kk > 0) ? 1u : 0u);
-                    }
                     if (k == T - 1) umma_commit(&kv_empty[st]);
                     if (j + 1 < n_kv) {
                         if (k == 0) {
@@ -298,8 +311,10 @@ __global__ void __launch_bounds__(32 * (4 * T + 2), 1) prefill_kernel(const __gr
             }
             umma_commit(o_final);
         }
+      }
     } else {
         // ------------------------------------------------------ softmax ----
+        if (T == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
         const int k = warp >> 2;                      // query tile (head h0 + k)
         const int r = threadIdx.x & 127;              // row within the tile = TMEM lane
         const int qi = tile * kBM + r;                // query index within the request
@@ -351,14 +366,10 @@ __global__ void __launch_bounds__(32 * (4 * T + 2), 1) prefill_kernel(const __gr
                     uint32_t orr[32];
                     tmem_ld32(o_tm + c * 32, orr);
                     tmem_wait_ld();
-                    uint32_t w0[16], w1[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        w0[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                        w1[e] = __float_as_uint(__uint_as_float(orr[16 + e]) * alpha);
-                    }
-                    tmem_st16(o_tm + c * 32, w0);
-                    tmem_st16(o_tm + c * 32 + 16, w1);
+                    for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                    tmem_st16(o_tm + c * 32, *reinterpret_cast<const uint32_t(*)[16]>(&orr[0]));
+                    tmem_st16(o_tm + c * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&orr[16]));
                 }
             }
             if (need) {
@@ -480,7 +491,7 @@ cudaError_t launch_t(const PrefillArgs &a, dim3 grid, cudaStream_t stream) {
     auto kern = prefill_kernel<D, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 32 * (4 * T + 2), smem, stream>>>(a);
+    kern<<<grid, 128 * (T + 1), smem, stream>>>(a);
     return cudaGetLastError();
 }
 
