@@ -67,12 +67,13 @@ SIGNATURES = {
 
 
 def load(path: str | None = None):
-    """Load libpa.so once and bind the signatures."""
+    """Load libpa.so once and bind the signatures.  PA_LIBRARY_PATH selects
+    another build of the library (e.g. one compiled with other flags)."""
     global _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
-        p = path or LIB_PATH
+        p = path or os.environ.get("PA_LIBRARY_PATH") or LIB_PATH
         if not os.path.exists(p):
             raise ImportError(
                 f"libpa.so not found at {p}: build it first "

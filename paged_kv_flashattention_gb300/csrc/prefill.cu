@@ -16,8 +16,10 @@
 //     128-byte swizzle, K-major), then per 128-key step the K and V tiles:
 //     page size 16 -> one 3-D TMA box of 16 tokens per page and half;
 //     page size 1  -> cp.async 16-byte rows placed in the same swizzled
-//     layout.  A two-stage ring; pages past the visible keys are filled with
-//     zeros by out-of-range TMA coordinates.
+//     layout.  K and V tiles go to separate slots of one ring (5 slots of
+//     32 KiB for d = 128 next to 64 KiB of Q), so loads run several tiles
+//     ahead; pages past the visible keys are filled with zeros by
+//     out-of-range TMA coordinates.
 //   warp 4T+1 (MMA): one thread issues tcgen05.mma.  Order per step j:
 //     PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...: S_k(j+1) overwrites the TMEM
 //     columns that PV_k(j) reads P from, which relies on tcgen05.mma ops of
@@ -30,9 +32,9 @@
 //     with a tree of independent maxima, updates the running maximum lazily
 //     (only when the tile maximum exceeds it by more than 8 in log2 units;
 //     then O_k in TMEM is rescaled), computes p = 2^(s*scale*log2 e - m) with
-//     packed f32x2 FMAs -- three quarters of the exponentials on the MUFU
-//     unit, one quarter as a cubic on the FMA pipe so the two units share the
-//     load -- writes P as bf16 over its S columns with tcgen05.st, and at the
+//     packed f32x2 FMAs and the MUFU unit (a cubic on the FMA pipe can take a
+//     share of the exponentials, kPolyEvery), writes P as bf16 over its S
+//     columns with tcgen05.st, and at the
 //     end normalises O and writes bf16 output and the natural-log LSE.
 // TMEM (512 columns): S_k at [128k, 128k+128), O_k at [256 + 128k, +d).
 #include <cuda.h>
@@ -52,8 +54,11 @@ namespace {
 
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per step
-constexpr int kKVStages = 2;
 constexpr float kLazy = 8.0f;
+// Every kPolyEvery-th pair of exponentials is computed by the FMA-pipe cubic
+// instead of the MUFU unit (0 = never).  Measured on the extend workload,
+// all-MUFU was faster while the K/V loads still limit the kernel.
+constexpr int kPolyEvery = 0;
 
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     uint64_t ai = *reinterpret_cast<uint64_t *>(&a), bi = *reinterpret_cast<uint64_t *>(&b), r;
@@ -108,18 +113,26 @@ struct PrefillArgs {
     float scale_log2;
 };
 
+// Shared memory: T query tiles, then a ring of K-or-V tile slots (as many as
+// fit next to Q in 227 KiB, at most 8), then the barriers.  K_j goes to slot
+// (2j) mod n and V_j to slot (2j+1) mod n, so the producer can run several
+// tiles ahead of the MMAs: with one CTA per SM the loads from L2 are latency
+// bound, and bytes in flight set the rate.
 template <int D, int T>
 struct PrefillSmem {
     static constexpr int kHalves = D / 64;                 // 64-column (128-byte) halves
     static constexpr int kTileBytes = kHalves * 128 * 128; // 128 rows x D bf16
     static constexpr int kQ = 0;                           // T query tiles
-    static constexpr int kKV = T * kTileBytes;             // stage s: K at kKV + s*2*tile, V after
-    static constexpr int kBars = kKV + kKVStages * 2 * kTileBytes;
-    static constexpr int kTotal = kBars + 256;
+    static constexpr int kRing = T * kTileBytes;
+    static constexpr int kSlotsFit = (232448 - 1024 - kRing - 512) / kTileBytes;
+    static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;
+    static constexpr int kBars = kRing + kSlots * kTileBytes;
+    static constexpr int kTotal = kBars + 512;
 };
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Register split (T = 2): 384 threads launch with 168 registers each
 // (64,512 in all); the softmax warpgroups raise theirs to 184 and the
@@ -157,13 +170,14 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
 
     uint8_t *sQ = smem + S::kQ;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBars);
+    constexpr int NS = S::kSlots;
     uint64_t *q_full = bars;                 // 1
-    uint64_t *kv_full = bars + 1;            // kKVStages
-    uint64_t *kv_empty = bars + 3;           // kKVStages
-    uint64_t *s_full = bars + 5;             // T
-    uint64_t *p_full = bars + 7;             // T
-    uint64_t *o_final = bars + 9;            // 1: every MMA of the CTA done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
+    uint64_t *full = bars + 1;               // NS: slot loaded
+    uint64_t *empty = full + NS;             // NS: slot consumed by the MMAs
+    uint64_t *s_full = empty + NS;           // T
+    uint64_t *p_full = s_full + T;           // T
+    uint64_t *o_final = p_full + T;          // 1: every MMA of the CTA done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_final + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -172,9 +186,9 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     if (warp == kMma) tmem_alloc(tmem_slot, 512);
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < kKVStages; ++s) {
-            mbar_init(&kv_full[s], paged16 ? 1 : 32);
-            mbar_init(&kv_empty[s], 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], paged16 ? 1 : 32);
+            mbar_init(&empty[s], 1);
         }
         for (int k = 0; k < T; ++k) {
             mbar_init(&s_full[k], 1);
@@ -203,16 +217,18 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                     tma_load_3d(sQ + k * S::kTileBytes + hh * 16384, &a.qmap, hh * 64, h0 + k,
                                 q0 + tile * kBM, q_full);
         }
-        for (int j = 0; j < n_kv; ++j) {
-            const int st = j % kKVStages;
-            if (j >= kKVStages && !mbar_wait(&kv_empty[st], ((j / kKVStages) - 1) & 1)) break;
-            uint8_t *sK = smem + S::kKV + st * 2 * S::kTileBytes;
-            uint8_t *sV = sK + S::kTileBytes;
-            const int key0 = j * kBN;
+        // load c = 2j is K_j, c = 2j + 1 is V_j
+        int gathered = -1;                       // page size 1: last load whose copies were issued
+        for (int c = 0; c < 2 * n_kv; ++c) {
+            const int slot = c % NS, round = c / NS;
+            if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) break;
+            uint8_t *dst = smem + S::kRing + slot * S::kTileBytes;
+            const bool is_v = c & 1;
+            const int key0 = (c >> 1) * kBN;
             if (paged16) {
-                // lanes 0..7 each own one 16-token page of the step: one
+                // lanes 0..7 each own one 16-token page of the tile: one
                 // page-table read per lane, then that page's TMA boxes
-                if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], 2 * S::kTileBytes);
+                if (lane == 0) mbar_arrive_expect_tx(&full[slot], S::kTileBytes);
                 __syncwarp();
                 if (lane < kBN / 16) {
                     const int kk = key0 + lane * 16;
@@ -222,43 +238,48 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                         if (page >= 0 && (int64_t)page * 16 < a.num_slots) slot0 = page * 16;
                         else raise_error(PA_DEVERR_PAGE_RANGE);
                     }
+                    const CUtensorMap *map = is_v ? &a.vmap : &a.kmap;
 #pragma unroll
-                    for (int hh = 0; hh < H; ++hh) {
-                        tma_load_3d(sK + hh * 16384 + lane * 2048, &a.kmap, hh * 64, kvh, slot0, &kv_full[st]);
-                        tma_load_3d(sV + hh * 16384 + lane * 2048, &a.vmap, hh * 64, kvh, slot0, &kv_full[st]);
-                    }
+                    for (int hh = 0; hh < H; ++hh)
+                        tma_load_3d(dst + hh * 16384 + lane * 2048, map, hh * 64, kvh, slot0, &full[slot]);
                 }
             } else {
                 // page size 1: each lane gathers 4 key rows with cp.async,
                 // writing the 128-byte-swizzled layout TMA would produce
+                const uint8_t *src = is_v ? a.v_cache : a.k_cache;
 #pragma unroll
                 for (int rr = 0; rr < kBN / 32; ++rr) {
                     const int r = rr * 32 + lane;
                     const int key = key0 + r;
-                    int64_t slot = -1;
+                    int64_t row = -1;
                     if (key < kv_end) {
-                        slot = pt[key];
-                        if (slot < 0 || slot >= a.num_slots) { raise_error(PA_DEVERR_PAGE_RANGE); slot = -1; }
+                        row = pt[key];
+                        if (row < 0 || row >= a.num_slots) { raise_error(PA_DEVERR_PAGE_RANGE); row = -1; }
                     }
                     for (int hh = 0; hh < H; ++hh) {
-                        for (int c = 0; c < 8; ++c) {
-                            const int so = hh * 16384 + r * 128 + ((c ^ (r & 7)) * 16);
-                            if (slot >= 0) {
-                                const int64_t go = (slot * a.num_kv_heads + kvh) * (int64_t)D * 2 + hh * 128 + c * 16;
-                                cp_async16(sK + so, a.k_cache + go);
-                                cp_async16(sV + so, a.v_cache + go);
-                            } else {
-                                *reinterpret_cast<uint4 *>(sK + so) = make_uint4(0, 0, 0, 0);
-                                *reinterpret_cast<uint4 *>(sV + so) = make_uint4(0, 0, 0, 0);
-                            }
+                        for (int q = 0; q < 8; ++q) {
+                            const int so = hh * 16384 + r * 128 + ((q ^ (r & 7)) * 16);
+                            if (row >= 0)
+                                cp_async16(dst + so, src + (row * a.num_kv_heads + kvh) * (int64_t)D * 2 + hh * 128 + q * 16);
+                            else
+                                *reinterpret_cast<uint4 *>(dst + so) = make_uint4(0, 0, 0, 0);
                         }
                     }
                 }
                 cp_async_commit();
-                cp_async_wait_all();
-                fence_proxy_async_smem();      // generic-proxy writes -> visible to the MMA
-                mbar_arrive(&kv_full[st]);
+                // keep one load in flight: the previous one is complete now
+                if (gathered >= 0) {
+                    cp_async_wait_1();
+                    fence_proxy_async_smem();      // generic-proxy writes -> visible to the MMA
+                    mbar_arrive(&full[gathered % NS]);
+                }
+                gathered = c;
             }
+        }
+        if (!paged16 && gathered >= 0) {
+            cp_async_wait_all();
+            fence_proxy_async_smem();
+            mbar_arrive(&full[gathered % NS]);
         }
       } else if (warp == kMma) {
         // ---------------------------------------------------------- MMA ----
@@ -268,11 +289,12 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             // Descriptors are built once; a k-step adds its byte offset >> 4 to
             // the 14-bit start-address field (shared addresses stay < 2^18).
             const uint64_t dq0 = umma_desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t dkv0 = umma_desc_sw128(smem_u32(smem + S::kKV), 16, 1024);
-            const uint64_t dv0 = umma_desc_sw128(smem_u32(smem + S::kKV + S::kTileBytes), 16384, 1024);
+            const uint64_t dk0 = umma_desc_sw128(smem_u32(smem + S::kRing), 16, 1024);
+            const uint64_t dv0 = umma_desc_sw128(smem_u32(smem + S::kRing), 16384, 1024);
+            auto wait_full = [&](int c) { return mbar_wait(&full[c % NS], (c / NS) & 1); };
             auto issue_s = [&](int k, int j) {
                 const uint64_t dq = dq0 + (uint64_t)((k * S::kTileBytes) >> 4);
-                const uint64_t dk = dkv0 + (uint64_t)(((j % kKVStages) * 2 * S::kTileBytes) >> 4);
+                const uint64_t dk = dk0 + (uint64_t)((((2 * j) % NS) * S::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t o = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
@@ -280,32 +302,32 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                 }
                 umma_commit(&s_full[k]);
             };
-            bool ok = mbar_wait(q_full, 0) && mbar_wait(&kv_full[0], 0);
+            bool ok = mbar_wait(q_full, 0) && wait_full(0);
             if (ok) {
                 tc_fence_after();
                 for (int k = 0; k < T; ++k) issue_s(k, 0);
+                umma_commit(&empty[0]);                        // K_0 consumed
             }
             for (int j = 0; ok && j < n_kv; ++j) {
-                const int st = j % kKVStages;
-                const uint64_t dv = dv0 + (uint64_t)((st * 2 * S::kTileBytes) >> 4);
+                const int cv = 2 * j + 1;
+                const uint64_t dv = dv0 + (uint64_t)(((cv % NS) * S::kTileBytes) >> 4);
                 for (int k = 0; k < T; ++k) {
                     if (!mbar_wait(&p_full[k], j & 1)) { ok = false; break; }
+                    if (k == 0 && !wait_full(cv)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t o_tm = tmem + 256 + kOCols * k;
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
                         umma_ts(o_tm, tmem + 128 * k + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                                 (j > 0 || kk > 0) ? 1u : 0u);
-                    if (k == T - 1) umma_commit(&kv_empty[st]);
+                    if (k == T - 1) umma_commit(&empty[cv % NS]);  // V_j consumed
                     if (j + 1 < n_kv) {
                         if (k == 0) {
-                            if (!mbar_wait(&kv_full[(j + 1) % kKVStages], ((j + 1) / kKVStages) & 1)) {
-                                ok = false;
-                                break;
-                            }
+                            if (!wait_full(2 * j + 2)) { ok = false; break; }
                             tc_fence_after();
                         }
                         issue_s(k, j + 1);
+                        if (k == T - 1) umma_commit(&empty[(2 * j + 2) % NS]);  // K_{j+1} consumed
                     }
                 }
             }
@@ -385,7 +407,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             for (int c = 0; c < kBN / 2; ++c) {
                 const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), c2, nm2);
                 float2 p;
-                if ((c & 3) == 3) {
+                if (kPolyEvery > 0 && (c % kPolyEvery) == kPolyEvery - 1) {
                     p = exp2_poly2(x);
                 } else {
                     p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
