@@ -16,17 +16,13 @@
 //     per token one cp.async.bulk of the K row and one of the V row (HPC*d
 //     contiguous bf16 each, >= 512 bytes), completion counted on the stage's
 //     mbarrier (transaction bytes);
-//   - HPC consumer warps, one per KV head.  A warp's lanes form 4 groups of
-//     8: group j takes token 4*step + j of the stage, lane i of the group owns
-//     16-byte chunks i (and i + 8 for d = 128) of the key row, so each quarter
-//     warp reads one contiguous 128-byte line of shared memory.  Dot products
-//     for the G query heads use packed f32x2 FMAs (one key value feeds G
-//     heads); three xor-shuffles finish each sum.  The online softmax runs in
-//     the log2 domain (scale * log2 e folded into q) and rescales lazily: the
-//     running maximum moves only when a stage maximum exceeds it by more than
-//     2^8, which keeps every exponent <= 8 and skips most O rescales exactly.
-//     P.V: each lane owns d/32 consecutive output dims for all G heads; the
-//     stage's probabilities are broadcast through a 16 x G float buffer.
+//   - HPC consumer warps, one per KV head.  Per stage a warp computes the
+//     16 x G scores and the P.V update with warp-level tensor-core MMAs
+//     (mma.sync m16n8k16; the GQA heads fill the MMA's 8 columns), reading K
+//     and V with ldmatrix from token rows padded by 16 bytes.  The online
+//     softmax runs in the log2 domain and rescales lazily: the running maximum
+//     moves only when a stage maximum exceeds it by more than 2^8, which keeps
+//     every exponent <= 8 and skips most O rescales exactly.
 // The whole kernel is bound by HBM: every K/V byte is read once.
 #include <cuda_bf16.h>
 
@@ -70,9 +66,33 @@ struct DecodeArgs {
 template <int D, int HPC>
 struct DecodeSmem {
     static constexpr int kRowBytes = HPC * D * 2;            // one token, CTA's KV heads
-    static constexpr int kStageBytes = 2 * kStageTok * kRowBytes;
+    static constexpr int kRowStride = kRowBytes + 16;        // +16 B: ldmatrix rows hit distinct banks
+    static constexpr int kStageBytes = 2 * kStageTok * kRowStride;
     static constexpr int kRingBytes = kStages * kStageBytes;
 };
+
+// Warp-level bf16 MMA, D(16x8, fp32) += A(16x16, row) * B(16x8, col).
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 b16 matrices from shared memory (each lane gives one row address).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
 
 // Locate item -> (b, split, hg) by binary search of the prefix array.
 __device__ __forceinline__ void locate_item(const int32_t *prefix, int num_seqs, int item,
@@ -95,8 +115,8 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kRingBytes);
     uint64_t *empty = full + kStages;
-    float *pbuf = reinterpret_cast<float *>(empty + kStages);     // [HPC][16][G]
-    int32_t *prefix = reinterpret_cast<int32_t *>(pbuf + HPC * kStageTok * G);  // [B+1]
+    uint16_t *pbuf = reinterpret_cast<uint16_t *>(empty + kStages);   // [HPC][8 heads][16 tokens] bf16
+    int32_t *prefix = reinterpret_cast<int32_t *>(pbuf + HPC * 8 * kStageTok);  // [B+1]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -171,8 +191,8 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
                     }
                     const int64_t row = page * a.page_size + (j % a.page_size);
                     const int64_t off = (row * a.num_kv_heads + (int64_t)hg * HPC) * D * 2;
-                    uint8_t *dst = ring + slot * S::kStageBytes + (lane >> 4) * (kStageTok * S::kRowBytes) +
-                                   tok * S::kRowBytes;
+                    uint8_t *dst = ring + slot * S::kStageBytes + (lane >> 4) * (kStageTok * S::kRowStride) +
+                                   tok * S::kRowStride;
                     const uint8_t *src = (lane < 16 ? a.k_cache : a.v_cache) + off;
                     bulk_g2s(dst, src, S::kRowBytes, &full[slot]);
                 }
@@ -182,11 +202,22 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
     }
 
     // ---------------------------------------------------- consumer warps ----
-    constexpr int NCH = D / 64;          // 16-byte key chunks per lane
-    constexpr int VPL = D / 32;          // output dims per lane
-    const int grp = lane >> 3;           // token within a step
-    const int sub = lane & 7;            // chunk owner
-    float *pw = pbuf + warp * kStageTok * G;
+    // The two contractions of a 16-token stage run on the warp-level tensor
+    // path (mma.sync m16n8k16, bf16 inputs, fp32 accumulate), one KV head per
+    // warp, its G query heads padded to the 8 columns of the MMA:
+    //   S   (16 tokens x 8 heads) = K (16 x d) . Q^T (d x 8)
+    //   O^T (d x 8 heads)        += V^T (d x 16 tokens) . P^T (16 x 8)
+    // The kernel stays bound by HBM; the tensor path only takes the dot
+    // products off the FMA and shuffle pipes.  Fragment coordinates: r8 =
+    // lane / 4, q4 = lane % 4; an S fragment holds tokens r8 and r8 + 8 of
+    // heads 2*q4 and 2*q4 + 1, an O^T fragment of d-tile mt holds dims
+    // 16*mt + r8 (+8) of the same two heads.
+    constexpr int KS = D / 16;                       // k-steps of S = d-tiles of O
+    const int r8 = lane >> 2, q4 = lane & 3;
+    uint16_t *pw = pbuf + warp * 8 * kStageTok;      // P^T as [8 heads][16 tokens] bf16
+    // ldmatrix: lane -> one row of one of the four 8x8 matrices
+    const int a_tok = (lane & 7) + 8 * ((lane >> 3) & 1), a_dim = 8 * (lane >> 4);   // K (row-major A)
+    const int v_tok = (lane & 7) + 8 * (lane >> 4), v_dim = 8 * ((lane >> 3) & 1);   // V (A = V^T)
     int stage_ctr = 0;
 
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
@@ -199,171 +230,136 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
         const int kvh = hg * HPC + warp;
         const int h0 = kvh * G;          // first query head of this KV head
 
-        // q for the G heads, this lane's chunks, pre-scaled by scale*log2(e)
-        float2 qv[G][NCH * 4];
+        // Q^T fragments of query head h0 + r8 (zero for the padding heads)
+        uint32_t qb[KS][2];
+        if (r8 < G) {
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.q + ((int64_t)b * a.num_q_heads + h0 + r8) * D);
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const uint4 *qrow = reinterpret_cast<const uint4 *>(a.q + ((int64_t)b * a.num_q_heads + h0 + g) * D);
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                uint4 w = __ldg(qrow + sub + 8 * c);
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    qv[g][c * 4 + e] = make_float2(bf16lo(ww[e]) * a.scale_log2, bf16hi(ww[e]) * a.scale_log2);
+            for (int kk = 0; kk < KS; ++kk) {
+                qb[kk][0] = __ldg(qrow + kk * 8 + q4);
+                qb[kk][1] = __ldg(qrow + kk * 8 + q4 + 4);
             }
-        }
-        float m_run[G], l_run[G];
-        float2 o[G][VPL / 2];
+        } else {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            m_run[g] = -INFINITY;
-            l_run[g] = 0.f;
-#pragma unroll
-            for (int e = 0; e < VPL / 2; ++e) o[g][e] = make_float2(0.f, 0.f);
+            for (int kk = 0; kk < KS; ++kk) qb[kk][0] = qb[kk][1] = 0u;
         }
+        float oacc[KS][4];
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY};
+        float l_run[2] = {0.f, 0.f};
 
         bool ok = true;
         for (int t0 = k0; t0 < k1; t0 += kStageTok, ++stage_ctr) {
             const int slot = stage_ctr % kStages;
             const int round = stage_ctr / kStages;
             if (!mbar_wait(&full[slot], round & 1)) { ok = false; break; }
+            __syncwarp();
             const int n = min(kStageTok, k1 - t0);
-            const uint8_t *Ks = ring + slot * S::kStageBytes + warp * D * 2;
-            const uint8_t *Vs = Ks + kStageTok * S::kRowBytes;
-
-            // ---- scores s[step][g] for token 4*step + grp (log2 domain)
-            float s[4][G];
-#pragma unroll
-            for (int st = 0; st < 4; ++st) {
-                const int t = st * 4 + grp;
-                float2 acc[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
-                if (t < n) {
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        const uint4 w = *reinterpret_cast<const uint4 *>(Ks + t * S::kRowBytes + (sub + 8 * c) * 16);
-                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 kf = make_float2(bf16lo(ww[e]), bf16hi(ww[e]));
-#pragma unroll
-                            for (int g = 0; g < G; ++g) acc[g] = ffma2(qv[g][c * 4 + e], kf, acc[g]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) s[st][g] = acc[g].x + acc[g].y;
+            uint8_t *kst = ring + slot * S::kStageBytes + warp * D * 2;
+            uint8_t *vst = kst + kStageTok * S::kRowStride;
+            if (n < kStageTok) {
+                // rows past the last token hold stale shared memory: P is 0
+                // there, but 0 * NaN is not, so the V rows are zeroed
+                constexpr int kChunks = D * 2 / 16;
+                for (int i = lane; i < (kStageTok - n) * kChunks; i += 32)
+                    *reinterpret_cast<uint4 *>(vst + (n + i / kChunks) * S::kRowStride + (i % kChunks) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                __syncwarp();
             }
-#pragma unroll
-            for (int st = 0; st < 4; ++st)
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float v = s[st][g];
-                    v += __shfl_xor_sync(0xffffffffu, v, 1);
-                    v += __shfl_xor_sync(0xffffffffu, v, 2);
-                    v += __shfl_xor_sync(0xffffffffu, v, 4);
-                    s[st][g] = (st * 4 + grp < n) ? v : -INFINITY;
-                }
+            const uint32_t ks = smem_u32(kst), vs = smem_u32(vst);
 
-            // ---- online softmax over the stage (lazy rescale)
+            // ---- S = K Q^T
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float mx = fmaxf(fmaxf(s[0][g], s[1][g]), fmaxf(s[2][g], s[3][g]));
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t af[4];
+                ldsm_x4(af, ks + a_tok * S::kRowStride + (kk * 16 + a_dim) * 2);
+                mma_bf16_16816(sc, af, qb[kk][0], qb[kk][1]);
+            }
+            // log2 domain; tokens past n masked
+            float x[4];
+            x[0] = r8 < n ? sc[0] * a.scale_log2 : -INFINITY;
+            x[1] = r8 < n ? sc[1] * a.scale_log2 : -INFINITY;
+            x[2] = r8 + 8 < n ? sc[2] * a.scale_log2 : -INFINITY;
+            x[3] = r8 + 8 < n ? sc[3] * a.scale_log2 : -INFINITY;
+
+            // ---- online softmax per head over the stage's 16 tokens (lazy
+            // rescale: the running maximum moves only by more than 2^8)
+            float p[4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float mx = fmaxf(x[j], x[2 + j]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                if (mx > m_run[g] + kLazyRescale) {      // warp-uniform decision
-                    const float alpha = fast_exp2(m_run[g] - mx);   // 0 when m_run = -inf
-                    l_run[g] *= alpha;
+                if (mx > m_run[j] + kLazyRescale) {
+                    const float alpha = fast_exp2(m_run[j] - mx);   // 0 when m_run = -inf
+                    l_run[j] *= alpha;
 #pragma unroll
-                    for (int e = 0; e < VPL / 2; ++e) {
-                        o[g][e].x *= alpha;
-                        o[g][e].y *= alpha;
+                    for (int mt = 0; mt < KS; ++mt) {
+                        oacc[mt][j] *= alpha;
+                        oacc[mt][2 + j] *= alpha;
                     }
-                    m_run[g] = mx;
+                    m_run[j] = mx;
                 }
-                float psum = 0.f;
-#pragma unroll
-                for (int st = 0; st < 4; ++st) {
-                    const float p = fast_exp2(s[st][g] - m_run[g]);
-                    s[st][g] = p;
-                    psum += p;
-                }
-                l_run[g] += psum;
+                p[j] = fast_exp2(x[j] - m_run[j]);
+                p[2 + j] = fast_exp2(x[2 + j] - m_run[j]);
+                l_run[j] += p[j] + p[2 + j];
             }
-            if (sub == 0) {
-#pragma unroll
-                for (int st = 0; st < 4; ++st)
-#pragma unroll
-                    for (int g = 0; g < G; ++g) pw[(st * 4 + grp) * G + g] = s[st][g];
-            }
+            // ---- P^T through shared memory into the B-fragment layout
+            pw[(2 * q4) * kStageTok + r8] = bf16_bits(p[0]);
+            pw[(2 * q4 + 1) * kStageTok + r8] = bf16_bits(p[1]);
+            pw[(2 * q4) * kStageTok + r8 + 8] = bf16_bits(p[2]);
+            pw[(2 * q4 + 1) * kStageTok + r8 + 8] = bf16_bits(p[3]);
             __syncwarp();
+            const uint32_t pb0 = *reinterpret_cast<const uint32_t *>(pw + r8 * kStageTok + 2 * q4);
+            const uint32_t pb1 = *reinterpret_cast<const uint32_t *>(pw + r8 * kStageTok + 2 * q4 + 8);
 
-            // ---- O += P V
-            for (int t = 0; t < n; ++t) {
-                float2 vf[VPL / 2];
-                if constexpr (VPL == 4) {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(Vs + t * S::kRowBytes + lane * 8);
-                    vf[0] = make_float2(bf16lo(w.x), bf16hi(w.x));
-                    vf[1] = make_float2(bf16lo(w.y), bf16hi(w.y));
-                } else {
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(Vs + t * S::kRowBytes + lane * 4);
-                    vf[0] = make_float2(bf16lo(w), bf16hi(w));
-                }
-                float pv[G];
-                if constexpr (G % 4 == 0) {
+            // ---- O^T += V^T P^T
 #pragma unroll
-                    for (int g = 0; g < G; g += 4) {
-                        const float4 p4 = *reinterpret_cast<const float4 *>(pw + t * G + g);
-                        pv[g] = p4.x; pv[g + 1] = p4.y; pv[g + 2] = p4.z; pv[g + 3] = p4.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int g = 0; g < G; ++g) pv[g] = pw[t * G + g];
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float2 pp = make_float2(pv[g], pv[g]);
-#pragma unroll
-                    for (int e = 0; e < VPL / 2; ++e) o[g][e] = ffma2(pp, vf[e], o[g][e]);
-                }
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t vf[4];
+                ldsm_x4_trans(vf, vs + v_tok * S::kRowStride + (mt * 16 + v_dim) * 2);
+                mma_bf16_16816(oacc[mt], vf, pb0, pb1);
             }
+            // the zeroed rows were generic-proxy writes; the next bulk copy
+            // into this slot is an async-proxy write
+            if (n < kStageTok) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
         }
         if (!ok) return;
 
-        // ---- finish: l over the four token groups, normalise, write
+        // ---- finish: l over the stage rows (lanes with equal q4), write
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float l = l_run[g];
+        for (int j = 0; j < 2; ++j) {
+            float l = l_run[j];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
             l += __shfl_xor_sync(0xffffffffu, l, 8);
             l += __shfl_xor_sync(0xffffffffu, l, 16);
+            const int hh = 2 * q4 + j;                   // head within the group
+            if (hh >= G) continue;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const float lse_v = l > 0.f ? (m_run[g] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-            const int h = h0 + g;
+            const float lse_v = l > 0.f ? (m_run[j] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            const int h = h0 + hh;
             if (a.max_splits == 1) {
-                __nv_bfloat16 *orow = a.out + ((int64_t)b * a.num_q_heads + h) * D + lane * VPL;
-                if constexpr (VPL == 4) {
-                    uint2 w;
-                    w.x = pack_bf16x2(o[g][0].x * inv, o[g][0].y * inv);
-                    w.y = pack_bf16x2(o[g][1].x * inv, o[g][1].y * inv);
-                    *reinterpret_cast<uint2 *>(orow) = w;
-                } else {
-                    *reinterpret_cast<uint32_t *>(orow) = pack_bf16x2(o[g][0].x * inv, o[g][0].y * inv);
+                __nv_bfloat16 *orow = a.out + ((int64_t)b * a.num_q_heads + h) * D;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    orow[mt * 16 + r8] = __float2bfloat16_rn(oacc[mt][j] * inv);
+                    orow[mt * 16 + r8 + 8] = __float2bfloat16_rn(oacc[mt][2 + j] * inv);
                 }
-                if (a.lse != nullptr && lane == 0) a.lse[(int64_t)b * a.num_q_heads + h] = lse_v;
+                if (a.lse != nullptr && r8 == 0) a.lse[(int64_t)b * a.num_q_heads + h] = lse_v;
             } else {
                 const int64_t r = ((int64_t)b * a.num_q_heads + h) * a.max_splits + split;
-                float *orow = a.o_part + r * D + lane * VPL;
-                if constexpr (VPL == 4) {
-                    *reinterpret_cast<float4 *>(orow) =
-                        make_float4(o[g][0].x * inv, o[g][0].y * inv, o[g][1].x * inv, o[g][1].y * inv);
-                } else {
-                    *reinterpret_cast<float2 *>(orow) = make_float2(o[g][0].x * inv, o[g][0].y * inv);
+                float *orow = a.o_part + r * D;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    orow[mt * 16 + r8] = oacc[mt][j] * inv;
+                    orow[mt * 16 + r8 + 8] = oacc[mt][2 + j] * inv;
                 }
-                if (lane == 0) a.lse_part[r] = lse_v;
+                if (r8 == 0) a.lse_part[r] = lse_v;
             }
         }
     }
@@ -429,7 +425,7 @@ template <int D, int G, int HPC>
 cudaError_t launch_decode_t(const DecodeArgs &a, int64_t items_max, cudaStream_t stream) {
     using S = DecodeSmem<D, HPC>;
     const size_t smem = S::kRingBytes + 2 * kStages * sizeof(uint64_t) +
-                        HPC * kStageTok * G * sizeof(float) + (a.num_seqs + 1) * sizeof(int32_t);
+                        HPC * 8 * kStageTok * sizeof(uint16_t) + (a.num_seqs + 1) * sizeof(int32_t);
     auto kern = decode_kernel<D, G, HPC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
