@@ -203,6 +203,19 @@ class MixedBatch:
         return ev
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's time: every rank contributes its own measurement and
+    all receive the maximum (a plain all-reduce; nothing of the attention
+    path is exchanged between ranks)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -242,10 +255,7 @@ def run_gpu(args):
         phase["store_meta"].append(e[0].elapsed_time(e[1]))
         phase["prefill"].append(e[1].elapsed_time(e[2]))
         phase["decode"].append(e[2].elapsed_time(e[3]))
-    t = torch.tensor([total_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step = float(t.item()) / args.steps
+    ms_step = max_over_ranks(total_ms, world, dev) / args.steps
     from paged_kv_flashattention_gb300 import device_error
     dev_err = device_error()
 
@@ -276,10 +286,7 @@ def run_gpu(args):
         e2e_step()
     e2.record()
     torch.cuda.synchronize()
-    t2 = torch.tensor([s2.elapsed_time(e2)], device=dev)
-    if world > 1:
-        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
-    ms_e2e = float(t2.item()) / args.steps
+    ms_e2e = max_over_ranks(s2.elapsed_time(e2), world, dev) / args.steps
     h2d += 3 * 4 * (mb.dec.num_seqs + 1 + mb.pre.num_seqs + 1)   # metadata copies of both batches
 
     dec_ms = statistics.mean(phase["decode"])
