@@ -6,12 +6,17 @@
 // KV head (section 15); a long key range is cut into splits whose partial
 // (m, l, O) are merged by a numerically stable combine (sections 12, 16).
 //
-// Work decomposition (GB300 design, not the pages'): a work ITEM is
-// (sequence b, split s, KV-head group hg): kv_chunk keys of HPC consecutive KV
-// heads, i.e. HPC*G query heads.  Each CTA is persistent; it builds the
-// compacted item list from cache_seqlens in shared memory (a prefix sum of
-// ceil(Lk_b / kv_chunk) per sequence, so no CTA is spent on empty splits) and
-// takes items round robin.  Within a CTA:
+// Work decomposition (GB300 design, not the pages'): the work is the list of
+// (sequence b, KV-head group hg, token t) rows laid out sequence-major, a
+// group being HPC consecutive KV heads (HPC*G query heads).  CTAs are
+// persistent and each takes one contiguous, equal-sized range of that list
+// (T rows, T a multiple of 16 chosen on the device from the actual lengths,
+// never below the host's minimum split), so every CTA streams the same number
+// of K/V bytes whatever the length mix.  A range covers one or more row
+// segments; each segment yields a partial (O_s, lse_s) for split s = (CTA
+// index) - (index of the CTA where its row starts), and a combine pass merges
+// them.  CTA 0 publishes T and the length prefix in the workspace header for
+// the combine.  Within a CTA:
 //   - one producer warp streams 16-token stages into a ring of NST stages:
 //     per token one cp.async.bulk of the K row and one of the V row (HPC*d
 //     contiguous bf16 each, >= 512 bytes), completion counted on the stage's
@@ -54,13 +59,16 @@ struct DecodeArgs {
     int32_t page_size;
     int64_t num_pages;
     float scale_log2;
-    int32_t kv_chunk;
+    int32_t min_split;            // smallest T (tokens per CTA range)
+    int32_t max_seqlen_k;
     int32_t max_splits;
     int32_t head_groups;
     __nv_bfloat16 *out;
     float *lse;
     float *o_part;
     float *lse_part;
+    int32_t *ws_header;           // [0] = T
+    int32_t *ws_prefix;           // [B+1] exclusive prefix of the sequence lengths
 };
 
 template <int D, int HPC>
@@ -94,19 +102,33 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
-// Locate item -> (b, split, hg) by binary search of the prefix array.
-__device__ __forceinline__ void locate_item(const int32_t *prefix, int num_seqs, int item,
-                                            int head_groups, int &b, int &split, int &hg) {
-    int lo = 0, hi = num_seqs;  // prefix[lo] <= item < prefix[hi]
-    while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= item) lo = mid; else hi = mid;
+// Walks the segments of one CTA's range [g, g1) of the sequence-major row
+// list; pb is the exclusive prefix of the sequence lengths, so sequence b's
+// rows start at HG * pb[b] and row (b, hg) at HG * pb[b] + hg * L_b.
+struct SegmentWalk {
+    const int32_t *pb;
+    int B, HG, cta;
+    int64_t T, g, g1;
+    __device__ bool next(int &b, int &hg, int &t0, int &t1, int &split) {
+        if (g >= g1) return false;
+        int lo = 0, hi = B;           // HG * pb[lo] <= g < HG * pb[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if ((int64_t)HG * pb[mid] <= g) lo = mid; else hi = mid;
+        }
+        b = lo;
+        const int L = pb[b + 1] - pb[b];                  // > 0 by the invariant
+        const int64_t local = g - (int64_t)HG * pb[b];
+        hg = (int)(local / L);
+        t0 = (int)(local % L);
+        const int64_t want = (int64_t)t0 + (g1 - g);
+        t1 = want < L ? (int)want : L;
+        const int64_t row_start = (int64_t)HG * pb[b] + (int64_t)hg * L;
+        split = cta - (int)(row_start / T);
+        g += t1 - t0;
+        return true;
     }
-    b = lo;
-    int r = item - prefix[lo];
-    split = r / head_groups;
-    hg = r % head_groups;
-}
+};
 
 template <int D, int G, int HPC>
 __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs a) {
@@ -121,17 +143,17 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int B = a.num_seqs;
-    const int C = a.kv_chunk;
+    const int HG = a.head_groups;
 
-    // Compacted item list: prefix[b] = sum_{b' < b} n_b * head_groups with
-    // n_b = ceil(Lk_b / C) splits (one for an empty sequence, so its output
-    // row is still written).  Loaded by all threads, scanned by warp 0.
+    // Exclusive prefix of the sequence lengths (clamped to max_seqlen_k):
+    // loaded by all threads, scanned by warp 0.
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         int L = a.cache_seqlens[b];
-        if (L < 0) { raise_error(PA_DEVERR_SEQLENS); L = 0; }
-        int n = L > 0 ? (L + C - 1) / C : 1;
-        if (n > a.max_splits) { raise_error(PA_DEVERR_SEQLENS); n = a.max_splits; }
-        prefix[b + 1] = n * a.head_groups;
+        if (L < 0 || L > a.max_seqlen_k) {
+            raise_error(PA_DEVERR_SEQLENS);
+            L = L < 0 ? 0 : a.max_seqlen_k;
+        }
+        prefix[b + 1] = L;
     }
     if (threadIdx.x == 0) {
         prefix[0] = 0;
@@ -161,18 +183,24 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
         }
     }
     __syncthreads();
-    const int num_items = prefix[B];
+    // equal ranges of T rows (a multiple of 16, at least min_split)
+    const int64_t total = (int64_t)HG * prefix[B];
+    int64_t T = (total + gridDim.x - 1) / gridDim.x;
+    T = (T + 15) / 16 * 16;
+    if (T < a.min_split) T = a.min_split;
+    if (blockIdx.x == 0) {
+        for (int b = threadIdx.x; b <= B; b += blockDim.x) a.ws_prefix[b] = prefix[b];
+        if (threadIdx.x == 0) a.ws_header[0] = (int32_t)T;
+    }
+    const int64_t g0 = (int64_t)blockIdx.x * T;
+    const int64_t g1 = min(g0 + T, total);
 
     if (warp == HPC) {
         // ------------------------------------------------ producer warp ----
         int stage_ctr = 0;
-        for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-            int b, split, hg;
-            locate_item(prefix, B, item, a.head_groups, b, split, hg);
-            int Lk = min(a.cache_seqlens[b], a.max_splits * C);
-            if (Lk < 0) Lk = 0;
-            const int k0 = split * C;
-            const int k1 = min(Lk, k0 + C);
+        SegmentWalk walk{prefix, B, HG, (int)blockIdx.x, T, g0, g1};
+        int b, hg, k0, k1, split;
+        while (walk.next(b, hg, k0, k1, split)) {
             const int32_t *pt = a.page_table + (int64_t)b * a.pt_stride;
             for (int t0 = k0; t0 < k1; t0 += kStageTok, ++stage_ctr) {
                 const int slot = stage_ctr % kStages;
@@ -220,13 +248,9 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
     const int v_tok = (lane & 7) + 8 * (lane >> 4), v_dim = 8 * ((lane >> 3) & 1);   // V (A = V^T)
     int stage_ctr = 0;
 
-    for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-        int b, split, hg;
-        locate_item(prefix, B, item, a.head_groups, b, split, hg);
-        int Lk = min(a.cache_seqlens[b], a.max_splits * C);
-        if (Lk < 0) Lk = 0;
-        const int k0 = split * C;
-        const int k1 = min(Lk, k0 + C);
+    SegmentWalk walk{prefix, B, HG, (int)blockIdx.x, T, g0, g1};
+    int b, hg, k0, k1, split;
+    while (walk.next(b, hg, k0, k1, split)) {
         const int kvh = hg * HPC + warp;
         const int h0 = kvh * G;          // first query head of this KV head
 
@@ -343,24 +367,18 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const float lse_v = l > 0.f ? (m_run[j] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             const int h = h0 + hh;
-            if (a.max_splits == 1) {
-                __nv_bfloat16 *orow = a.out + ((int64_t)b * a.num_q_heads + h) * D;
-#pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    orow[mt * 16 + r8] = __float2bfloat16_rn(oacc[mt][j] * inv);
-                    orow[mt * 16 + r8 + 8] = __float2bfloat16_rn(oacc[mt][2 + j] * inv);
-                }
-                if (a.lse != nullptr && r8 == 0) a.lse[(int64_t)b * a.num_q_heads + h] = lse_v;
-            } else {
-                const int64_t r = ((int64_t)b * a.num_q_heads + h) * a.max_splits + split;
-                float *orow = a.o_part + r * D;
-#pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    orow[mt * 16 + r8] = oacc[mt][j] * inv;
-                    orow[mt * 16 + r8 + 8] = oacc[mt][2 + j] * inv;
-                }
-                if (r8 == 0) a.lse_part[r] = lse_v;
+            if (split < 0 || split >= a.max_splits) {       // cannot happen for valid lengths
+                raise_error(PA_DEVERR_SEQLENS);
+                continue;
             }
+            const int64_t r = ((int64_t)b * a.num_q_heads + h) * a.max_splits + split;
+            float *orow = a.o_part + r * D;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                orow[mt * 16 + r8] = oacc[mt][j] * inv;
+                orow[mt * 16 + r8 + 8] = oacc[mt][2 + j] * inv;
+            }
+            if (r8 == 0) a.lse_part[r] = lse_v;
         }
     }
 }
@@ -369,8 +387,9 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
 template <int D>
 __global__ void __launch_bounds__(256) lse_combine_kernel(
     const float *__restrict__ o_part, const float *__restrict__ lse_part,
-    const int32_t *__restrict__ splits_per_row, const int32_t *__restrict__ cache_seqlens,
-    int32_t kv_chunk, int32_t heads_per_seq, int32_t num_rows, int32_t max_splits,
+    const int32_t *__restrict__ splits_per_row, const int32_t *__restrict__ seg_header,
+    const int32_t *__restrict__ seg_prefix, int32_t head_groups, int32_t heads_per_group,
+    int32_t heads_per_seq, int32_t num_rows, int32_t max_splits,
     __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out) {
     constexpr int VPL = D / 32;
     const int lane = threadIdx.x & 31;
@@ -379,9 +398,13 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(
     int n = max_splits;
     if (splits_per_row != nullptr) {
         n = splits_per_row[row];
-    } else if (cache_seqlens != nullptr) {
-        const int L = cache_seqlens[row / heads_per_seq];
-        n = L > 0 ? (L + kv_chunk - 1) / kv_chunk : 0;
+    } else if (seg_header != nullptr) {
+        // decode: the row's splits are the CTA ranges of T rows it overlaps
+        const int64_t T = seg_header[0];
+        const int b = row / heads_per_seq, hg = (row % heads_per_seq) / heads_per_group;
+        const int L = seg_prefix[b + 1] - seg_prefix[b];
+        const int64_t rs = (int64_t)head_groups * seg_prefix[b] + (int64_t)hg * L;
+        n = L > 0 ? (int)((rs + L - 1) / T - rs / T + 1) : 0;
     }
     n = max(0, min(n, max_splits));
     const float *lrow = lse_part + (int64_t)row * max_splits;
@@ -470,23 +493,20 @@ DecodePlan plan_decode(const pa_decode_params &p) {
     int hpc = 1;
     while (hpc * 2 <= 4 && p.num_kv_heads % (hpc * 2) == 0) hpc *= 2;
     plan.heads_per_cta = hpc;
+    // Minimum split (the floor of T): the caller's kv_chunk, else 1/32 of the
+    // longest context (>= 64 keys).  It bounds the splits of one row by
+    // ceil(max_seqlen_k / min_split) + 1 and with it the workspace.
     int32_t chunk = p.kv_chunk;
     if (chunk <= 0) {
-        // about 16 splits for the longest sequence, 128..1024 keys each
-        chunk = (p.max_seqlen_k / 16 + 15) / 16 * 16;
-        if (chunk < 128) chunk = 128;
-        if (chunk > 1024) chunk = 1024;
+        chunk = (p.max_seqlen_k / 32 + 15) / 16 * 16;
+        if (chunk < 64) chunk = 64;
     }
     plan.kv_chunk = chunk;
-    plan.max_splits = p.max_seqlen_k > 0 ? (p.max_seqlen_k + chunk - 1) / chunk : 1;
-    if (plan.max_splits <= 1) {
-        plan.max_splits = 1;
-        plan.workspace_bytes = 0;
-    } else {
-        const size_t rows = (size_t)p.num_seqs * p.num_q_heads * plan.max_splits;
-        const size_t obytes = rows * p.head_dim * sizeof(float);
-        plan.workspace_bytes = ((obytes + 255) / 256) * 256 + rows * sizeof(float);
-    }
+    plan.max_splits = (p.max_seqlen_k + chunk - 1) / chunk + 1;
+    const size_t rows = (size_t)p.num_seqs * p.num_q_heads * plan.max_splits;
+    const size_t header = 256 + (((size_t)p.num_seqs + 1) * sizeof(int32_t) + 255) / 256 * 256;
+    const size_t obytes = (rows * p.head_dim * sizeof(float) + 255) / 256 * 256;
+    plan.workspace_bytes = header + obytes + rows * sizeof(float);
     return plan;
 }
 
@@ -504,32 +524,40 @@ cudaError_t launch_decode(const pa_decode_params &p, const DecodePlan &plan, cud
     a.page_size = p.page_size;
     a.num_pages = p.num_pages;
     a.scale_log2 = p.scale * 1.4426950408889634f;
-    a.kv_chunk = plan.kv_chunk;
+    a.min_split = plan.kv_chunk;
+    a.max_seqlen_k = p.max_seqlen_k;
     a.max_splits = plan.max_splits;
     a.head_groups = p.num_kv_heads / plan.heads_per_cta;
     a.out = static_cast<__nv_bfloat16 *>(p.out);
     a.lse = p.lse;
-    if (plan.max_splits > 1) {
+    {
+        // workspace: [T | pad to 256][prefix B+1 | pad][O partials][lse partials]
+        uint8_t *ws = static_cast<uint8_t *>(p.workspace);
         const size_t rows = (size_t)p.num_seqs * p.num_q_heads * plan.max_splits;
-        const size_t obytes = ((rows * p.head_dim * sizeof(float) + 255) / 256) * 256;
-        a.o_part = static_cast<float *>(p.workspace);
-        a.lse_part = reinterpret_cast<float *>(static_cast<uint8_t *>(p.workspace) + obytes);
+        const size_t pre = (((size_t)p.num_seqs + 1) * sizeof(int32_t) + 255) / 256 * 256;
+        const size_t obytes = (rows * p.head_dim * sizeof(float) + 255) / 256 * 256;
+        a.ws_header = reinterpret_cast<int32_t *>(ws);
+        a.ws_prefix = reinterpret_cast<int32_t *>(ws + 256);
+        a.o_part = reinterpret_cast<float *>(ws + 256 + pre);
+        a.lse_part = reinterpret_cast<float *>(ws + 256 + pre + obytes);
     }
     if (p.num_seqs == 0) return cudaSuccess;
-    // Upper bound of items: every sequence at max length.
-    const int64_t items_max = (int64_t)p.num_seqs * plan.max_splits * a.head_groups;
+    // Upper bound of useful CTAs: every sequence at max length, minimal split.
+    const int64_t items_max = ((int64_t)p.num_seqs * p.max_seqlen_k * a.head_groups + plan.kv_chunk - 1) /
+                              plan.kv_chunk + 1;
     const int g = p.num_q_heads / p.num_kv_heads;
     cudaError_t e = p.head_dim == 64 ? dispatch_g<64>(a, g, plan.heads_per_cta, items_max, stream)
                                      : dispatch_g<128>(a, g, plan.heads_per_cta, items_max, stream);
-    if (e != cudaSuccess || plan.max_splits == 1) return e;
-    return launch_lse_combine(a.o_part, a.lse_part, nullptr, p.cache_seqlens, plan.kv_chunk,
-                              p.num_q_heads, p.num_seqs * p.num_q_heads, plan.max_splits,
-                              p.head_dim, p.out, p.lse, stream);
+    if (e != cudaSuccess) return e;
+    return launch_lse_combine(a.o_part, a.lse_part, nullptr, a.ws_header, a.ws_prefix, a.head_groups,
+                              g * plan.heads_per_cta, p.num_q_heads, p.num_seqs * p.num_q_heads,
+                              plan.max_splits, p.head_dim, p.out, p.lse, stream);
 }
 
 cudaError_t launch_lse_combine(const float *o_partial, const float *lse_partial,
-                               const int32_t *splits_per_row, const int32_t *cache_seqlens,
-                               int32_t kv_chunk, int32_t heads_per_seq, int32_t num_rows,
+                               const int32_t *splits_per_row, const int32_t *seg_header,
+                               const int32_t *seg_prefix, int32_t head_groups,
+                               int32_t heads_per_group, int32_t heads_per_seq, int32_t num_rows,
                                int32_t max_splits, int32_t head_dim, void *out, float *lse_out,
                                cudaStream_t stream) {
     if (num_rows == 0) return cudaSuccess;
@@ -538,12 +566,12 @@ cudaError_t launch_lse_combine(const float *o_partial, const float *lse_partial,
     auto *o = static_cast<__nv_bfloat16 *>(out);
     if (head_dim == 64)
         lse_combine_kernel<64><<<blocks, rows_per_block * 32, 0, stream>>>(
-            o_partial, lse_partial, splits_per_row, cache_seqlens, kv_chunk, heads_per_seq,
-            num_rows, max_splits, o, lse_out);
+            o_partial, lse_partial, splits_per_row, seg_header, seg_prefix, head_groups,
+            heads_per_group, heads_per_seq, num_rows, max_splits, o, lse_out);
     else
         lse_combine_kernel<128><<<blocks, rows_per_block * 32, 0, stream>>>(
-            o_partial, lse_partial, splits_per_row, cache_seqlens, kv_chunk, heads_per_seq,
-            num_rows, max_splits, o, lse_out);
+            o_partial, lse_partial, splits_per_row, seg_header, seg_prefix, head_groups,
+            heads_per_group, heads_per_seq, num_rows, max_splits, o, lse_out);
     return cudaGetLastError();
 }
 

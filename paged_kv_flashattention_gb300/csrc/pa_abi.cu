@@ -290,8 +290,9 @@ pa_status pa_lse_combine(const float *o_partial, const float *lse_partial, const
     if (num_rows == 0) return PA_OK;
     if (!out || (max_splits > 0 && (!o_partial || !lse_partial))) return fail(PA_ERR_INVALID, "NULL pointer");
     if (!aligned16(o_partial) || !aligned16(out)) return fail(PA_ERR_INVALID, "o_partial and out must be 16-byte aligned");
-    cudaError_t e = launch_lse_combine(o_partial, lse_partial, splits_per_row, nullptr, 1, 1, num_rows,
-                                       max_splits, head_dim, out, lse_out, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_lse_combine(o_partial, lse_partial, splits_per_row, nullptr, nullptr, 1, 1, 1,
+                                       num_rows, max_splits, head_dim, out, lse_out,
+                                       static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "lse_combine launch");
 }
 

@@ -28,9 +28,13 @@ struct DecodePlan {
 DecodePlan plan_decode(const pa_decode_params &p);
 cudaError_t launch_decode(const pa_decode_params &p, const DecodePlan &plan, cudaStream_t stream);
 
+// Merge split partials.  Row r's split count is splits_per_row[r] if given;
+// else, with seg_header / seg_prefix (decode), the number of T-row CTA ranges
+// its (sequence, head group) rows overlap; else max_splits.
 cudaError_t launch_lse_combine(const float *o_partial, const float *lse_partial,
-                               const int32_t *splits_per_row, const int32_t *cache_seqlens,
-                               int32_t kv_chunk, int32_t heads_per_seq, int32_t num_rows,
+                               const int32_t *splits_per_row, const int32_t *seg_header,
+                               const int32_t *seg_prefix, int32_t head_groups,
+                               int32_t heads_per_group, int32_t heads_per_seq, int32_t num_rows,
                                int32_t max_splits, int32_t head_dim, void *out, float *lse_out,
                                cudaStream_t stream);
 

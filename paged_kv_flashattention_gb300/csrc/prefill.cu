@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             for (int c = 0; c < kBN / 2; ++c) {
                 const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), c2, nm2);
                 float2 p;
-                if (kPolyEvery > 0 && (c % kPolyEvery) == kPolyEvery - 1) {
+                if (kPolyEvery > 0 && (c % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
                     p = exp2_poly2(x);
                 } else {
                     p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
