@@ -111,7 +111,78 @@ struct PrefillArgs {
     int32_t num_slots;
     int32_t causal;
     float scale_log2;
+    int32_t num_virtual;          // max_tiles * num_seqs * (Hq / T) work-item slots
+    int32_t *sched;               // [0] next item, [1] CTAs finished; both 0 between launches
 };
+
+// One work item: a 128-row query tile of T query heads of one request.
+struct PrefillItem {
+    int b, tile, h0, kvh, q0, Lk, off, rows_here, kv_end, n_kv, min_vis;
+};
+
+// Item v of the virtual list (k-th tile from the end of request b, head group
+// hp), k-major: every request's later, longer tiles come before its earlier
+// ones, so persistent CTAs taking items round robin start with the longest
+// work.  Returns false for a hole (request b has fewer than k + 1 tiles).
+template <int T>
+__device__ __forceinline__ bool prefill_item(const PrefillArgs &a, int v, PrefillItem &it) {
+    const int groups = a.num_q_heads / T;
+    const int hp = v % groups;
+    const int rest = v / groups;
+    const int b = rest % a.num_seqs;
+    const int k = rest / a.num_seqs;
+    const int q0 = a.cu_q[b];
+    const int Lq = a.cu_q[b + 1] - q0;
+    const int tiles = (Lq + kBM - 1) / kBM;
+    if (k >= tiles) return false;
+    it.b = b;
+    it.tile = tiles - 1 - k;
+    it.h0 = hp * T;
+    it.kvh = it.h0 / (a.num_q_heads / a.num_kv_heads);
+    it.q0 = q0;
+    it.Lk = a.cu_k[b + 1] - a.cu_k[b];
+    it.off = it.Lk - Lq;                                  // cached prefix length
+    it.rows_here = min(kBM, Lq - it.tile * kBM);
+    int kv_end = it.Lk;                                   // keys the tile's last row sees
+    if (a.causal) kv_end = min(it.Lk, it.off + it.tile * kBM + it.rows_here);
+    it.kv_end = kv_end < 0 ? 0 : kv_end;
+    it.n_kv = (it.kv_end + kBN - 1) / kBN;
+    // keys every row of the tile sees: steps entirely below this need no mask
+    const int mv = a.causal ? min(it.Lk, it.off + it.tile * kBM + 1) : it.Lk;
+    it.min_vis = mv < 0 ? 0 : mv;
+    return true;
+}
+
+// Next item for this CTA (producer lane 0), or -1 when none is left.  Items
+// are handed out by one counter in the order above, so CTAs that finish early
+// take more.  A hole means the whole row (k, b) is a hole, and the rows after
+// it often are too (short requests have few tiles): the counter is moved past
+// every hole row up to the next row with work before taking another number.
+template <int T>
+__device__ int prefill_fetch(const PrefillArgs &a) {
+    const int groups = a.num_q_heads / T;
+    const int rows = a.num_virtual / groups;
+    for (;;) {
+        const int v = atomicAdd(&a.sched[0], 1);
+        if (v >= a.num_virtual) return -1;
+        PrefillItem it;
+        if (prefill_item<T>(a, v, it)) return v;
+        int row = v / groups + 1;
+        for (; row < rows; ++row)
+            if (prefill_item<T>(a, row * groups, it)) break;
+        atomicMax(&a.sched[0], row * groups);
+    }
+}
+
+// Called once per CTA after its last fetch: the last CTA to finish resets the
+// counters for the next launch that uses them.
+__device__ void prefill_sched_done(const PrefillArgs &a) {
+    __threadfence();
+    if (atomicAdd(&a.sched[1], 1) == (int)gridDim.x - 1) {
+        atomicExch(&a.sched[0], 0);
+        atomicExch(&a.sched[1], 0);
+    }
+}
 
 // Shared memory: T query tiles, then a ring of K-or-V tile slots (as many as
 // fit next to Q in 227 KiB, at most 8), then the barriers.  K_j goes to slot
@@ -138,6 +209,7 @@ __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_
 // (64,512 in all); the softmax warpgroups raise theirs to 184 and the
 // producer/MMA warpgroup lowers its to 128: 256 * 184 + 128 * 128 = 63,488.
 constexpr int kSoftmaxRegs = 184;
+constexpr int kItemRing = 4;      // items published ahead of the consumers
 constexpr int kControlRegs = 128;
 
 template <int D, int T>
@@ -150,34 +222,24 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int b = blockIdx.z;
-    const int q0 = a.cu_q[b];
-    const int Lq = a.cu_q[b + 1] - q0;
-    const int Lk = a.cu_k[b + 1] - a.cu_k[b];
-    const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;     // later (heavier) tiles launch first
-    if (tile * kBM >= Lq) return;                               // uniform per CTA
-    const int h0 = blockIdx.y * T;                              // query heads h0 .. h0+T-1
-    const int kvh = h0 / (a.num_q_heads / a.num_kv_heads);
-    const int off = Lk - Lq;                                    // cached prefix length
-    const int rows_here = min(kBM, Lq - tile * kBM);
-    int kv_end = Lk;                                            // keys the tile's last row sees
-    if (a.causal) kv_end = min(Lk, off + tile * kBM + rows_here);
-    if (kv_end < 0) kv_end = 0;
-    const int n_kv = (kv_end + kBN - 1) / kBN;
-    // keys every row of the tile sees: steps entirely below this need no mask
-    int min_vis = a.causal ? min(Lk, off + tile * kBM + 1) : Lk;
-    if (min_vis < 0) min_vis = 0;
-
     uint8_t *sQ = smem + S::kQ;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBars);
     constexpr int NS = S::kSlots;
-    uint64_t *q_full = bars;                 // 1
-    uint64_t *full = bars + 1;               // NS: slot loaded
+    uint64_t *q_full = bars;                 // 1: Q tiles of the item loaded
+    uint64_t *q_empty = bars + 1;            // 1: every S MMA of the item done
+    uint64_t *full = bars + 2;               // NS: slot loaded
     uint64_t *empty = full + NS;             // NS: slot consumed by the MMAs
     uint64_t *s_full = empty + NS;           // T
     uint64_t *p_full = s_full + T;           // T
-    uint64_t *o_final = p_full + T;          // 1: every MMA of the CTA done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_final + 1);
+    uint64_t *o_final = p_full + T;          // 1: every MMA of an item (with keys) done
+    constexpr int R = kItemRing;
+    uint64_t *item_full = o_final + 1;       // R: item index published
+    uint64_t *item_empty = item_full + R;    // R: read by the MMA thread and every softmax warp
+    int *item_idx = reinterpret_cast<int *>(item_empty + R);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(item_idx + R);
+    // Each role walks the same item list and keeps its own counts of items
+    // (phase of q_full / q_empty), items with keys (phase of o_final), key
+    // steps (phase of s_full / p_full) and K/V loads (ring slot and phase).
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -186,6 +248,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     if (warp == kMma) tmem_alloc(tmem_slot, 512);
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], paged16 ? 1 : 32);
             mbar_init(&empty[s], 1);
@@ -195,6 +258,10 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             mbar_init(&p_full[k], 128);
         }
         mbar_init(o_final, 1);
+        for (int i = 0; i < R; ++i) {
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], 1 + 4 * T);
+        }
         fence_mbar_init();
     }
     tc_fence_before();
@@ -207,83 +274,110 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         if (T == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
       if (warp == kProducer) {
         // ----------------------------------------------------- producer ----
-        const int32_t *pt = a.page_table + (int64_t)b * a.pt_stride;
         if (lane == 0) {
             prefetch_tmap(&a.qmap);
             if (paged16) { prefetch_tmap(&a.kmap); prefetch_tmap(&a.vmap); }
-            mbar_arrive_expect_tx(q_full, T * S::kTileBytes);
-            for (int k = 0; k < T; ++k)
-                for (int hh = 0; hh < H; ++hh)
-                    tma_load_3d(sQ + k * S::kTileBytes + hh * 16384, &a.qmap, hh * 64, h0 + k,
-                                q0 + tile * kBM, q_full);
         }
-        // load c = 2j is K_j, c = 2j + 1 is V_j
-        int gathered = -1;                       // page size 1: last load whose copies were issued
-        for (int c = 0; c < 2 * n_kv; ++c) {
-            const int slot = c % NS, round = c / NS;
-            if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) break;
-            uint8_t *dst = smem + S::kRing + slot * S::kTileBytes;
-            const bool is_v = c & 1;
-            const int key0 = (c >> 1) * kBN;
-            if (paged16) {
-                // lanes 0..7 each own one 16-token page of the tile: one
-                // page-table read per lane, then that page's TMA boxes
-                if (lane == 0) mbar_arrive_expect_tx(&full[slot], S::kTileBytes);
-                __syncwarp();
-                if (lane < kBN / 16) {
-                    const int kk = key0 + lane * 16;
-                    int slot0 = a.num_slots;                // out of range: zero fill
-                    if (kk < kv_end) {
-                        const int page = pt[kk / 16];
-                        if (page >= 0 && (int64_t)page * 16 < a.num_slots) slot0 = page * 16;
-                        else raise_error(PA_DEVERR_PAGE_RANGE);
-                    }
-                    const CUtensorMap *map = is_v ? &a.vmap : &a.kmap;
-#pragma unroll
-                    for (int hh = 0; hh < H; ++hh)
-                        tma_load_3d(dst + hh * 16384 + lane * 2048, map, hh * 64, kvh, slot0, &full[slot]);
+        int local = 0, gl = 0;
+        PrefillItem it;
+        for (;;) {
+            int v = 0;
+            bool pub = true;
+            if (lane == 0) {
+                v = prefill_fetch<T>(a);
+                // publish the item (or the end mark) to the MMA and softmax warps
+                const int slot = local % R;
+                if (local >= R) pub = mbar_wait(&item_empty[slot], ((local / R) - 1) & 1);
+                if (pub) {
+                    item_idx[slot] = v;
+                    mbar_arrive(&item_full[slot]);
                 }
-            } else {
-                // page size 1: each lane gathers 4 key rows with cp.async,
-                // writing the 128-byte-swizzled layout TMA would produce
-                const uint8_t *src = is_v ? a.v_cache : a.k_cache;
+            }
+            v = __shfl_sync(0xffffffffu, v, 0);
+            if (!__shfl_sync(0xffffffffu, pub, 0) || v < 0) break;
+            prefill_item<T>(a, v, it);
+            // the Q buffer is free once every S MMA of the previous item ran
+            if (local > 0 && !mbar_wait(q_empty, (local - 1) & 1)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(q_full, T * S::kTileBytes);
+                for (int k = 0; k < T; ++k)
+                    for (int hh = 0; hh < H; ++hh)
+                        tma_load_3d(sQ + k * S::kTileBytes + hh * 16384, &a.qmap, hh * 64, it.h0 + k,
+                                    it.q0 + it.tile * kBM, q_full);
+            }
+            const int32_t *pt = a.page_table + (int64_t)it.b * a.pt_stride;
+            // load 2j is K_j, 2j + 1 is V_j; gl counts loads over the CTA's life
+            int gathered = -1;                   // page size 1: last load whose copies were issued
+            bool ok = true;
+            for (int c = 0; c < 2 * it.n_kv; ++c, ++gl) {
+                const int slot = gl % NS, round = gl / NS;
+                if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) { ok = false; break; }
+                uint8_t *dst = smem + S::kRing + slot * S::kTileBytes;
+                const bool is_v = c & 1;
+                const int key0 = (c >> 1) * kBN;
+                if (paged16) {
+                    // lanes 0..7 each own one 16-token page of the tile: one
+                    // page-table read per lane, then that page's TMA boxes
+                    if (lane == 0) mbar_arrive_expect_tx(&full[slot], S::kTileBytes);
+                    __syncwarp();
+                    if (lane < kBN / 16) {
+                        const int kk = key0 + lane * 16;
+                        int slot0 = a.num_slots;            // out of range: zero fill
+                        if (kk < it.kv_end) {
+                            const int page = pt[kk / 16];
+                            if (page >= 0 && (int64_t)page * 16 < a.num_slots) slot0 = page * 16;
+                            else raise_error(PA_DEVERR_PAGE_RANGE);
+                        }
+                        const CUtensorMap *map = is_v ? &a.vmap : &a.kmap;
 #pragma unroll
-                for (int rr = 0; rr < kBN / 32; ++rr) {
-                    const int r = rr * 32 + lane;
-                    const int key = key0 + r;
-                    int64_t row = -1;
-                    if (key < kv_end) {
-                        row = pt[key];
-                        if (row < 0 || row >= a.num_slots) { raise_error(PA_DEVERR_PAGE_RANGE); row = -1; }
+                        for (int hh = 0; hh < H; ++hh)
+                            tma_load_3d(dst + hh * 16384 + lane * 2048, map, hh * 64, it.kvh, slot0, &full[slot]);
                     }
-                    for (int hh = 0; hh < H; ++hh) {
-                        for (int q = 0; q < 8; ++q) {
-                            const int so = hh * 16384 + r * 128 + ((q ^ (r & 7)) * 16);
-                            if (row >= 0)
-                                cp_async16(dst + so, src + (row * a.num_kv_heads + kvh) * (int64_t)D * 2 + hh * 128 + q * 16);
-                            else
-                                *reinterpret_cast<uint4 *>(dst + so) = make_uint4(0, 0, 0, 0);
+                } else {
+                    // page size 1: each lane gathers 4 key rows with cp.async,
+                    // writing the 128-byte-swizzled layout TMA would produce
+                    const uint8_t *src = is_v ? a.v_cache : a.k_cache;
+#pragma unroll
+                    for (int rr = 0; rr < kBN / 32; ++rr) {
+                        const int r = rr * 32 + lane;
+                        const int key = key0 + r;
+                        int64_t row = -1;
+                        if (key < it.kv_end) {
+                            row = pt[key];
+                            if (row < 0 || row >= a.num_slots) { raise_error(PA_DEVERR_PAGE_RANGE); row = -1; }
+                        }
+                        for (int hh = 0; hh < H; ++hh) {
+                            for (int q = 0; q < 8; ++q) {
+                                const int so = hh * 16384 + r * 128 + ((q ^ (r & 7)) * 16);
+                                if (row >= 0)
+                                    cp_async16(dst + so, src + (row * a.num_kv_heads + it.kvh) * (int64_t)D * 2 + hh * 128 + q * 16);
+                                else
+                                    *reinterpret_cast<uint4 *>(dst + so) = make_uint4(0, 0, 0, 0);
+                            }
                         }
                     }
+                    cp_async_commit();
+                    // keep one load in flight: the previous one is complete now
+                    if (gathered >= 0) {
+                        cp_async_wait_1();
+                        fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA
+                        mbar_arrive(&full[gathered]);
+                    }
+                    gathered = slot;
                 }
-                cp_async_commit();
-                // keep one load in flight: the previous one is complete now
-                if (gathered >= 0) {
-                    cp_async_wait_1();
-                    fence_proxy_async_smem();      // generic-proxy writes -> visible to the MMA
-                    mbar_arrive(&full[gathered % NS]);
-                }
-                gathered = c;
             }
+            if (!paged16 && gathered >= 0) {
+                cp_async_wait_all();
+                fence_proxy_async_smem();
+                mbar_arrive(&full[gathered]);
+            }
+            if (!ok) break;
+            ++local;
         }
-        if (!paged16 && gathered >= 0) {
-            cp_async_wait_all();
-            fence_proxy_async_smem();
-            mbar_arrive(&full[gathered % NS]);
-        }
+        if (lane == 0) prefill_sched_done(a);
       } else if (warp == kMma) {
         // ---------------------------------------------------------- MMA ----
-        if (lane == 0 && n_kv > 0) {
+        if (lane == 0) {
             constexpr uint32_t idesc_s = umma_idesc_bf16(kBM, kBN, false);
             constexpr uint32_t idesc_o = umma_idesc_bf16(kBM, D, true);
             // Descriptors are built once; a k-step adds its byte offset >> 4 to
@@ -292,9 +386,9 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             const uint64_t dk0 = umma_desc_sw128(smem_u32(smem + S::kRing), 16, 1024);
             const uint64_t dv0 = umma_desc_sw128(smem_u32(smem + S::kRing), 16384, 1024);
             auto wait_full = [&](int c) { return mbar_wait(&full[c % NS], (c / NS) & 1); };
-            auto issue_s = [&](int k, int j) {
+            auto issue_s = [&](int k, int c) {            // S_k from the K tile of load c
                 const uint64_t dq = dq0 + (uint64_t)((k * S::kTileBytes) >> 4);
-                const uint64_t dk = dk0 + (uint64_t)((((2 * j) % NS) * S::kTileBytes) >> 4);
+                const uint64_t dk = dk0 + (uint64_t)(((c % NS) * S::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t o = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
@@ -302,36 +396,56 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                 }
                 umma_commit(&s_full[k]);
             };
-            bool ok = mbar_wait(q_full, 0) && wait_full(0);
-            if (ok) {
-                tc_fence_after();
-                for (int k = 0; k < T; ++k) issue_s(k, 0);
-                umma_commit(&empty[0]);                        // K_0 consumed
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int cv = 2 * j + 1;
-                const uint64_t dv = dv0 + (uint64_t)(((cv % NS) * S::kTileBytes) >> 4);
-                for (int k = 0; k < T; ++k) {
-                    if (!mbar_wait(&p_full[k], j & 1)) { ok = false; break; }
-                    if (k == 0 && !wait_full(cv)) { ok = false; break; }
+            int local = 0, gl = 0, gs = 0;
+            bool ok = true;
+            PrefillItem it;
+            while (ok) {
+                const int slot = local % R;
+                if (!mbar_wait(&item_full[slot], (local / R) & 1)) break;
+                const int v = item_idx[slot];
+                mbar_arrive(&item_empty[slot]);
+                if (v < 0) break;
+                prefill_item<T>(a, v, it);
+                const int n_kv = it.n_kv;
+                if (!mbar_wait(q_full, local & 1)) break;
+                if (n_kv > 0) {
+                    if (!wait_full(gl)) break;
                     tc_fence_after();
-                    const uint32_t o_tm = tmem + 256 + kOCols * k;
+                    for (int k = 0; k < T; ++k) issue_s(k, gl);
+                    umma_commit(&empty[gl % NS]);                        // K_0 consumed
+                }
+                if (n_kv <= 1) umma_commit(q_empty);                     // every S of the item issued
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    const int cv = gl + 2 * j + 1;
+                    const uint64_t dv = dv0 + (uint64_t)(((cv % NS) * S::kTileBytes) >> 4);
+                    for (int k = 0; k < T; ++k) {
+                        if (!mbar_wait(&p_full[k], (gs + j) & 1)) { ok = false; break; }
+                        if (k == 0 && !wait_full(cv)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t o_tm = tmem + 256 + kOCols * k;
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        umma_ts(o_tm, tmem + 128 * k + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                    if (k == T - 1) umma_commit(&empty[cv % NS]);  // V_j consumed
-                    if (j + 1 < n_kv) {
-                        if (k == 0) {
-                            if (!wait_full(2 * j + 2)) { ok = false; break; }
-                            tc_fence_after();
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            umma_ts(o_tm, tmem + 128 * k + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                        if (k == T - 1) umma_commit(&empty[cv % NS]);    // V_j consumed
+                        if (j + 1 < n_kv) {
+                            if (k == 0) {
+                                if (!wait_full(cv + 1)) { ok = false; break; }
+                                tc_fence_after();
+                            }
+                            issue_s(k, cv + 1);
+                            if (k == T - 1) {
+                                umma_commit(&empty[(cv + 1) % NS]);      // K_{j+1} consumed
+                                if (j + 2 == n_kv) umma_commit(q_empty);  // last S of the item
+                            }
                         }
-                        issue_s(k, j + 1);
-                        if (k == T - 1) umma_commit(&empty[(2 * j + 2) % NS]);  // K_{j+1} consumed
                     }
                 }
+                if (n_kv > 0) umma_commit(o_final);   // items without keys write zeros, no MMA
+                gl += 2 * n_kv;
+                gs += n_kv;
+                ++local;
             }
-            umma_commit(o_final);
         }
       }
     } else {
@@ -339,21 +453,34 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         if (T == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
         const int k = warp >> 2;                      // query tile (head h0 + k)
         const int r = threadIdx.x & 127;              // row within the tile = TMEM lane
-        const int qi = tile * kBM + r;                // query index within the request
-        const bool row_valid = r < rows_here;
-        const int vis_end = a.causal ? min(Lk, off + qi + 1) : Lk;   // keys [0, vis_end)
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t s_tm = tmem + lane_base + 128 * k;
         const uint32_t o_tm = tmem + lane_base + 256 + kOCols * k;
         const float2 c2 = make_float2(a.scale_log2, a.scale_log2);
+        int fin = 0, gs = 0, local = 0;
+        bool ok = true;
+        PrefillItem it;
+        while (ok) {
+        const int slot = local % R;
+        ok = __all_sync(0xffffffffu, mbar_wait(&item_full[slot], (local / R) & 1));
+        if (!ok) break;
+        const int v = item_idx[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&item_empty[slot]);
+        ++local;
+        if (v < 0) break;
+        prefill_item<T>(a, v, it);
+        const int n_kv = it.n_kv, Lk = it.Lk, off = it.off, min_vis = it.min_vis;
+        const int qi = it.tile * kBM + r;             // query index within the request
+        const bool row_valid = r < it.rows_here;
+        const int vis_end = a.causal ? min(Lk, off + qi + 1) : Lk;   // keys [0, vis_end)
         float m_run = -INFINITY;
         float l_run = 0.f;
-        bool ok = true;
         // tcgen05.ld / st are warp-collective (.sync.aligned): every branch
         // that encloses one is warp-uniform, and the warp reconverges after
         // each (per-lane) barrier wait.
         for (int j = 0; j < n_kv; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[k], j & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[k], (gs + j) & 1));
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[kBN];
@@ -425,11 +552,11 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             mbar_arrive(&p_full[k]);
         }
         // ---- epilogue: O / l -> bf16, lse
-        if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0));
+        if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_final, fin & 1));
         tc_fence_after();
         if (ok) {
-            const int64_t tok = (int64_t)q0 + qi;
-            const int h = h0 + k;
+            const int64_t tok = (int64_t)it.q0 + qi;
+            const int h = it.h0 + k;
             __nv_bfloat16 *orow = a.out + (tok * a.num_q_heads + h) * D;
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
@@ -445,19 +572,22 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                 if (row_valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
+                    for (int u = 0; u < 4; ++u) {
                         uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
-                        dst[v] = w;
+                        w.x = pack_bf16x2(__uint_as_float(orr[8 * u + 0]) * inv, __uint_as_float(orr[8 * u + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(orr[8 * u + 2]) * inv, __uint_as_float(orr[8 * u + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(orr[8 * u + 4]) * inv, __uint_as_float(orr[8 * u + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(orr[8 * u + 6]) * inv, __uint_as_float(orr[8 * u + 7]) * inv);
+                        dst[u] = w;
                     }
                 }
             }
             if (row_valid && a.lse != nullptr)
                 a.lse[(int64_t)h * a.lse_stride + tok] =
                     l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+        }
+        gs += n_kv;
+        fin += n_kv > 0;
         }
     }
     tc_fence_before();
@@ -517,6 +647,33 @@ cudaError_t launch_t(const PrefillArgs &a, dim3 grid, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Work counters of the prefill scheduler: kSchedSlots pairs per device, zero
+// at module load and reset to zero by the last CTA of every launch.  Launches
+// take pairs in turn, so launches that may run at the same time (different
+// streams) use different pairs as long as fewer than kSchedSlots prefill
+// launches are issued on the device between them.
+constexpr int kSchedSlots = 1024;
+static __device__ int32_t g_prefill_sched[2 * kSchedSlots];
+
+cudaError_t prefill_sched(int32_t **ptr) {
+    static std::mutex lock;
+    static int32_t *base[kMaxDevices] = {nullptr};
+    static uint32_t next[kMaxDevices] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(lock);
+    if (base[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_prefill_sched);
+        if (e != cudaSuccess) return e;
+        base[dev] = static_cast<int32_t *>(p);
+    }
+    *ptr = base[dev] + 2 * (next[dev]++ % kSchedSlots);
+    return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
@@ -547,8 +704,15 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     // two query heads per CTA whenever they share a KV head
     const int group = p.num_q_heads / p.num_kv_heads;
     const int T = (group % 2 == 0) ? 2 : 1;
-    dim3 grid((p.max_seqlen_q + kBM - 1) / kBM, p.num_q_heads / T, p.num_seqs);
-    if (grid.y > 65535 || grid.z > 65535) return cudaErrorNotSupported;
+    const int64_t max_tiles = (p.max_seqlen_q + kBM - 1) / kBM;
+    const int64_t virt = max_tiles * p.num_seqs * (p.num_q_heads / T);
+    if (virt > INT32_MAX) return cudaErrorNotSupported;
+    a.num_virtual = (int32_t)virt;
+    if (virt == 0) return cudaSuccess;
+    cudaError_t e = prefill_sched(&a.sched);
+    if (e != cudaSuccess) return e;
+    // persistent: one CTA per SM (each holds all 512 TMEM columns)
+    dim3 grid((unsigned)(virt < num_sms() ? virt : num_sms()));
     if (p.head_dim == 128)
         return T == 2 ? launch_t<128, 2>(a, grid, stream) : launch_t<128, 1>(a, grid, stream);
     return T == 2 ? launch_t<64, 2>(a, grid, stream) : launch_t<64, 1>(a, grid, stream);
