@@ -139,6 +139,11 @@ pa_status pa_build_page_table(const int32_t *token_table, int64_t token_table_st
  *   lse[h * lse_stride + t] = ln sum_j exp(scale * q . K_j)   (optional)
  * The score matrix never leaves the chip (tiled, online softmax; [T] s.11-12).
  * max_seqlen_q / max_seqlen_k must bound every request's Lq / Lk.
+ * Work is handed to persistent CTAs by a pair of device counters that the
+ * library owns (1024 pairs per device, taken in turn by successive calls and
+ * left at zero by every launch).  Calls whose kernels may run at the same
+ * time on one device (different streams) must therefore be fewer than 1024
+ * pa_prefill calls apart; calls on one stream never conflict.
  */
 typedef struct {
     const void *q;               /* bf16 [total_q, Hq, d] */
@@ -169,10 +174,15 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream);
 /*
  * pa_decode - decode attention ([T] s.13 and s.16): one query token per
  * sequence (q row b) attends to all cache_seqlens[b] keys of its page-table
- * row (the new token already stored).  The key range is cut into splits of
- * kv_chunk keys; each split yields a partial (O_s, lse_s) in the workspace
- * and a log-sum-exp combine pass merges them.  When every sequence fits one
- * split the first pass writes `out` directly and no combine runs.
+ * row (the new token already stored).  Work is balanced by keys, not by
+ * sequences: the batch's (sequence, head group, key) list is cut into equal
+ * ranges, one per resident CTA, and each range is never shorter than
+ * kv_chunk keys.  A sequence that spans several ranges gets one partial
+ * (O_s, lse_s) per range in the workspace; a second, log-sum-exp combine
+ * launch merges them into `out` (it always runs; a row with one partial is
+ * copied).  The split layout depends only on the device-side cache_seqlens,
+ * so it is the same on every call with the same lengths (run-to-run
+ * deterministic).
  */
 typedef struct {
     const void *q;               /* bf16 [num_seqs, Hq, d] */
@@ -193,13 +203,16 @@ typedef struct {
     float *lse;                  /* optional fp32 [num_seqs, Hq]; NULL = not written */
     void *workspace;             /* device, >= pa_decode_workspace_size(p) bytes */
     size_t workspace_bytes;
-    int32_t kv_chunk;            /* keys per split, multiple of 16; 0 = automatic */
+    int32_t kv_chunk;            /* minimum keys per split, multiple of 16;
+                                    0 = automatic (max_seqlen_k / 32, >= 64) */
 } pa_decode_params;
 
-/* Bytes of workspace pa_decode needs for these parameters (0 when a single
- * split covers max_seqlen_k).  Reads only host fields of *p. */
+/* Bytes of workspace pa_decode needs for these parameters (always > 0: a
+ * header, a length prefix, and partials for at most
+ * ceil(max_seqlen_k / kv_chunk) + 1 splits per (sequence, head)).  Reads
+ * only host fields of *p. */
 size_t pa_decode_workspace_size(const pa_decode_params *p);
-/* The split size pa_decode will use for these parameters. */
+/* The minimum split pa_decode will use for these parameters. */
 int32_t pa_decode_kv_chunk(const pa_decode_params *p);
 
 pa_status pa_decode(const pa_decode_params *p, void *stream);
