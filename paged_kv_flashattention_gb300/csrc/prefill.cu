@@ -10,16 +10,22 @@
 // mini-sglang 07": seqlens_q = extend_len, seqlens_k = device_len).
 //
 // GB300 design (the pages' prior art is Ampere/Hopper; this is not it).
-// One CTA = one 128-row query tile of T query heads that share a KV head
-// (T = 2 when the GQA group allows it), so every K/V tile feeds 2T MMAs.
-//   warp 4T (producer): TMA loads the T Q tiles once (64-column halves,
-//     128-byte swizzle, K-major), then per 128-key step the K and V tiles:
+// Persistent: one CTA per SM.  A work item is one 128-row query tile of T
+// query heads that share a KV head (T = 2 when the GQA group allows it), so
+// every K/V tile feeds 2T MMAs.  Items are ordered last tile first (the k-th
+// tile from the end of every request before any (k+1)-th) and handed out by a
+// device counter; the producer publishes each item index to the other roles
+// through a small ring of mbarriers, and TMEM, barriers and the K/V ring
+// carry over from one item to the next.
+//   warp 4T (producer): takes the next item, TMA-loads its T Q tiles
+//     (64-column halves, 128-byte swizzle, K-major) once the previous item's
+//     last score MMA is done, then per 128-key step the K and V tiles:
 //     page size 16 -> one 3-D TMA box of 16 tokens per page and half;
-//     page size 1  -> cp.async 16-byte rows placed in the same swizzled
-//     layout.  K and V tiles go to separate slots of one ring (5 slots of
-//     32 KiB for d = 128 next to 64 KiB of Q), so loads run several tiles
-//     ahead; pages past the visible keys are filled with zeros by
-//     out-of-range TMA coordinates.
+//     page size 1  -> cp.async 16-byte pieces of key rows placed in the same
+//     swizzled layout, shared round robin with warps 4T+2 and 4T+3.  K and V
+//     tiles go to separate slots of one ring (5 slots of 32 KiB for d = 128
+//     next to 64 KiB of Q), so loads run several tiles ahead; pages past the
+//     visible keys are filled with zeros by out-of-range TMA coordinates.
 //   warp 4T+1 (MMA): one thread issues tcgen05.mma.  Order per step j:
 //     PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...: S_k(j+1) overwrites the TMEM
 //     columns that PV_k(j) reads P from, which relies on tcgen05.mma ops of
@@ -203,7 +209,11 @@ struct PrefillSmem {
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// Page size 1: warps that gather K/V rows (the producer and the two warps of
+// the control warpgroup that have no other role), loads dealt out round
+// robin; each keeps one copy group in flight.  Measured on the extend
+// workload with page size 1: 1 warp 698 us, 2 warps 393 us, 3 warps 282 us.
+constexpr int kGatherWarps = 3;
 
 // Register split (T = 2): 384 threads launch with 168 registers each
 // (64,512 in all); the softmax warpgroups raise theirs to 184 and the
@@ -225,6 +235,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     uint8_t *sQ = smem + S::kQ;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBars);
     constexpr int NS = S::kSlots;
+    static_assert(kGatherWarps + 2 <= NS, "gathers in flight must leave ring slots for the MMA");
     uint64_t *q_full = bars;                 // 1: Q tiles of the item loaded
     uint64_t *q_empty = bars + 1;            // 1: every S MMA of the item done
     uint64_t *full = bars + 2;               // NS: slot loaded
@@ -234,7 +245,8 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     uint64_t *o_final = p_full + T;          // 1: every MMA of an item (with keys) done
     constexpr int R = kItemRing;
     uint64_t *item_full = o_final + 1;       // R: item index published
-    uint64_t *item_empty = item_full + R;    // R: read by the MMA thread and every softmax warp
+    uint64_t *item_empty = item_full + R;    // R: read by the MMA thread, every softmax warp
+                                             //    and (page size 1) the other gather warps
     int *item_idx = reinterpret_cast<int *>(item_empty + R);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(item_idx + R);
     // Each role walks the same item list and keeps its own counts of items
@@ -260,7 +272,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         mbar_init(o_final, 1);
         for (int i = 0; i < R; ++i) {
             mbar_init(&item_full[i], 1);
-            mbar_init(&item_empty[i], 1 + 4 * T);
+            mbar_init(&item_empty[i], 1 + 4 * T + (paged16 ? 0 : kGatherWarps - 1));
         }
         fence_mbar_init();
     }
@@ -268,6 +280,77 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    // Page size 1 gathers.  gather_rows reads the page-table entries of K or
+    // V tile c of item `it` (lane l holds keys l, l + 32, ...); gather_copy
+    // copies those rows with cp.async into ring slot gl in the 128-byte-
+    // swizzled layout TMA would produce (rows past the visible keys are
+    // zero), two key rows per instruction (16 lanes x 16 bytes per 256-byte
+    // row at d = 128), as one copy group.
+    auto gather_rows = [&](const PrefillItem &it, int c, int (&rows)[kBN / 32]) {
+        const int32_t *pt = a.page_table + (int64_t)it.b * a.pt_stride;
+        const int key0 = (c >> 1) * kBN;
+#pragma unroll
+        for (int rr = 0; rr < kBN / 32; ++rr) {
+            const int key = key0 + rr * 32 + lane;
+            rows[rr] = key < it.kv_end ? pt[key] : -1;
+        }
+    };
+    auto gather_copy = [&](const PrefillItem &it, int c, int gl, const int (&rows)[kBN / 32]) {
+        constexpr int kChunks = D / 8;                // 16-byte chunks per row
+        constexpr int kRowsPerIssue = 32 / kChunks;   // 2 (d = 128) or 4 (d = 64)
+        uint8_t *dst = smem + S::kRing + (gl % NS) * S::kTileBytes;
+        const uint8_t *src = (c & 1) ? a.v_cache : a.k_cache;
+        const int key0 = (c >> 1) * kBN;
+        const int q = lane % kChunks;                 // this lane's chunk of a row
+        const int hh = q / 8;
+        const int sub = lane / kChunks;
+        static_assert(kBN / 32 == 4, "row selection below assumes 4 blocks of 32 keys");
+        // rolled loops: the kernel's code is large and instruction fetch
+        // stalls were measured when this part was fully unrolled
+#pragma unroll 1
+        for (int rr = 0; rr < kBN / 32; ++rr) {
+            int row = rr == 0 ? rows[0] : rr == 1 ? rows[1] : rr == 2 ? rows[2] : rows[3];
+            if (key0 + rr * 32 + lane < it.kv_end && (row < 0 || row >= a.num_slots)) {
+                raise_error(PA_DEVERR_PAGE_RANGE);
+                row = -1;
+            }
+#pragma unroll 4
+            for (int i = 0; i < 32 / kRowsPerIssue; ++i) {
+                const int rl = i * kRowsPerIssue + sub;            // row within this block of 32
+                const int rowv = __shfl_sync(0xffffffffu, row, rl);
+                const int r = rr * 32 + rl;                        // row within the tile
+                const int so = hh * 16384 + r * 128 + (((q % 8) ^ (r & 7)) * 16);
+                if (rowv >= 0)
+                    cp_async16(dst + so, src + ((int64_t)rowv * a.num_kv_heads + it.kvh) * (int64_t)D * 2 + q * 16);
+                else
+                    *reinterpret_cast<uint4 *>(dst + so) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        cp_async_commit();
+    };
+    // The loads of one item that gather warp g issues (page size 1): loads
+    // g, g + kGatherWarps, ... of the CTA.  Each waits for its ring slot, is
+    // copied, and is signalled as soon as its copies are complete; the next
+    // load's page-table entries are read while the copies are in flight.
+    // False on a timeout.
+    auto gather_item = [&](const PrefillItem &it, int gl0, int g) {
+        const int n = 2 * it.n_kv;
+        int c = ((g - gl0) % kGatherWarps + kGatherWarps) % kGatherWarps;
+        if (c >= n) return true;
+        int rows[kBN / 32];
+        gather_rows(it, c, rows);
+        for (; c < n; c += kGatherWarps) {
+            const int gl = gl0 + c;
+            if (gl >= NS && !mbar_wait(&empty[gl % NS], ((gl / NS) - 1) & 1)) return false;
+            gather_copy(it, c, gl, rows);
+            if (c + kGatherWarps < n) gather_rows(it, c + kGatherWarps, rows);
+            cp_async_wait_all();
+            fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA
+            mbar_arrive(&full[gl % NS]);
+        }
+        return true;
+    };
 
     if (warp >= kProducer) {
         // ------------------------------------- producer / MMA warpgroup ----
@@ -278,103 +361,106 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             prefetch_tmap(&a.qmap);
             if (paged16) { prefetch_tmap(&a.kmap); prefetch_tmap(&a.vmap); }
         }
-        int local = 0, gl = 0;
-        PrefillItem it;
-        for (;;) {
+        // Take item n (lane 0) and publish its index, or the end mark, to
+        // the other roles.  Returns the index (all lanes), -2 on a timeout.
+        auto take = [&](int n) {
             int v = 0;
-            bool pub = true;
             if (lane == 0) {
                 v = prefill_fetch<T>(a);
-                // publish the item (or the end mark) to the MMA and softmax warps
-                const int slot = local % R;
-                if (local >= R) pub = mbar_wait(&item_empty[slot], ((local / R) - 1) & 1);
-                if (pub) {
+                const int slot = n % R;
+                if (n >= R && !mbar_wait(&item_empty[slot], ((n / R) - 1) & 1)) {
+                    v = -2;
+                } else {
                     item_idx[slot] = v;
                     mbar_arrive(&item_full[slot]);
                 }
             }
-            v = __shfl_sync(0xffffffffu, v, 0);
-            if (!__shfl_sync(0xffffffffu, pub, 0) || v < 0) break;
+            return __shfl_sync(0xffffffffu, v, 0);
+        };
+        // Page size 16: lanes 0..7 read the ids of the 8 pages of 128-key
+        // step j (-1 past the visible keys); page_slot0 turns one into the
+        // first slot of the page, num_slots (zero fill) when there is none or
+        // the id is outside the pool.  Split so that the read is in flight
+        // while the producer waits for a ring slot.
+        auto page_id = [&](const PrefillItem &it, int j) {
+            const int kk = j * kBN + lane * 16;
+            return (lane < kBN / 16 && kk < it.kv_end) ? a.page_table[(int64_t)it.b * a.pt_stride + kk / 16] : -1;
+        };
+        auto page_slot0 = [&](const PrefillItem &it, int j, int page) {
+            const int kk = j * kBN + lane * 16;
+            if (lane >= kBN / 16 || kk >= it.kv_end) return a.num_slots;
+            if (page >= 0 && (int64_t)page * 16 < a.num_slots) return page * 16;
+            raise_error(PA_DEVERR_PAGE_RANGE);
+            return a.num_slots;
+        };
+        int local = 0, gl = 0;
+        PrefillItem it;
+        // An item is taken when the previous one's loads are all issued (not
+        // earlier: a CTA that holds an item it has not started keeps it from
+        // CTAs that are idle at the end).
+        for (int v; (v = take(local)) >= 0;) {
             prefill_item<T>(a, v, it);
-            // the Q buffer is free once every S MMA of the previous item ran
-            if (local > 0 && !mbar_wait(q_empty, (local - 1) & 1)) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(q_full, T * S::kTileBytes);
-                for (int k = 0; k < T; ++k)
-                    for (int hh = 0; hh < H; ++hh)
-                        tma_load_3d(sQ + k * S::kTileBytes + hh * 16384, &a.qmap, hh * 64, it.h0 + k,
-                                    it.q0 + it.tile * kBM, q_full);
-            }
-            const int32_t *pt = a.page_table + (int64_t)it.b * a.pt_stride;
-            // load 2j is K_j, 2j + 1 is V_j; gl counts loads over the CTA's life
-            int gathered = -1;                   // page size 1: last load whose copies were issued
+            // load 2j is K_j, 2j + 1 is V_j; gl counts loads over the CTA's
+            // life.  The Q tiles are loaded once the previous item's last S
+            // MMA is done.
             bool ok = true;
-            for (int c = 0; c < 2 * it.n_kv; ++c, ++gl) {
-                const int slot = gl % NS, round = gl / NS;
-                if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) { ok = false; break; }
-                uint8_t *dst = smem + S::kRing + slot * S::kTileBytes;
-                const bool is_v = c & 1;
-                const int key0 = (c >> 1) * kBN;
-                if (paged16) {
-                    // lanes 0..7 each own one 16-token page of the tile: one
-                    // page-table read per lane, then that page's TMA boxes
+            auto load_q = [&]() {
+                if (local > 0 && !mbar_wait(q_empty, (local - 1) & 1)) return false;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(q_full, T * S::kTileBytes);
+                    for (int k = 0; k < T; ++k)
+                        for (int hh = 0; hh < H; ++hh)
+                            tma_load_3d(sQ + k * S::kTileBytes + hh * 16384, &a.qmap, hh * 64, it.h0 + k,
+                                        it.q0 + it.tile * kBM, q_full);
+                }
+                return true;
+            };
+            if (paged16) {
+                int page = page_id(it, 0);              // pages of the current step
+                int slot0 = a.num_slots;
+                ok = load_q();
+                for (int c = 0; ok && c < 2 * it.n_kv; ++c, ++gl) {
+                    if (!(c & 1)) slot0 = page_slot0(it, c >> 1, page);
+                    const int slot = gl % NS, round = gl / NS;
+                    if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) { ok = false; break; }
+                    uint8_t *dst = smem + S::kRing + slot * S::kTileBytes;
+                    // lanes 0..7 each own one 16-token page of the tile
                     if (lane == 0) mbar_arrive_expect_tx(&full[slot], S::kTileBytes);
                     __syncwarp();
                     if (lane < kBN / 16) {
-                        const int kk = key0 + lane * 16;
-                        int slot0 = a.num_slots;            // out of range: zero fill
-                        if (kk < it.kv_end) {
-                            const int page = pt[kk / 16];
-                            if (page >= 0 && (int64_t)page * 16 < a.num_slots) slot0 = page * 16;
-                            else raise_error(PA_DEVERR_PAGE_RANGE);
-                        }
-                        const CUtensorMap *map = is_v ? &a.vmap : &a.kmap;
+                        const CUtensorMap *map = (c & 1) ? &a.vmap : &a.kmap;
 #pragma unroll
                         for (int hh = 0; hh < H; ++hh)
                             tma_load_3d(dst + hh * 16384 + lane * 2048, map, hh * 64, it.kvh, slot0, &full[slot]);
                     }
-                } else {
-                    // page size 1: each lane gathers 4 key rows with cp.async,
-                    // writing the 128-byte-swizzled layout TMA would produce
-                    const uint8_t *src = is_v ? a.v_cache : a.k_cache;
-#pragma unroll
-                    for (int rr = 0; rr < kBN / 32; ++rr) {
-                        const int r = rr * 32 + lane;
-                        const int key = key0 + r;
-                        int64_t row = -1;
-                        if (key < it.kv_end) {
-                            row = pt[key];
-                            if (row < 0 || row >= a.num_slots) { raise_error(PA_DEVERR_PAGE_RANGE); row = -1; }
-                        }
-                        for (int hh = 0; hh < H; ++hh) {
-                            for (int q = 0; q < 8; ++q) {
-                                const int so = hh * 16384 + r * 128 + ((q ^ (r & 7)) * 16);
-                                if (row >= 0)
-                                    cp_async16(dst + so, src + (row * a.num_kv_heads + it.kvh) * (int64_t)D * 2 + hh * 128 + q * 16);
-                                else
-                                    *reinterpret_cast<uint4 *>(dst + so) = make_uint4(0, 0, 0, 0);
-                            }
-                        }
-                    }
-                    cp_async_commit();
-                    // keep one load in flight: the previous one is complete now
-                    if (gathered >= 0) {
-                        cp_async_wait_1();
-                        fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA
-                        mbar_arrive(&full[gathered]);
-                    }
-                    gathered = slot;
+                    // K_j and V_j share pages; after K_j start reading the next step's
+                    if (!(c & 1) && c + 2 < 2 * it.n_kv) page = page_id(it, (c >> 1) + 1);
                 }
-            }
-            if (!paged16 && gathered >= 0) {
-                cp_async_wait_all();
-                fence_proxy_async_smem();
-                mbar_arrive(&full[gathered]);
+            } else {
+                ok = load_q() && gather_item(it, gl, 0);
+                gl += 2 * it.n_kv;
             }
             if (!ok) break;
             ++local;
         }
         if (lane == 0) prefill_sched_done(a);
+      } else if (warp != kMma && !paged16 && warp - kMma < kGatherWarps) {
+        // --------------------------------- extra gather warps (page 1) ----
+        const int g = warp - kMma;                      // 1, 2
+        int local = 0, gl = 0;
+        PrefillItem it;
+        for (;;) {
+            const int slot = local % R;
+            if (!__all_sync(0xffffffffu, mbar_wait(&item_full[slot], (local / R) & 1))) break;
+            const int v = item_idx[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[slot]);
+            ++local;
+            if (v < 0) break;
+            prefill_item<T>(a, v, it);
+            if (!gather_item(it, gl, g)) break;
+            gl += 2 * it.n_kv;
+        }
       } else if (warp == kMma) {
         // ---------------------------------------------------------- MMA ----
         if (lane == 0) {
