@@ -191,29 +191,34 @@ __device__ void prefill_sched_done(const PrefillArgs &a) {
 }
 
 // Shared memory: T query tiles, then a ring of K-or-V tile slots (as many as
-// fit next to Q in 227 KiB, at most 8), then the barriers.  K_j goes to slot
+// fit in 227 KiB next to Q and the output staging, at most 8), then 4 KiB of
+// output staging per softmax warp, then the barriers.  K_j goes to slot
 // (2j) mod n and V_j to slot (2j+1) mod n, so the producer can run several
 // tiles ahead of the MMAs: with one CTA per SM the loads from L2 are latency
-// bound, and bytes in flight set the rate.
+// bound, and bytes in flight set the rate (at d = 128 with two heads, 4
+// slots measured as fast as 5).
 template <int D, int T>
 struct PrefillSmem {
     static constexpr int kHalves = D / 64;                 // 64-column (128-byte) halves
     static constexpr int kTileBytes = kHalves * 128 * 128; // 128 rows x D bf16
     static constexpr int kQ = 0;                           // T query tiles
     static constexpr int kRing = T * kTileBytes;
-    static constexpr int kSlotsFit = (232448 - 1024 - kRing - 512) / kTileBytes;
+    static constexpr int kStageBytes = 4 * T * 4096;      // 32 rows x 64 columns bf16 per warp
+    static constexpr int kSlotsFit = (232448 - 1024 - kRing - kStageBytes - 512) / kTileBytes;
     static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;
-    static constexpr int kBars = kRing + kSlots * kTileBytes;
+    static constexpr int kStage = kRing + kSlots * kTileBytes;
+    static constexpr int kBars = kStage + kStageBytes;
     static constexpr int kTotal = kBars + 512;
 };
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Page size 1: warps that gather K/V rows (the producer and the two warps of
-// the control warpgroup that have no other role), loads dealt out round
-// robin; each keeps one copy group in flight.  Measured on the extend
-// workload with page size 1: 1 warp 698 us, 2 warps 393 us, 3 warps 282 us.
-constexpr int kGatherWarps = 3;
+// the control warpgroup that have no other role, fewer if the ring is
+// shorter), loads dealt out round robin; each keeps one copy group in flight.
+// Measured on the extend workload with page size 1 (5 ring slots): 1 warp
+// 698 us, 2 warps 393 us, 3 warps 282 us.
+constexpr int kGatherWarpsMax = 3;
 
 // Register split (T = 2): 384 threads launch with 168 registers each
 // (64,512 in all); the softmax warpgroups raise theirs to 184 and the
@@ -235,16 +240,18 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     uint8_t *sQ = smem + S::kQ;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBars);
     constexpr int NS = S::kSlots;
-    static_assert(kGatherWarps + 2 <= NS, "gathers in flight must leave ring slots for the MMA");
+    // each gather warp has at most one load in flight and signals it when it
+    // is complete, so G < NS leaves the MMA a slot
+    constexpr int kGatherWarps = NS - 1 < kGatherWarpsMax ? NS - 1 : kGatherWarpsMax;
     uint64_t *q_full = bars;                 // 1: Q tiles of the item loaded
     uint64_t *q_empty = bars + 1;            // 1: every S MMA of the item done
     uint64_t *full = bars + 2;               // NS: slot loaded
     uint64_t *empty = full + NS;             // NS: slot consumed by the MMAs
     uint64_t *s_full = empty + NS;           // T
     uint64_t *p_full = s_full + T;           // T
-    uint64_t *o_final = p_full + T;          // 1: every MMA of an item (with keys) done
+    uint64_t *o_final = p_full + T;          // T: every MMA of O_k of an item (with keys) done
     constexpr int R = kItemRing;
-    uint64_t *item_full = o_final + 1;       // R: item index published
+    uint64_t *item_full = o_final + T;       // R: item index published
     uint64_t *item_empty = item_full + R;    // R: read by the MMA thread, every softmax warp
                                              //    and (page size 1) the other gather warps
     int *item_idx = reinterpret_cast<int *>(item_empty + R);
@@ -269,7 +276,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             mbar_init(&s_full[k], 1);
             mbar_init(&p_full[k], 128);
         }
-        mbar_init(o_final, 1);
+        for (int k = 0; k < T; ++k) mbar_init(&o_final[k], 1);
         for (int i = 0; i < R; ++i) {
             mbar_init(&item_full[i], 1);
             mbar_init(&item_empty[i], 1 + 4 * T + (paged16 ? 0 : kGatherWarps - 1));
@@ -514,6 +521,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                             umma_ts(o_tm, tmem + 128 * k + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                                     (j > 0 || kk > 0) ? 1u : 0u);
                         if (k == T - 1) umma_commit(&empty[cv % NS]);    // V_j consumed
+                        if (j + 1 == n_kv) umma_commit(&o_final[k]);     // O_k of the item complete
                         if (j + 1 < n_kv) {
                             if (k == 0) {
                                 if (!wait_full(cv + 1)) { ok = false; break; }
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                         }
                     }
                 }
-                if (n_kv > 0) umma_commit(o_final);   // items without keys write zeros, no MMA
+                // (items without keys write zeros and use no MMA)
                 gl += 2 * n_kv;
                 gs += n_kv;
                 ++local;
@@ -638,35 +646,52 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             mbar_arrive(&p_full[k]);
         }
         // ---- epilogue: O / l -> bf16, lse
-        if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_final, fin & 1));
+        if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_final[k], fin & 1));
         tc_fence_after();
         if (ok) {
             const int64_t tok = (int64_t)it.q0 + qi;
             const int h = it.h0 + k;
-            __nv_bfloat16 *orow = a.out + (tok * a.num_q_heads + h) * D;
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t orr[32];
+            // Through the warp's staging buffer, 64 columns at a time: each
+            // thread writes its row (16-byte pieces, XOR-swizzled by row so
+            // the writes and reads below are free of bank conflicts), then the
+            // warp stores 4 rows x 128 contiguous bytes per instruction.
+            uint8_t *stage = smem + S::kStage + warp * 4096;
+            const int rw = lane;                                   // row within the warp's 32
+#pragma unroll 1
+            for (int half = 0; half < D / 64; ++half) {
+                // both 32-column loads in flight before one wait
+                uint32_t orr[64];
                 if (n_kv > 0) {                       // CTA-uniform
-                    tmem_ld32(o_tm + c * 32, orr);
+                    tmem_ld32(o_tm + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&orr[0]));
+                    tmem_ld32(o_tm + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&orr[32]));
                     tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) orr[e] = 0u;
+                    for (int e = 0; e < 64; ++e) orr[e] = 0u;
                 }
-                if (row_valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(orr[8 * u + 0]) * inv, __uint_as_float(orr[8 * u + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(orr[8 * u + 2]) * inv, __uint_as_float(orr[8 * u + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(orr[8 * u + 4]) * inv, __uint_as_float(orr[8 * u + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(orr[8 * u + 6]) * inv, __uint_as_float(orr[8 * u + 7]) * inv);
-                        dst[u] = w;
+                for (int u = 0; u < 8; ++u) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(orr[8 * u + 0]) * inv, __uint_as_float(orr[8 * u + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(orr[8 * u + 2]) * inv, __uint_as_float(orr[8 * u + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(orr[8 * u + 4]) * inv, __uint_as_float(orr[8 * u + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(orr[8 * u + 6]) * inv, __uint_as_float(orr[8 * u + 7]) * inv);
+                    *reinterpret_cast<uint4 *>(stage + rw * 128 + ((u ^ (rw & 7)) * 16)) = w;
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = i * 4 + (lane >> 3);
+                    const int q = lane & 7;
+                    const uint4 val = *reinterpret_cast<const uint4 *>(stage + rr * 128 + ((q ^ (rr & 7)) * 16));
+                    const int rt = (warp & 3) * 32 + rr;                // row within the tile
+                    if (rt < it.rows_here) {
+                        const int64_t t = (int64_t)it.q0 + it.tile * kBM + rt;
+                        *reinterpret_cast<uint4 *>(a.out + (t * a.num_q_heads + h) * D + half * 64 + q * 8) = val;
                     }
                 }
+                __syncwarp();
             }
             if (row_valid && a.lse != nullptr)
                 a.lse[(int64_t)h * a.lse_stride + tok] =
