@@ -12,7 +12,8 @@ module compiles it with gcc and wraps it for numpy arrays.  ``online.py`` holds
 the online-softmax block merge and the split-KV merge written from sections 12
 and 16 of the first page; ``brute.py`` a tiny pure-Python brute force.
 
-All bf16 tensors cross this interface as ``numpy.uint16`` bit patterns.
+All bf16 tensors cross this interface as ``numpy.uint16`` bit patterns, FP8
+(E4M3) pools as ``numpy.uint8`` codes with float32 per-KV-head scales.
 """
 from __future__ import annotations
 
@@ -56,6 +57,15 @@ def _bind(lib):
     lib.oracle_attention.argtypes = [P, P, P, P, i64, P, P, i32, i32, i32, i32, i32,
                                      i64, ctypes.c_int, dbl, P, i64, P, P]
     lib.oracle_attention.restype = ctypes.c_int
+    lib.oracle_attention_fp8.argtypes = [P, P, P, P, P, P, i64, P, P, i32, i32, i32, i32, i32,
+                                         i64, ctypes.c_int, dbl, P, i64, P, P]
+    lib.oracle_attention_fp8.restype = ctypes.c_int
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_value.restype = dbl
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_store_kv_fp8.argtypes = [P, P, P, i64, P, P, i64, i32, i32, P, P]
+    lib.oracle_store_kv_fp8.restype = ctypes.c_int
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     return lib
@@ -124,6 +134,39 @@ def store_kv(k, v, slot_mapping, k_cache, v_cache, *, lib=None) -> None:
                                    slots, row), "oracle_store_kv")
 
 
+def e4m3_value(codes, *, lib=None) -> np.ndarray:
+    """float64 values of E4M3 codes (uint8), NaN for the NaN codes."""
+    c = np.asarray(codes, dtype=np.uint8)
+    lib = _load(lib)
+    table = np.array([lib.oracle_e4m3_value(i) for i in range(256)], dtype=np.float64)
+    return table[c]
+
+
+def e4m3_encode(x, *, lib=None) -> np.ndarray:
+    """Nearest E4M3 codes (uint8) of float32 values (ties to even, saturating)."""
+    xf = np.asarray(x, dtype=np.float32)
+    lib = _load(lib)
+    flat = [lib.oracle_e4m3_encode(float(v)) for v in xf.ravel()]
+    return np.array(flat, dtype=np.uint8).reshape(xf.shape)
+
+
+def store_kv_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, *, lib=None) -> None:
+    """FP8 KV-cache store into uint8 ``k_cache``/``v_cache`` ([slots, Hkv, d])
+    in place; k, v: bf16 bits [T, Hkv, d]; scales float32 [Hkv]."""
+    assert k_cache.dtype == np.uint8 and k_cache.flags.c_contiguous and k_cache.ndim == 3
+    assert v_cache.dtype == np.uint8 and v_cache.flags.c_contiguous and v_cache.shape == k_cache.shape
+    slots, Hkv, d = k_cache.shape
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    sm = _c(slot_mapping, np.int32)
+    ks = _c(k_scale, np.float32)
+    vs = _c(v_scale, np.float32)
+    T = sm.shape[0]
+    assert k.size == T * Hkv * d and v.size == T * Hkv * d and ks.size == Hkv and vs.size == Hkv
+    _check(_load(lib).oracle_store_kv_fp8(_ptr(k), _ptr(v), _ptr(sm), T, _ptr(k_cache), _ptr(v_cache),
+                                          slots, Hkv, d, _ptr(ks), _ptr(vs)), "oracle_store_kv_fp8")
+
+
 def page_table_from_token_table(token_table, table_idx, max_seqlen_k: int, page_size: int,
                                 out_cols: int | None = None, *, lib=None) -> np.ndarray:
     tt = _c(token_table, np.int32)
@@ -154,17 +197,20 @@ def seqlens(cached_len, extend_len, *, lib=None):
 
 def attention(q, k_cache, v_cache, page_table, cu_seqlens_q, cu_seqlens_k, *,
               num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
-              causal: bool, scale: float, rows=None, lib=None):
+              causal: bool, scale: float, rows=None, k_scale=None, v_scale=None, lib=None):
     """fp64 attention over paged K/V.
 
     q: uint16 [Tq, Hq, d]; caches: uint16 [num_pages*page_size, Hkv, d] (any
-    shape with that element order); page_table int32 [B, stride].
+    shape with that element order), or uint8 E4M3 codes with float32
+    ``k_scale``/``v_scale`` [Hkv]; page_table int32 [B, stride].
     Returns (out, lse): float64 [Tq, Hq, d] and [Tq, Hq], or, when ``rows`` (an
     int64 [n, 2] array of (token, head)) is given, [n, d] and [n].
     """
     q = _c(q, np.uint16)
-    kc = k_cache if (k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous) else _c(k_cache, np.uint16)
-    vc = v_cache if (v_cache.dtype == np.uint16 and v_cache.flags.c_contiguous) else _c(v_cache, np.uint16)
+    fp8 = k_scale is not None
+    kt = np.uint8 if fp8 else np.uint16
+    kc = k_cache if (k_cache.dtype == kt and k_cache.flags.c_contiguous) else _c(k_cache, kt)
+    vc = v_cache if (v_cache.dtype == kt and v_cache.flags.c_contiguous) else _c(v_cache, kt)
     pt = _c(page_table, np.int32)
     if pt.ndim == 1:
         pt = pt.reshape(-1, 1)
@@ -183,6 +229,15 @@ def attention(q, k_cache, v_cache, page_table, cu_seqlens_q, cu_seqlens_k, *,
         out = np.zeros((rws.shape[0], d), dtype=np.float64)
         lse = np.zeros((rws.shape[0],), dtype=np.float64)
         rp, nr = _ptr(rws), rws.shape[0]
+    if fp8:
+        ks = _c(k_scale, np.float32)
+        vs = _c(v_scale, np.float32)
+        assert ks.size == Hkv and vs.size == Hkv
+        _check(_load(lib).oracle_attention_fp8(
+            _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(pt), pt.shape[1], _ptr(cq), _ptr(ck),
+            B, Hq, Hkv, d, P, num_pages, int(bool(causal)), float(scale), rp, nr,
+            _ptr(out), _ptr(lse)), "oracle_attention_fp8")
+        return out, lse
     _check(_load(lib).oracle_attention(
         _ptr(q), _ptr(kc), _ptr(vc), _ptr(pt), pt.shape[1], _ptr(cq), _ptr(ck), B,
         Hq, Hkv, d, P, num_pages, int(bool(causal)), float(scale), rp, nr,
@@ -191,7 +246,8 @@ def attention(q, k_cache, v_cache, page_table, cu_seqlens_q, cu_seqlens_k, *,
 
 
 def decode(q, k_cache, v_cache, page_table, cache_seqlens, *, num_q_heads: int,
-           num_kv_heads: int, head_dim: int, page_size: int, scale: float, rows=None, lib=None):
+           num_kv_heads: int, head_dim: int, page_size: int, scale: float, rows=None,
+           k_scale=None, v_scale=None, lib=None):
     """Decode attention: one query token per sequence attending to all
     cache_seqlens[b] keys (the new token already stored).  q: [B, Hq, d]."""
     cs = np.asarray(cache_seqlens, dtype=np.int64)
@@ -201,7 +257,8 @@ def decode(q, k_cache, v_cache, page_table, cache_seqlens, *, num_q_heads: int,
     cu_k[1:] = np.cumsum(cs)
     return attention(q, k_cache, v_cache, page_table, cu_q, cu_k.astype(np.int32),
                      num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
-                     page_size=page_size, causal=False, scale=scale, rows=rows, lib=lib)
+                     page_size=page_size, causal=False, scale=scale, rows=rows, k_scale=k_scale,
+                     v_scale=v_scale, lib=lib)
 
 
 from . import online  # noqa: E402,F401  (re-export)

@@ -37,6 +37,20 @@
  *    max_seqlen_k and, for P > 1, floor-divided by P to turn the slot of each
  *    page's first token into that page's id.
  *
+ *  - FP8 KV cache (oracle_e4m3_value, oracle_e4m3_encode,
+ *    oracle_store_kv_fp8, oracle_attention_fp8).  The first page lists FP8
+ *    and quantized KV as a dispatch axis and a KV layout (section 19) and
+ *    "quantized" KV as an edge case (section 24); the second page ("Inference
+ *    systems and kernel optimisation", section 1) names FP8 quantization as
+ *    part of FlashAttention-3.  Neither fixes a format, so the reading here is
+ *    the plainest one: the E4M3 format with no infinities (1 sign bit, 4
+ *    exponent bits with bias 7, 3 mantissa bits; exponent field 0 encodes
+ *    subnormals m/8 * 2^-6; S.1111.111 is NaN, so the largest finite value is
+ *    448), one fp32 scale per KV head for K and one for V, a stored element
+ *    being code = E4M3(x / scale) with x / scale an IEEE single division,
+ *    rounded to the nearest E4M3 value, ties to the even code, magnitudes of
+ *    448 and above saturating to 448; attention then reads code * scale.
+ *
  * All arithmetic on floating point is IEEE double.  bf16 inputs are widened
  * exactly (a bf16 value is the top 16 bits of an IEEE single).
  */
@@ -60,6 +74,80 @@ static double widen_bf16(uint16_t bits)
     memcpy(&f, &u, sizeof f);
     return (double)f;
 }
+
+/* ---------------------------------------------------------- E4M3 codec */
+
+/* Value of an E4M3 code, from the format's definition. */
+double oracle_e4m3_value(uint8_t code)
+{
+    int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) mag = ldexp((double)m / 8.0, -6);          /* subnormal */
+    else mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* Nearest E4M3 code to x (ties to the even code), saturating to +-448.
+ * The non-negative finite codes 0x00..0x7E have increasing values, so the
+ * code just below |x| is found by bisection and compared with its upper
+ * neighbour.  NaN gives 0x7F. */
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    int lo = 0, hi = 0x7E;                 /* value(lo) <= a < value(hi) */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (oracle_e4m3_value((uint8_t)mid) <= a) lo = mid; else hi = mid;
+    }
+    double dlo = a - oracle_e4m3_value((uint8_t)lo);
+    double dhi = oracle_e4m3_value((uint8_t)hi) - a;
+    int c;
+    if (dlo < dhi) c = lo;
+    else if (dhi < dlo) c = hi;
+    else c = (lo & 1) ? hi : lo;           /* tie: the even code */
+    return sign | (uint8_t)c;
+}
+
+static float widen_bf16_f32(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* FP8 KV store.  k, v: [T, Hkv, d] bf16 bits; caches: [num_slots, Hkv, d]
+ * E4M3 codes; k_scale, v_scale: [Hkv].  Element c of head h of token t goes
+ * to row slot_mapping[t] as E4M3(x / scale[h]), the division in IEEE single. */
+int oracle_store_kv_fp8(const uint16_t *k, const uint16_t *v, const int32_t *slot_mapping,
+                        int64_t num_tokens, uint8_t *k_cache, uint8_t *v_cache,
+                        int64_t num_slots, int32_t Hkv, int32_t d,
+                        const float *k_scale, const float *v_scale)
+{
+    if (num_tokens < 0 || num_slots < 0 || Hkv <= 0 || d <= 0) return ORACLE_EINVAL;
+    int64_t row = (int64_t)Hkv * d;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) return ORACLE_ERANGE;
+        for (int32_t h = 0; h < Hkv; ++h) {
+            for (int32_t c = 0; c < d; ++c) {
+                int64_t src = t * row + (int64_t)h * d + c, dst = slot * row + (int64_t)h * d + c;
+                volatile float qk = widen_bf16_f32(k[src]) / k_scale[h];
+                volatile float qv = widen_bf16_f32(v[src]) / v_scale[h];
+                k_cache[dst] = oracle_e4m3_encode(qk);
+                v_cache[dst] = oracle_e4m3_encode(qv);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------- threads */
 
 int oracle_num_threads(void)
 {
@@ -152,7 +240,21 @@ int oracle_seqlens(const int32_t *cached_len, const int32_t *extend_len, int32_t
 
 /* One attention row: query token t (global index into q), query head h.
  * Writes d doubles to o and one to *lse.  scratch holds >= Lk doubles. */
-static int attention_row(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+/* The K/V pools as attention reads them: bf16 bits, or E4M3 codes with a
+ * scale per KV head (value = code value * scale). */
+typedef struct {
+    const void *k, *v;
+    int fp8;
+    const float *k_scale, *v_scale;
+} kv_pools;
+
+static double kv_value(const void *cache, int fp8, const float *scale, int64_t idx, int32_t kvh)
+{
+    if (!fp8) return widen_bf16(((const uint16_t *)cache)[idx]);
+    return oracle_e4m3_value(((const uint8_t *)cache)[idx]) * (double)scale[kvh];
+}
+
+static int attention_row(const uint16_t *q, const kv_pools *kv,
                          const int32_t *page_table, int64_t pt_stride,
                          const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
                          int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
@@ -187,9 +289,10 @@ static int attention_row(const uint16_t *q, const uint16_t *k_cache, const uint1
         int64_t page = page_table[b * pt_stride + j / P];
         if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
         int64_t row = page * P + j % P;
-        const uint16_t *krow = k_cache + (row * Hkv + kvh) * (int64_t)d;
+        int64_t kbase = (row * Hkv + kvh) * (int64_t)d;
         double acc = 0.0;
-        for (int c = 0; c < d; ++c) acc += widen_bf16(qrow[c]) * widen_bf16(krow[c]);
+        for (int c = 0; c < d; ++c)
+            acc += widen_bf16(qrow[c]) * kv_value(kv->k, kv->fp8, kv->k_scale, kbase + c, kvh);
         s_row[j] = scale * acc;
     }
     /* pass 1: row maximum */
@@ -202,8 +305,8 @@ static int attention_row(const uint16_t *q, const uint16_t *k_cache, const uint1
         l += p;
         int64_t page = page_table[b * pt_stride + j / P];
         int64_t row = page * P + j % P;
-        const uint16_t *vrow = v_cache + (row * Hkv + kvh) * (int64_t)d;
-        for (int c = 0; c < d; ++c) o[c] += p * widen_bf16(vrow[c]);
+        int64_t vbase = (row * Hkv + kvh) * (int64_t)d;
+        for (int c = 0; c < d; ++c) o[c] += p * kv_value(kv->v, kv->fp8, kv->v_scale, vbase + c, kvh);
     }
     for (int c = 0; c < d; ++c) o[c] /= l;
     *lse = m + log(l);
@@ -215,12 +318,12 @@ static int attention_row(const uint16_t *q, const uint16_t *k_cache, const uint1
  * page_table: [num_seqs, pt_stride] int32; cu_q, cu_k: [num_seqs+1] int32.
  * rows == NULL: every (token, head) row; out [Tq, Hq, d], lse [Tq, Hq].
  * rows != NULL: nrows pairs (token, head) as int64; out [nrows, d], lse [nrows]. */
-int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                     const int32_t *page_table, int64_t pt_stride,
-                     const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
-                     int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
-                     int causal, double scale, const int64_t *rows, int64_t nrows,
-                     double *out, double *lse)
+static int attention_all(const uint16_t *q, const kv_pools *kv,
+                         const int32_t *page_table, int64_t pt_stride,
+                         const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
+                         int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
+                         int causal, double scale, const int64_t *rows, int64_t nrows,
+                         double *out, double *lse)
 {
     if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || P <= 0 || Hq % Hkv) return ORACLE_EINVAL;
     int64_t Tq = num_seqs > 0 ? cu_q[num_seqs] : 0;
@@ -250,7 +353,7 @@ int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t 
                     status = ORACLE_EINVAL;
                     continue;
                 }
-                int st = attention_row(q, k_cache, v_cache, page_table, pt_stride, cu_q, cu_k,
+                int st = attention_row(q, kv, page_table, pt_stride, cu_q, cu_k,
                                        num_seqs, Hq, Hkv, d, P, num_pages, causal, scale, t, h,
                                        out + r * (int64_t)d, lse + r, s_row);
                 if (st != ORACLE_OK) {
@@ -262,4 +365,31 @@ int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t 
         }
     }
     return status;
+}
+
+int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                     const int32_t *page_table, int64_t pt_stride,
+                     const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
+                     int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
+                     int causal, double scale, const int64_t *rows, int64_t nrows,
+                     double *out, double *lse)
+{
+    kv_pools kv = {k_cache, v_cache, 0, NULL, NULL};
+    return attention_all(q, &kv, page_table, pt_stride, cu_q, cu_k, num_seqs, Hq, Hkv, d, P,
+                         num_pages, causal, scale, rows, nrows, out, lse);
+}
+
+/* The same over E4M3 pools (codes [num_pages*P, Hkv, d]) with per-KV-head
+ * scales k_scale[Hkv], v_scale[Hkv]. */
+int oracle_attention_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                         const float *k_scale, const float *v_scale,
+                         const int32_t *page_table, int64_t pt_stride,
+                         const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
+                         int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
+                         int causal, double scale, const int64_t *rows, int64_t nrows,
+                         double *out, double *lse)
+{
+    kv_pools kv = {k_cache, v_cache, 1, k_scale, v_scale};
+    return attention_all(q, &kv, page_table, pt_stride, cu_q, cu_k, num_seqs, Hq, Hkv, d, P,
+                         num_pages, causal, scale, rows, nrows, out, lse);
 }

@@ -18,6 +18,14 @@ source) and raises AssertionError when the oracle disagrees with:
   nothing, the online block merge and the split merge equal the two-pass
   softmax.
 
+The FP8 (E4M3) KV path is pinned by closed-form code values from the
+format's definition, by a second rounding procedure written the other way
+(binade quantum and numpy's round-half-even instead of the oracle's
+bisection over the code table), by an elementwise quantisation reference for
+the store, and by the identity "attention over FP8 pools = attention over
+bf16 pools holding the same values" (every E4M3 value times a power-of-two
+scale is a bf16 value, so both paths see identical numbers).
+
 The hand-worked golden cases live in tests/golden/.
 """
 from __future__ import annotations
@@ -433,7 +441,103 @@ def check_metadata(lib=None):
     assert np.array_equal(pt1, p.token_table[:, :mk])
 
 
-ALL_CHECKS = [check_store, check_metadata, check_golden, check_brute_force, check_equal_scores,
+def _e4m3_reference_round(x: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 value of float32 x, computed by binades: the quantum of
+    the binade [2^e, 2^(e+1)) is 2^(e-3) (3 mantissa bits), subnormals share
+    the quantum 2^-9 of the lowest normal binade (e = -6), numpy rounds half
+    to even, and magnitudes of 448 and more saturate to 448."""
+    a = np.abs(x.astype(np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)
+    quantum = np.exp2(e - 3.0)
+    val = np.round(a / quantum) * quantum
+    val = np.where(a >= 448.0, 448.0, np.minimum(val, 448.0))
+    return np.copysign(val, x.astype(np.float64))
+
+
+def check_e4m3_codec(lib=None):
+    """E4M3 decode against closed forms and encode against an independent
+    rounding procedure."""
+    v = oracle.e4m3_value(np.arange(256), lib=lib)
+    closed = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x30: 0.5,
+              0x38: 1.0, 0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x78: 256.0, 0x7E: 448.0,
+              0xB8: -1.0, 0xFE: -448.0}
+    for c, want in closed.items():
+        assert v[c] == want, f"E4M3 code {c:#x} decodes to {v[c]}, not {want}"
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    assert np.all(np.diff(v[:0x7F]) > 0), "positive codes must increase"
+    assert np.array_equal(v[0x80:0xFF], -v[:0x7F]), "sign bit must negate"
+    codes = np.arange(0x7F, dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(v[:0x7F].astype(np.float32), lib=lib), codes), \
+        "every finite value must encode to its own code"
+    rng = np.random.default_rng(11)
+    x = np.concatenate([
+        rng.standard_normal(4000) * 10.0 ** rng.uniform(-4, 3, 4000),
+        (v[1:0x7E] + v[2:0x7F]) / 2.0,              # midpoints between neighbours: ties
+        [0.0, 2.0 ** -10, 3 * 2.0 ** -11, 447.9, 448.0, 460.0, 464.0, 1e6, 2.0 ** -20]]).astype(np.float32)
+    x = np.concatenate([x, -x])
+    got = oracle.e4m3_value(oracle.e4m3_encode(x, lib=lib), lib=lib)
+    want = _e4m3_reference_round(x)
+    assert np.array_equal(np.abs(got), np.abs(want)), "E4M3 rounding differs from the binade rule"
+    nz = want != 0
+    assert np.array_equal(np.signbit(got[nz]), np.signbit(want[nz]))
+
+
+def check_store_fp8(lib=None):
+    """FP8 store: each element becomes E4M3(x / scale[head]) (the division in
+    float32), rows of negative slots are skipped, other rows untouched."""
+    rng = np.random.default_rng(5)
+    slots, Hkv, d = 30, 3, 8
+    kc = rng.integers(0, 256, size=(slots, Hkv, d), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(slots, Hkv, d), dtype=np.uint8)
+    sm = np.array([4, -1, 29, 0, 11], np.int32)
+    kf = (rng.standard_normal((5, Hkv, d)) * 3).astype(np.float32)
+    vf = (rng.standard_normal((5, Hkv, d)) * 3).astype(np.float32)
+    k = W.f32_to_bf16_bits(kf)
+    v = W.f32_to_bf16_bits(vf)
+    ks = np.array([0.02, 0.5, 3.0], np.float32)
+    vs = np.array([0.25, 0.0078125, 1.5], np.float32)
+    ke, ve = kc.copy(), vc.copy()
+    for t, s_ in enumerate(sm):
+        if s_ < 0:
+            continue
+        kq = (W.bf16_bits_to_f32(k[t]) / ks[:, None]).astype(np.float32)
+        vq = (W.bf16_bits_to_f32(v[t]) / vs[:, None]).astype(np.float32)
+        ke[s_] = oracle.e4m3_encode(kq, lib=lib)
+        ve[s_] = oracle.e4m3_encode(vq, lib=lib)
+    oracle.store_kv_fp8(k, v, sm, kc, vc, ks, vs, lib=lib)
+    assert np.array_equal(kc, ke) and np.array_equal(vc, ve), "FP8 store differs from E4M3(x / scale)"
+    # the codec agrees with the binade rule on these quotients as well
+    q = (W.bf16_bits_to_f32(k[0]) / ks[:, None]).astype(np.float32)
+    assert np.array_equal(np.abs(oracle.e4m3_value(kc[4], lib=lib)), np.abs(_e4m3_reference_round(q)))
+
+
+def check_attention_fp8_exact_values(lib=None):
+    """Attention over E4M3 pools with per-head power-of-two scales equals,
+    bit for bit, attention over bf16 pools holding code value * scale."""
+    p = W.small_problem(31, [5, 0, 40], [3, 9, 1], num_q_heads=8, num_kv_heads=4, head_dim=16,
+                        page_size=4)
+    rng = np.random.default_rng(9)
+    shape = p.k_cache.shape
+    kc8 = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    vc8 = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    for c8 in (kc8, vc8):                       # no NaN codes
+        c8[(c8 & 0x7F) == 0x7F] = 0x3A
+    ks = np.array([0.125, 1.0, 4.0, 0.5], np.float32)
+    vs = np.array([2.0, 0.25, 1.0, 8.0], np.float32)
+    kval = oracle.e4m3_value(kc8, lib=lib) * ks[None, None, :, None]
+    vval = oracle.e4m3_value(vc8, lib=lib) * vs[None, None, :, None]
+    kb, vb = W.f32_to_bf16_bits(kval.astype(np.float32)), W.f32_to_bf16_bits(vval.astype(np.float32))
+    assert np.array_equal(W.bf16_bits_to_f32(kb).astype(np.float64), kval), "values must be bf16-exact"
+    cu_q, cu_k, _, pt = _meta(p, lib)
+    kw = dict(num_q_heads=p.num_q_heads, num_kv_heads=p.num_kv_heads, head_dim=p.head_dim,
+              page_size=p.page_size, causal=True, scale=p.scale, lib=lib)
+    o8, l8 = oracle.attention(p.q, kc8, vc8, pt, cu_q, cu_k, k_scale=ks, v_scale=vs, **kw)
+    ob, lb = oracle.attention(p.q, kb, vb, pt, cu_q, cu_k, **kw)
+    assert np.array_equal(o8, ob) and np.array_equal(l8, lb), "FP8 attention differs from bf16 on equal values"
+
+
+ALL_CHECKS = [check_e4m3_codec, check_store_fp8, check_attention_fp8_exact_values, check_store, check_metadata, check_golden, check_brute_force, check_equal_scores,
               check_single_key, check_dominant_key, check_empty, check_sdpa_library,
               check_decode_is_last_prefill_row, check_extend_is_prefill_tail,
               check_gqa_equals_repeated_mha, check_page_size_equivalence,

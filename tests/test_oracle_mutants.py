@@ -21,12 +21,19 @@ MUTANTS = [
     ("page_index_transposed", "page_table[b * pt_stride + j / P]", "page_table[b * pt_stride + j % P]", 1),
     ("no_normalisation", "for (int c = 0; c < d; ++c) o[c] /= l;", "", 1),
     ("lse_missing_max", "*lse = m + log(l);", "*lse = log(l);", 1),
-    ("values_from_k_cache", "const uint16_t *vrow = v_cache +", "const uint16_t *vrow = k_cache +", 1),
+    ("values_from_k_cache", "o[c] += p * kv_value(kv->v,", "o[c] += p * kv_value(kv->k,", 1),
     ("exp_sign_flipped", "double p = exp(s_row[j] - m);", "double p = exp(m - s_row[j]);", 1),
     ("last_key_dropped", "for (int64_t j = 0; j < n_vis; ++j) {\n        double p", "for (int64_t j = 0; j + 1 < n_vis; ++j) {\n        double p", 1),
     ("cu_k_prefix_wrong", "cu_k[b + 1] = (int32_t)sk;", "cu_k[b + 1] = (int32_t)sq;", 1),
     ("page_table_no_divide", "int64_t q = slot / page_size;", "int64_t q = slot;", 1),
     ("store_swaps_k_v", "memcpy(k_cache + slot * row_elems, k + t * row_elems", "memcpy(k_cache + slot * row_elems, v + t * row_elems", 1),
+    ("e4m3_bias_8", "else mag = ldexp(1.0 + (double)m / 8.0, e - 7);", "else mag = ldexp(1.0 + (double)m / 8.0, e - 8);", 1),
+    ("e4m3_subnormal_scale", "if (e == 0) mag = ldexp((double)m / 8.0, -6);", "if (e == 0) mag = ldexp((double)m / 8.0, -7);", 1),
+    ("e4m3_ties_up", "else c = (lo & 1) ? hi : lo;", "else c = hi;", 1),
+    ("e4m3_truncates", "if (dlo < dhi) c = lo;", "if (1) c = lo;", 1),
+    ("fp8_scale_head_0", "* (double)scale[kvh];", "* (double)scale[0];", 1),
+    ("fp8_store_multiplies", "widen_bf16_f32(k[src]) / k_scale[h]", "widen_bf16_f32(k[src]) * k_scale[h]", 1),
+    ("fp8_k_read_with_v_scale", "kv_value(kv->k, kv->fp8, kv->k_scale,", "kv_value(kv->k, kv->fp8, kv->v_scale,", 1),
 ]
 
 

@@ -52,6 +52,11 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return ((u + rounding) >> 16).astype(np.uint16)
 
 
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact float32 values of bf16 bit patterns."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
 def normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
     """bf16 bits of N(0, 1) float32 draws, in chunks to bound memory."""
     n = int(np.prod(shape))
