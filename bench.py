@@ -448,6 +448,9 @@ MICRO_CASES = {
     # a smaller mixed-batch decode: 64 sequences, contexts log-uniform
     # [512, 32768], ~2 GB pool (inputs still far larger than L2)
     "decode_64seq_logu": (None, None, "decode"),
+    # the same decode workloads over FP8 (E4M3) pools with per-head scales
+    "llama32_1b_decode_fp8": (2, None, "decode"),
+    "decode_64seq_logu_fp8": (None, None, "decode"),
 }
 
 
@@ -457,7 +460,7 @@ def micro_problem(name):
         return W.config(cfg, variant), kernel
     rng = np.random.default_rng(W.SEED_BASE + 70)
     Lk = np.exp(rng.uniform(math.log(512), math.log(32768), size=64)).astype(np.int32)
-    p = W.build(name, cached_len=Lk - 1, extend_len=np.ones(64, np.int32), num_q_heads=32,
+    p = W.build(name.replace("_fp8", ""), cached_len=Lk - 1, extend_len=np.ones(64, np.int32), num_q_heads=32,
                 num_kv_heads=8, head_dim=128, page_size=16, seed=W.SEED_BASE + 71, pool_factor=1.1)
     return p, kernel
 
@@ -470,11 +473,20 @@ def run_micro(args):
     from paged_kv_flashattention_gb300 import metadata
     dev = torch.device("cuda", 0)
     p, kernel = micro_problem(args.micro)
+    fp8 = args.micro.endswith("_fp8")
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-    kc, vc, q = to(p.k_cache), to(p.v_cache), to(p.q)
+    q = to(p.q)
     kn, vn = to(p.k_new), to(p.v_new)
     sm = torch.from_numpy(p.slot_mapping).to(dev)
-    pa.store_kv(kn, vn, sm, kc, vc)
+    scales = {}
+    if fp8:
+        kc8, vc8, ks, vs = W.fp8_pools(p, W.SEED_BASE + 72)
+        kc, vc = torch.from_numpy(kc8).to(dev), torch.from_numpy(vc8).to(dev)
+        scales = dict(k_scale=torch.from_numpy(ks).to(dev), v_scale=torch.from_numpy(vs).to(dev))
+        pa.store_kv_fp8(kn, vn, sm, kc, vc, **scales)
+    else:
+        kc, vc = to(p.k_cache), to(p.v_cache)
+        pa.store_kv(kn, vn, sm, kc, vc)
     m = metadata.prepare(p.cached_len, p.extend_len, torch.from_numpy(p.token_table).to(dev),
                          torch.from_numpy(p.table_idx).to(dev), p.page_size)
     Hkv, D, Hq = p.num_kv_heads, p.head_dim, p.num_q_heads
@@ -483,8 +495,8 @@ def run_micro(args):
         ws = torch.empty(max(16, pa.decode_workspace_size(q.shape, kc, m.max_seqlen_k)),
                          dtype=torch.uint8, device=dev)
         fn = lambda: pa.decode(q, kc, vc, m.page_table, m.cache_seqlens, m.max_seqlen_k,
-                               scale=p.scale, out=out, workspace=ws)
-        work = int(p.device_len.astype(np.int64).sum()) * Hkv * D * 4 + 2 * q.numel() * 2
+                               scale=p.scale, out=out, workspace=ws, **scales)
+        work = int(p.device_len.astype(np.int64).sum()) * Hkv * D * 2 * kc.element_size() + 2 * q.numel() * 2
         unit = "GB/s"
     elif kernel == "prefill":
         fn = lambda: pa.prefill(q, kc, vc, m.page_table, m.cu_seqlens_q, m.cu_seqlens_k,

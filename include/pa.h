@@ -3,6 +3,7 @@
  *
  * Exact attention over a paged KV cache, as a serving engine runs it:
  *   pa_store_kv          write the new tokens' K/V rows into the paged pool
+ *   pa_store_kv_fp8      the same into an FP8 (E4M3) pool with per-head scales
  *   pa_build_seqlens     per-request boundaries from the three lengths (host)
  *   pa_build_page_table  per-request page table from the token-granular table
  *   pa_prefill           varlen causal prefill / extend attention
@@ -16,7 +17,7 @@
  *      s.10 scaled dot-product attention, s.11 tiled exact attention, s.12
  *      online softmax, s.13 prefill vs decode, s.14 paged-KV address
  *      translation, s.15 GQA head mapping, s.16 split-KV with stable merge,
- *      s.24 edge-case matrix.
+ *      s.19 dispatch axes (FP8 / quantized KV), s.24 edge-case matrix.
  *  [M] "code-series sgl-project mini-sglang 07": "from ledger to tensors"
  *      (extend_len / device_len / cached_len, cu_seqlens_q, cu_seqlens_k,
  *      cache_seqlens, the page-size-1 global table sliced with step P and
@@ -101,6 +102,25 @@ pa_status pa_store_kv(const void *k, const void *v, const int32_t *slot_mapping,
                       int32_t num_kv_heads, int32_t head_dim, void *stream);
 
 /*
+ * pa_store_kv_fp8 - KV-cache store into an FP8 pool ([T] s.19 and s.24 name
+ * FP8 / quantized KV without fixing a format; this library's reading):
+ *   for t with s = slot_mapping[t] >= 0, head h, element c:
+ *     k_cache[s, h, c] = E4M3(k[t, h, c] / k_scale[h])   (same for v)
+ * E4M3: 1 sign, 4 exponent (bias 7) and 3 mantissa bits, no infinities,
+ * largest finite value 448; the quotient is an IEEE single division, rounded
+ * to the nearest E4M3 value (ties to even), magnitudes >= 448 saturate to
+ * +-448.  Attention reads the element back as value(code) * scale[h].
+ * k, v:             device bf16 [num_tokens, Hkv, head_dim]
+ * k_cache, v_cache: device uint8 codes [num_slots, Hkv, head_dim]
+ * k_scale, v_scale: device fp32 [Hkv], positive and finite
+ * slot_mapping: as for pa_store_kv.  head_dim must be a multiple of 16.
+ */
+pa_status pa_store_kv_fp8(const void *k, const void *v, const int32_t *slot_mapping,
+                          int64_t num_tokens, void *k_cache, void *v_cache, int64_t num_slots,
+                          int32_t num_kv_heads, int32_t head_dim, const float *k_scale,
+                          const float *v_scale, void *stream);
+
+/*
  * pa_build_seqlens - host-side metadata ([M], "from ledger to tensors").
  * All pointers are HOST memory.  From cached_len[b] and extend_len[b]:
  *   cu_seqlens_q  [num_seqs+1] = exclusive prefix sum of extend_len
@@ -171,6 +191,12 @@ typedef struct {
 
 pa_status pa_prefill(const pa_prefill_params *p, void *stream);
 
+/* Element type of the K/V pools read by pa_decode.  FP8 pools hold E4M3
+ * codes written by pa_store_kv_fp8 with per-KV-head scales.  On FP8 pools the
+ * contractions run in f16 with fp32 accumulation: q * k_scale is rounded to
+ * f16 (|q * k_scale| must stay below 65504), P is rounded to f16. */
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+
 /*
  * pa_decode - decode attention ([T] s.13 and s.16): one query token per
  * sequence (q row b) attends to all cache_seqlens[b] keys of its page-table
@@ -205,6 +231,9 @@ typedef struct {
     size_t workspace_bytes;
     int32_t kv_chunk;            /* minimum keys per split, multiple of 16;
                                     0 = automatic (max_seqlen_k / 32, >= 64) */
+    int32_t kv_dtype;            /* pa_kv_dtype of k_cache / v_cache (0 = bf16) */
+    const float *k_scale;        /* PA_KV_FP8_E4M3: device fp32 [Hkv]; else unused */
+    const float *v_scale;        /* (element = value(code) * scale[kv head]) */
 } pa_decode_params;
 
 /* Bytes of workspace pa_decode needs for these parameters (always > 0: a

@@ -1,18 +1,19 @@
 """Paged-KV exact attention for GB300 (sm_103a).
 
 A small C-ABI library (``libpa.so``, declared in ``include/pa.h``) with
-hand-written CUDA kernels for the KV-cache store, varlen causal prefill /
+hand-written CUDA kernels for the KV-cache store (bf16, or FP8 E4M3 with
+per-head scales), varlen causal prefill /
 extend attention over a page table, split-KV decode and the log-sum-exp
 combine; this package is its thin torch binding.  PyTorch provides device
 memory and streams only.
 """
-from .api import (PagedAttentionError, abi_version, build_page_table, build_seqlens, decode,
-                  decode_noalloc, decode_kv_chunk, decode_workspace_size, device_error, lse_combine, prefill,
-                  store_kv)
+from .api import (PA_KV_BF16, PA_KV_FP8_E4M3, PagedAttentionError, abi_version, build_page_table,
+                  build_seqlens, decode, decode_noalloc, decode_kv_chunk, decode_workspace_size,
+                  device_error, lse_combine, prefill, store_kv, store_kv_fp8)
 
 __all__ = [
     "PagedAttentionError", "abi_version", "build_page_table", "build_seqlens", "decode",
     "decode_noalloc",
     "decode_kv_chunk", "decode_workspace_size", "device_error", "lse_combine", "prefill",
-    "store_kv",
+    "store_kv", "store_kv_fp8", "PA_KV_BF16", "PA_KV_FP8_E4M3",
 ]

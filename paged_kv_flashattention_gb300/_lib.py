@@ -43,7 +43,7 @@ class DecodeParams(ctypes.Structure):
         ("num_q_heads", c_i32), ("num_kv_heads", c_i32), ("head_dim", c_i32),
         ("page_size", c_i32), ("num_pages", c_i64), ("scale", c_f32),
         ("out", c_p), ("lse", c_p), ("workspace", c_p), ("workspace_bytes", c_size),
-        ("kv_chunk", c_i32),
+        ("kv_chunk", c_i32), ("kv_dtype", c_i32), ("k_scale", c_p), ("v_scale", c_p),
     ]
 
 
@@ -54,6 +54,7 @@ SIGNATURES = {
     "pa_last_error": (ctypes.c_char_p, []),
     "pa_device_error": (ctypes.c_int, [ctypes.POINTER(c_i32), c_p]),
     "pa_store_kv": (ctypes.c_int, [c_p, c_p, c_p, c_i64, c_p, c_p, c_i64, c_i32, c_i32, c_p]),
+    "pa_store_kv_fp8": (ctypes.c_int, [c_p, c_p, c_p, c_i64, c_p, c_p, c_i64, c_i32, c_i32, c_p, c_p, c_p]),
     "pa_build_seqlens": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p]),
     "pa_build_page_table": (ctypes.c_int, [c_p, c_i64, c_p, c_i32, c_i32, c_i32, c_p, c_i32, c_p]),
     "pa_prefill": (ctypes.c_int, [ctypes.POINTER(PrefillParams), c_p]),

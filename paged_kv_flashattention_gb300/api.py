@@ -51,6 +51,31 @@ def _need(t: torch.Tensor, name: str, dtype, device=None, contiguous=True):
         raise ValueError(f"{name} must be contiguous")
 
 
+PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+_FP8_DTYPES = (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+
+
+def _kv_dtype(k_cache: torch.Tensor, v_cache: torch.Tensor) -> int:
+    """PA_KV_BF16 for bf16 pools, PA_KV_FP8_E4M3 for E4M3 codes (uint8 or
+    torch.float8_e4m3fn)."""
+    if k_cache.dtype != v_cache.dtype:
+        raise TypeError("k_cache and v_cache dtypes differ")
+    if k_cache.dtype == torch.bfloat16:
+        return PA_KV_BF16
+    if k_cache.dtype in _FP8_DTYPES:
+        return PA_KV_FP8_E4M3
+    raise TypeError(f"pools must be bf16 or E4M3 (uint8 / float8_e4m3fn), got {k_cache.dtype}")
+
+
+def _need_scales(k_scale, v_scale, Hkv: int, dev):
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t is None:
+            raise ValueError(f"{n} is required for FP8 pools")
+        _need(t, n, torch.float32, dev)
+        if t.numel() != Hkv:
+            raise ValueError(f"{n} must hold one scale per KV head ({Hkv})")
+
+
 def abi_version() -> int:
     return int(_lib.load().pa_abi_version())
 
@@ -82,6 +107,34 @@ def store_kv(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
     lib = _lib.load()
     _check(lib.pa_store_kv(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
                            num_slots, Hkv, d, _stream(k_cache)), lib)
+
+
+def store_kv_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                 k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                 v_scale: torch.Tensor) -> None:
+    """Write token t's K/V rows into row slot_mapping[t] of E4M3 pools:
+    code = E4M3(x / scale[kv head]).  k, v: bf16 [T, Hkv, d]; caches: uint8
+    or float8_e4m3fn [num_pages, page_size, Hkv, d] or [num_slots, Hkv, d];
+    k_scale, v_scale: fp32 [Hkv]."""
+    dev = k_cache.device
+    for t, n in ((k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, dev)
+    if _kv_dtype(k_cache, v_cache) != PA_KV_FP8_E4M3:
+        raise TypeError("store_kv_fp8 needs E4M3 pools")
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, k_cache.dtype, dev)
+    _need(slot_mapping, "slot_mapping", torch.int32, dev)
+    Hkv, d = k_cache.shape[-2], k_cache.shape[-1]
+    _need_scales(k_scale, v_scale, Hkv, dev)
+    T = slot_mapping.numel()
+    if k.numel() != T * Hkv * d or v.numel() != T * Hkv * d:
+        raise ValueError("k/v must hold num_tokens rows of Hkv*d")
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    num_slots = k_cache.numel() // (Hkv * d)
+    lib = _lib.load()
+    _check(lib.pa_store_kv_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
+                               num_slots, Hkv, d, _ptr(k_scale), _ptr(v_scale), _stream(k_cache)), lib)
 
 
 def build_seqlens(cached_len, extend_len):
@@ -178,11 +231,14 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
 
 
 def _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k, scale, page_size,
-                   out, lse, workspace, kv_chunk):
+                   out, lse, workspace, kv_chunk, k_scale=None, v_scale=None):
     num_pages, P, Hkv, d = _pool_geometry(k_cache, v_cache, page_size)
     B, Hq, dq = q.shape
     if dq != d:
         raise ValueError("head_dim of q and the pool differ")
+    kvd = _kv_dtype(k_cache, v_cache)
+    if kvd == PA_KV_FP8_E4M3:
+        _need_scales(k_scale, v_scale, Hkv, q.device)
     return _lib.DecodeParams(
         q=_ptr(q), k_cache=_ptr(k_cache), v_cache=_ptr(v_cache), page_table=_ptr(page_table),
         page_table_stride=page_table.stride(0) if page_table is not None else 0,
@@ -191,7 +247,9 @@ def _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k,
         scale=float(1.0 / math.sqrt(d) if scale is None else scale), out=_ptr(out), lse=_ptr(lse),
         workspace=_ptr(workspace), workspace_bytes=(workspace.numel() * workspace.element_size()
                                                     if workspace is not None else 0),
-        kv_chunk=int(kv_chunk))
+        kv_chunk=int(kv_chunk), kv_dtype=kvd,
+        k_scale=_ptr(k_scale) if kvd == PA_KV_FP8_E4M3 else None,
+        v_scale=_ptr(v_scale) if kvd == PA_KV_FP8_E4M3 else None)
 
 
 def decode_workspace_size(q_shape, k_cache: torch.Tensor, max_seqlen_k: int, *,
@@ -219,12 +277,17 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_t
            cache_seqlens: torch.Tensor, max_seqlen_k: int, *, scale: float | None = None,
            page_size: int | None = None, out: torch.Tensor | None = None,
            lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-           kv_chunk: int = 0) -> torch.Tensor:
+           kv_chunk: int = 0, k_scale: torch.Tensor | None = None,
+           v_scale: torch.Tensor | None = None) -> torch.Tensor:
     """Split-KV decode: q bf16 [B, Hq, d] -> out bf16 [B, Hq, d]; lse fp32 [B, Hq].
-    ``workspace`` (a uint8 CUDA tensor) is allocated here when not given."""
+    Pools are bf16, or E4M3 codes (uint8 / float8_e4m3fn) with fp32 per-KV-head
+    ``k_scale`` and ``v_scale``.  ``workspace`` (a uint8 CUDA tensor) is
+    allocated here when not given."""
     dev = q.device
-    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t, n, torch.bfloat16, dev)
+    _need(q, "q", torch.bfloat16, dev)
+    kvd = _kv_dtype(k_cache, v_cache)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, k_cache.dtype, dev)
     _need(cache_seqlens, "cache_seqlens", torch.int32, dev)
     _need(page_table, "page_table", torch.int32, dev, contiguous=False)
     if page_table.dim() != 2 or page_table.stride(1) != 1:
@@ -238,7 +301,7 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_t
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     p = _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k, scale, page_size,
-                       out, lse, workspace, kv_chunk)
+                       out, lse, workspace, kv_chunk, k_scale, v_scale)
     lib = _lib.load()
     _check(lib.pa_decode(ctypes.byref(p), _stream(q)), lib)
     return out
@@ -248,7 +311,8 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                    page_table: torch.Tensor, cache_seqlens: torch.Tensor, max_seqlen_k: int, *,
                    scale: float | None = None, page_size: int | None = None,
                    out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-                   kv_chunk: int = 0) -> torch.Tensor:
+                   kv_chunk: int = 0, k_scale: torch.Tensor | None = None,
+                   v_scale: torch.Tensor | None = None) -> torch.Tensor:
     """Split-KV decode through ``pa_decode_noalloc``: the split partials go to
     the library's fixed 32 MiB device scratch, so no workspace is allocated
     (for callers that may not allocate device memory).  Calls on one device
@@ -256,8 +320,10 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     PagedAttentionError.  ``out`` (and ``lse``) must be given by a caller that
     cannot allocate; they are created here only for convenience."""
     dev = q.device
-    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t, n, torch.bfloat16, dev)
+    _need(q, "q", torch.bfloat16, dev)
+    _kv_dtype(k_cache, v_cache)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, k_cache.dtype, dev)
     _need(cache_seqlens, "cache_seqlens", torch.int32, dev)
     _need(page_table, "page_table", torch.int32, dev, contiguous=False)
     if page_table.dim() != 2 or page_table.stride(1) != 1:
@@ -268,7 +334,7 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     if lse is not None:
         _need(lse, "lse", torch.float32, dev)
     p = _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k, scale, page_size,
-                       out, lse, None, kv_chunk)
+                       out, lse, None, kv_chunk, k_scale, v_scale)
     lib = _lib.load()
     _check(lib.pa_decode_noalloc(ctypes.byref(p), _stream(q)), lib)
     return out

@@ -29,6 +29,19 @@
 //     moves only when a stage maximum exceeds it by more than 2^8, which keeps
 //     every exponent <= 8 and skips most O rescales exactly.
 // The whole kernel is bound by HBM: every K/V byte is read once.
+//
+// FP8 pools (E4M3 codes with a scale per KV head; the first page lists FP8 /
+// quantized KV as a dispatch axis in section 19): the same kernel streams
+// rows of one byte per element, half the bytes.  The contractions run in f16
+// on the same MMA shape: K and V codes are read with the same ldmatrix
+// patterns (pairs of codes as b16), widened exactly to f16 with the
+// hardware's E4M3 conversion, and the K scale is folded into the query (q *
+// k_scale as f16), the V scale into the final O.  Because an ldmatrix
+// register then holds 4 consecutive codes of a row, the k index of the score
+// MMA runs over d in the order 4c, 4c+1 | 4c+2, 4c+3 (the query fragment is
+// loaded in the same order), and the transposed V fragment holds two
+// adjacent d rows, so O^T row g of a d-tile is d = 2g and row g + 8 is
+// d = 2g + 1.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -67,13 +80,15 @@ struct DecodeArgs {
     float *lse;
     float *o_part;
     float *lse_part;
+    const float *k_scale;         // FP8 pools: per-KV-head scales
+    const float *v_scale;
     int32_t *ws_header;           // [0] = T
     int32_t *ws_prefix;           // [B+1] exclusive prefix of the sequence lengths
 };
 
-template <int D, int HPC>
+template <int D, int HPC, int EB>
 struct DecodeSmem {
-    static constexpr int kRowBytes = HPC * D * 2;            // one token, CTA's KV heads
+    static constexpr int kRowBytes = HPC * D * EB;           // one token, CTA's KV heads (EB bytes each)
     static constexpr int kRowStride = kRowBytes + 16;        // +16 B: ldmatrix rows hit distinct banks
     static constexpr int kStageBytes = 2 * kStageTok * kRowStride;
     static constexpr int kRingBytes = kStages * kStageBytes;
@@ -96,6 +111,27 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+
+// Warp-level f16 MMA, D(16x8, fp32) += A(16x16, row) * B(16x8, col).
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 codes (low byte first) to two f16 (exact: every E4M3 value is an
+// f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two_codes));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
+    return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
@@ -130,14 +166,15 @@ struct SegmentWalk {
     }
 };
 
-template <int D, int G, int HPC>
+template <int D, int G, int HPC, bool F8>
 __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs a) {
-    using S = DecodeSmem<D, HPC>;
+    constexpr int EB = F8 ? 1 : 2;                   // bytes per K/V element
+    using S = DecodeSmem<D, HPC, EB>;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kRingBytes);
     uint64_t *empty = full + kStages;
-    uint16_t *pbuf = reinterpret_cast<uint16_t *>(empty + kStages);   // [HPC][8 heads][16 tokens] bf16
+    uint16_t *pbuf = reinterpret_cast<uint16_t *>(empty + kStages);   // [HPC][8 heads][16 tokens] bf16 / f16
     int32_t *prefix = reinterpret_cast<int32_t *>(pbuf + HPC * 8 * kStageTok);  // [B+1]
 
     const int warp = threadIdx.x >> 5;
@@ -218,7 +255,7 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
                         page = 0;
                     }
                     const int64_t row = page * a.page_size + (j % a.page_size);
-                    const int64_t off = (row * a.num_kv_heads + (int64_t)hg * HPC) * D * 2;
+                    const int64_t off = (row * a.num_kv_heads + (int64_t)hg * HPC) * D * EB;
                     uint8_t *dst = ring + slot * S::kStageBytes + (lane >> 4) * (kStageTok * S::kRowStride) +
                                    tok * S::kRowStride;
                     const uint8_t *src = (lane < 16 ? a.k_cache : a.v_cache) + off;
@@ -256,7 +293,17 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
 
         // Q^T fragments of query head h0 + r8 (zero for the padding heads)
         uint32_t qb[KS][2];
-        if (r8 < G) {
+        if (F8 && r8 < G) {
+            // q * k_scale as f16, k index order 4c, 4c+1 | 4c+2, 4c+3 per 16
+            const float ksc = __ldg(a.k_scale + kvh);
+            const uint2 *qrow = reinterpret_cast<const uint2 *>(a.q + ((int64_t)b * a.num_q_heads + h0 + r8) * D);
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                const uint2 w = __ldg(qrow + kk * 4 + q4);           // d = 16 kk + 4 q4 .. + 3
+                qb[kk][0] = f16x2_bits(__uint_as_float(w.x << 16) * ksc, __uint_as_float(w.x & 0xffff0000u) * ksc);
+                qb[kk][1] = f16x2_bits(__uint_as_float(w.y << 16) * ksc, __uint_as_float(w.y & 0xffff0000u) * ksc);
+            }
+        } else if (r8 < G) {
             const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.q + ((int64_t)b * a.num_q_heads + h0 + r8) * D);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
@@ -280,12 +327,12 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
             if (!mbar_wait(&full[slot], round & 1)) { ok = false; break; }
             __syncwarp();
             const int n = min(kStageTok, k1 - t0);
-            uint8_t *kst = ring + slot * S::kStageBytes + warp * D * 2;
+            uint8_t *kst = ring + slot * S::kStageBytes + warp * D * EB;
             uint8_t *vst = kst + kStageTok * S::kRowStride;
             if (n < kStageTok) {
                 // rows past the last token hold stale shared memory: P is 0
                 // there, but 0 * NaN is not, so the V rows are zeroed
-                constexpr int kChunks = D * 2 / 16;
+                constexpr int kChunks = D * EB / 16;
                 for (int i = lane; i < (kStageTok - n) * kChunks; i += 32)
                     *reinterpret_cast<uint4 *>(vst + (n + i / kChunks) * S::kRowStride + (i % kChunks) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
@@ -295,11 +342,27 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
 
             // ---- S = K Q^T
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (F8) {
+                // one ldmatrix.x4 = two k-steps: matrices (tokens 0-7 | 8-15) x
+                // (codes 32 kp .. +15 | 32 kp + 16 .. +31) as b16 pairs
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                uint32_t af[4];
-                ldsm_x4(af, ks + a_tok * S::kRowStride + (kk * 16 + a_dim) * 2);
-                mma_bf16_16816(sc, af, qb[kk][0], qb[kk][1]);
+                for (int kp = 0; kp < KS / 2; ++kp) {
+                    uint32_t r[4];
+                    ldsm_x4(r, ks + a_tok * S::kRowStride + kp * 32 + a_dim * 2);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t af[4] = {e4m3x2_to_f16x2(r[2 * h]), e4m3x2_to_f16x2(r[2 * h + 1]),
+                                                e4m3x2_to_f16x2(r[2 * h] >> 16), e4m3x2_to_f16x2(r[2 * h + 1] >> 16)};
+                        mma_f16_16816(sc, af, qb[2 * kp + h][0], qb[2 * kp + h][1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    uint32_t af[4];
+                    ldsm_x4(af, ks + a_tok * S::kRowStride + (kk * 16 + a_dim) * 2);
+                    mma_bf16_16816(sc, af, qb[kk][0], qb[kk][1]);
+                }
             }
             // log2 domain; tokens past n masked
             float x[4];
@@ -332,20 +395,44 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
                 l_run[j] += p[j] + p[2 + j];
             }
             // ---- P^T through shared memory into the B-fragment layout
-            pw[(2 * q4) * kStageTok + r8] = bf16_bits(p[0]);
-            pw[(2 * q4 + 1) * kStageTok + r8] = bf16_bits(p[1]);
-            pw[(2 * q4) * kStageTok + r8 + 8] = bf16_bits(p[2]);
-            pw[(2 * q4 + 1) * kStageTok + r8 + 8] = bf16_bits(p[3]);
+            auto pbits = [](float x) -> uint16_t {
+                if constexpr (F8) return __half_as_ushort(__float2half_rn(x));
+                else return bf16_bits(x);
+            };
+            pw[(2 * q4) * kStageTok + r8] = pbits(p[0]);
+            pw[(2 * q4 + 1) * kStageTok + r8] = pbits(p[1]);
+            pw[(2 * q4) * kStageTok + r8 + 8] = pbits(p[2]);
+            pw[(2 * q4 + 1) * kStageTok + r8 + 8] = pbits(p[3]);
             __syncwarp();
             const uint32_t pb0 = *reinterpret_cast<const uint32_t *>(pw + r8 * kStageTok + 2 * q4);
             const uint32_t pb1 = *reinterpret_cast<const uint32_t *>(pw + r8 * kStageTok + 2 * q4 + 8);
 
             // ---- O^T += V^T P^T
+            if constexpr (F8) {
+                // transposed b16 pairs: lane (g, c) gets tokens 2c, 2c+1 of
+                // codes d = 2g, 2g+1 (bytes t2c.d0 t2c.d1 t2c1.d0 t2c1.d1);
+                // a byte permute groups them by d, so one register widens to
+                // O^T row 2g (tokens 2c, 2c+1) and the other to row 2g + 1
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                uint32_t vf[4];
-                ldsm_x4_trans(vf, vs + v_tok * S::kRowStride + (mt * 16 + v_dim) * 2);
-                mma_bf16_16816(oacc[mt], vf, pb0, pb1);
+                for (int mp = 0; mp < KS / 2; ++mp) {
+                    uint32_t r[4];
+                    ldsm_x4_trans(r, vs + a_tok * S::kRowStride + mp * 32 + a_dim * 2);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t p0 = __byte_perm(r[2 * h], 0u, 0x3120);
+                        const uint32_t p1 = __byte_perm(r[2 * h + 1], 0u, 0x3120);
+                        const uint32_t vf[4] = {e4m3x2_to_f16x2(p0), e4m3x2_to_f16x2(p0 >> 16),
+                                                e4m3x2_to_f16x2(p1), e4m3x2_to_f16x2(p1 >> 16)};
+                        mma_f16_16816(oacc[2 * mp + h], vf, pb0, pb1);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    uint32_t vf[4];
+                    ldsm_x4_trans(vf, vs + v_tok * S::kRowStride + (mt * 16 + v_dim) * 2);
+                    mma_bf16_16816(oacc[mt], vf, pb0, pb1);
+                }
             }
             // the zeroed rows were generic-proxy writes; the next bulk copy
             // into this slot is an async-proxy write
@@ -364,7 +451,7 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
             l += __shfl_xor_sync(0xffffffffu, l, 16);
             const int hh = 2 * q4 + j;                   // head within the group
             if (hh >= G) continue;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = (l > 0.f ? 1.f / l : 0.f) * (F8 ? __ldg(a.v_scale + kvh) : 1.f);
             const float lse_v = l > 0.f ? (m_run[j] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             const int h = h0 + hh;
             if (split < 0 || split >= a.max_splits) {       // cannot happen for valid lengths
@@ -375,8 +462,13 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
             float *orow = a.o_part + r * D;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
-                orow[mt * 16 + r8] = oacc[mt][j] * inv;
-                orow[mt * 16 + r8 + 8] = oacc[mt][2 + j] * inv;
+                if constexpr (F8) {          // rows g, g + 8 of the tile are d = 2g, 2g + 1
+                    *reinterpret_cast<float2 *>(orow + mt * 16 + 2 * r8) =
+                        make_float2(oacc[mt][j] * inv, oacc[mt][2 + j] * inv);
+                } else {
+                    orow[mt * 16 + r8] = oacc[mt][j] * inv;
+                    orow[mt * 16 + r8 + 8] = oacc[mt][2 + j] * inv;
+                }
             }
             if (r8 == 0) a.lse_part[r] = lse_v;
         }
@@ -444,12 +536,12 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(
     if (lse_out != nullptr && lane == 0) lse_out[row] = den > 0.f ? M + __logf(den) : -INFINITY;
 }
 
-template <int D, int G, int HPC>
+template <int D, int G, int HPC, bool F8>
 cudaError_t launch_decode_t(const DecodeArgs &a, int64_t items_max, cudaStream_t stream) {
-    using S = DecodeSmem<D, HPC>;
+    using S = DecodeSmem<D, HPC, F8 ? 1 : 2>;
     const size_t smem = S::kRingBytes + 2 * kStages * sizeof(uint64_t) +
                         HPC * 8 * kStageTok * sizeof(uint16_t) + (a.num_seqs + 1) * sizeof(int32_t);
-    auto kern = decode_kernel<D, G, HPC>;
+    auto kern = decode_kernel<D, G, HPC, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -462,23 +554,23 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int64_t items_max, cudaStream_t
     return cudaGetLastError();
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 cudaError_t dispatch_hpc(const DecodeArgs &a, int hpc, int64_t grid, cudaStream_t s) {
     switch (hpc) {
-        case 1: return launch_decode_t<D, G, 1>(a, grid, s);
-        case 2: return launch_decode_t<D, G, 2>(a, grid, s);
-        case 4: return launch_decode_t<D, G, 4>(a, grid, s);
+        case 1: return launch_decode_t<D, G, 1, F8>(a, grid, s);
+        case 2: return launch_decode_t<D, G, 2, F8>(a, grid, s);
+        case 4: return launch_decode_t<D, G, 4, F8>(a, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t dispatch_g(const DecodeArgs &a, int g, int hpc, int64_t grid, cudaStream_t s) {
     switch (g) {
-        case 1: return dispatch_hpc<D, 1>(a, hpc, grid, s);
-        case 2: return dispatch_hpc<D, 2>(a, hpc, grid, s);
-        case 4: return dispatch_hpc<D, 4>(a, hpc, grid, s);
-        case 8: return dispatch_hpc<D, 8>(a, hpc, grid, s);
+        case 1: return dispatch_hpc<D, 1, F8>(a, hpc, grid, s);
+        case 2: return dispatch_hpc<D, 2, F8>(a, hpc, grid, s);
+        case 4: return dispatch_hpc<D, 4, F8>(a, hpc, grid, s);
+        case 8: return dispatch_hpc<D, 8, F8>(a, hpc, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -530,6 +622,8 @@ cudaError_t launch_decode(const pa_decode_params &p, const DecodePlan &plan, cud
     a.head_groups = p.num_kv_heads / plan.heads_per_cta;
     a.out = static_cast<__nv_bfloat16 *>(p.out);
     a.lse = p.lse;
+    a.k_scale = p.k_scale;
+    a.v_scale = p.v_scale;
     {
         // workspace: [T | pad to 256][prefix B+1 | pad][O partials][lse partials]
         uint8_t *ws = static_cast<uint8_t *>(p.workspace);
@@ -546,8 +640,14 @@ cudaError_t launch_decode(const pa_decode_params &p, const DecodePlan &plan, cud
     const int64_t items_max = ((int64_t)p.num_seqs * p.max_seqlen_k * a.head_groups + plan.kv_chunk - 1) /
                               plan.kv_chunk + 1;
     const int g = p.num_q_heads / p.num_kv_heads;
-    cudaError_t e = p.head_dim == 64 ? dispatch_g<64>(a, g, plan.heads_per_cta, items_max, stream)
-                                     : dispatch_g<128>(a, g, plan.heads_per_cta, items_max, stream);
+    const bool f8 = p.kv_dtype == PA_KV_FP8_E4M3;
+    cudaError_t e;
+    if (f8)
+        e = p.head_dim == 64 ? dispatch_g<64, true>(a, g, plan.heads_per_cta, items_max, stream)
+                             : dispatch_g<128, true>(a, g, plan.heads_per_cta, items_max, stream);
+    else
+        e = p.head_dim == 64 ? dispatch_g<64, false>(a, g, plan.heads_per_cta, items_max, stream)
+                             : dispatch_g<128, false>(a, g, plan.heads_per_cta, items_max, stream);
     if (e != cudaSuccess) return e;
     return launch_lse_combine(a.o_part, a.lse_part, nullptr, a.ws_header, a.ws_prefix, a.head_groups,
                               g * plan.heads_per_cta, p.num_q_heads, p.num_seqs * p.num_q_heads,

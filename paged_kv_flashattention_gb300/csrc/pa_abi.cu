@@ -120,6 +120,25 @@ pa_status pa_store_kv(const void *k, const void *v, const int32_t *slot_mapping,
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "store_kv launch");
 }
 
+pa_status pa_store_kv_fp8(const void *k, const void *v, const int32_t *slot_mapping, int64_t num_tokens,
+                          void *k_cache, void *v_cache, int64_t num_slots, int32_t num_kv_heads,
+                          int32_t head_dim, const float *k_scale, const float *v_scale, void *stream) {
+    g_last_error[0] = 0;
+    if (num_tokens < 0 || num_slots < 0) return fail(PA_ERR_INVALID, "negative num_tokens or num_slots");
+    if (num_kv_heads <= 0 || head_dim <= 0) return fail(PA_ERR_INVALID, "num_kv_heads and head_dim must be positive");
+    if (head_dim % 16 != 0) return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not a multiple of 16", head_dim);
+    if ((int64_t)num_kv_heads * head_dim > (1 << 20)) return fail(PA_ERR_UNSUPPORTED, "K/V row too large");
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+        return fail(PA_ERR_INVALID, "NULL pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID, "K/V pointers must be 16-byte aligned");
+    cudaError_t e = launch_store_kv_fp8(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_slots,
+                                        num_kv_heads, head_dim, k_scale, v_scale,
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "store_kv_fp8 launch");
+}
+
 pa_status pa_build_seqlens(const int32_t *cached_len, const int32_t *extend_len, int32_t num_seqs,
                            int32_t *cu_seqlens_q, int32_t *cu_seqlens_k, int32_t *cache_seqlens,
                            int32_t *max_seqlen_q, int32_t *max_seqlen_k) {
@@ -215,6 +234,10 @@ static pa_status check_decode(const pa_decode_params *p) {
     if (!(p->scale == p->scale)) return fail(PA_ERR_INVALID, "scale is NaN");
     if (p->num_pages > (int64_t)INT32_MAX / p->page_size)
         return fail(PA_ERR_UNSUPPORTED, "pool larger than 2^31 slots");
+    if (p->kv_dtype != PA_KV_BF16 && p->kv_dtype != PA_KV_FP8_E4M3)
+        return fail(PA_ERR_INVALID, "kv_dtype %d is neither PA_KV_BF16 nor PA_KV_FP8_E4M3", p->kv_dtype);
+    if (p->kv_dtype == PA_KV_FP8_E4M3 && p->num_seqs > 0 && (!p->k_scale || !p->v_scale))
+        return fail(PA_ERR_INVALID, "FP8 pools need k_scale and v_scale");
     return PA_OK;
 }
 

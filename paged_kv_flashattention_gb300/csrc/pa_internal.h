@@ -13,6 +13,11 @@ cudaError_t launch_store_kv(const void *k, const void *v, const int32_t *slot_ma
                             int64_t num_tokens, void *k_cache, void *v_cache, int64_t num_slots,
                             int32_t row_bytes, cudaStream_t stream);
 
+cudaError_t launch_store_kv_fp8(const void *k, const void *v, const int32_t *slot_mapping,
+                                int64_t num_tokens, void *k_cache, void *v_cache, int64_t num_slots,
+                                int32_t num_kv_heads, int32_t head_dim, const float *k_scale,
+                                const float *v_scale, cudaStream_t stream);
+
 cudaError_t launch_build_page_table(const int32_t *token_table, int64_t tt_stride,
                                     const int32_t *table_idx, int32_t num_seqs, int32_t ncols,
                                     int32_t page_size, int32_t *page_table, int32_t pt_stride,

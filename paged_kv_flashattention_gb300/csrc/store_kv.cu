@@ -7,6 +7,13 @@
 // per step, so a warp's accesses are contiguous 512-byte runs.  The work is
 // pure data movement, bounded by HBM (read 2 rows, write 2 rows per token).
 //
+// FP8 store: the pages list FP8 / quantized KV as a dispatch axis and a KV
+// layout (same page, sections 19 and 24) without fixing a format; here an
+// element x of KV head h is stored as the E4M3 code nearest x / scale[h]
+// (the division correctly rounded in single precision, the conversion the
+// hardware's round-to-nearest-even with saturation to +-448).  One warp per
+// token as above; a lane converts 8 elements (16 bytes in, 8 bytes out).
+//
 // Page table: "code-series sgl-project mini-sglang 07", "from ledger to
 // tensors": the global table is token granular; a request's row is sliced
 // with step page_size up to max_seqlen_k and floor-divided by page_size.
@@ -48,6 +55,55 @@ __global__ void __launch_bounds__(256) store_kv_kernel(const uint4 *__restrict__
     }
 }
 
+// Two floats to two E4M3 codes, lo in the low byte (the first operand of the
+// conversion lands in the high byte).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint2 quantize8(uint4 x, float s) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+        q[i] = f32x2_to_e4m3x2(__fdiv_rn(lo, s), __fdiv_rn(hi, s));
+    }
+    return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+}
+
+__global__ void __launch_bounds__(256) store_kv_fp8_kernel(const uint4 *__restrict__ k,
+                                                           const uint4 *__restrict__ v,
+                                                           const int32_t *__restrict__ slot_mapping,
+                                                           int64_t num_tokens, uint2 *k_cache,
+                                                           uint2 *v_cache, int64_t num_slots,
+                                                           int32_t row_groups, int32_t head_dim,
+                                                           const float *__restrict__ k_scale,
+                                                           const float *__restrict__ v_scale) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < num_tokens;
+         t += warps_total) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;                 // padding token
+        if (slot >= num_slots) {                // never write outside the pool
+            if (lane == 0) raise_error(PA_DEVERR_PAGE_RANGE);
+            continue;
+        }
+        const uint4 *ks = k + t * row_groups;
+        const uint4 *vs = v + t * row_groups;
+        uint2 *kd = k_cache + slot * row_groups;
+        uint2 *vd = v_cache + slot * row_groups;
+        for (int i = lane; i < row_groups; i += 32) {
+            const int h = (i * 8) / head_dim;   // 8 | head_dim: a group never straddles heads
+            kd[i] = quantize8(__ldg(ks + i), __ldg(k_scale + h));
+            vd[i] = quantize8(__ldg(vs + i), __ldg(v_scale + h));
+        }
+    }
+}
+
 __global__ void build_page_table_kernel(const int32_t *__restrict__ token_table, int64_t tt_stride,
                                         const int32_t *__restrict__ table_idx, int32_t num_seqs,
                                         int32_t ncols, int32_t page_size, int32_t *page_table,
@@ -67,6 +123,22 @@ __global__ void build_page_table_kernel(const int32_t *__restrict__ token_table,
 }
 
 }  // namespace
+
+cudaError_t launch_store_kv_fp8(const void *k, const void *v, const int32_t *slot_mapping,
+                                int64_t num_tokens, void *k_cache, void *v_cache, int64_t num_slots,
+                                int32_t num_kv_heads, int32_t head_dim, const float *k_scale,
+                                const float *v_scale, cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int warps_per_block = 8;
+    int64_t blocks = (num_tokens + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = (int64_t)num_sms() * 16;
+    if (blocks > cap) blocks = cap;
+    store_kv_fp8_kernel<<<(unsigned)blocks, warps_per_block * 32, 0, stream>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
+        static_cast<uint2 *>(k_cache), static_cast<uint2 *>(v_cache), num_slots,
+        num_kv_heads * head_dim / 8, head_dim, k_scale, v_scale);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_store_kv(const void *k, const void *v, const int32_t *slot_mapping,
                             int64_t num_tokens, void *k_cache, void *v_cache, int64_t num_slots,

@@ -118,6 +118,8 @@ def test_prefill_rejects_before_launch(lib, kw, status):
     (dict(k_cache=0x2008), INVALID),
     (dict(page_table_stride=8), INVALID),
     (dict(num_seqs=20000), UNSUPPORTED),
+    (dict(kv_dtype=2), INVALID),
+    (dict(kv_dtype=1), INVALID),                              # FP8 without scales
 ])
 def test_decode_rejects_before_launch(lib, kw, status):
     assert _decode(lib, **kw) == status
@@ -129,6 +131,11 @@ def test_store_rejects_before_launch(lib):
     assert lib.pa_store_kv(0x1000, 0x2000, 0x3000, 4, 0x4000, 0x5000, 64, 1, 4, None) == UNSUPPORTED
     # zero tokens: nothing to do, nothing launched
     assert lib.pa_store_kv(0, 0, 0, 0, 0, 0, 0, 2, 64, None) == 0
+    # FP8 store: scales required, head_dim a multiple of 16
+    assert lib.pa_store_kv_fp8(0x1000, 0x2000, 0x3000, 4, 0x4000, 0x5000, 64, 2, 64, None, 0x6000, None) == INVALID
+    assert lib.pa_store_kv_fp8(0x1000, 0x2000, 0x3000, 4, 0x4000, 0x5000, 64, 2, 72, 0x6000, 0x7000, None) == UNSUPPORTED
+    assert lib.pa_store_kv_fp8(0x1008, 0x2000, 0x3000, 4, 0x4000, 0x5000, 64, 2, 64, 0x6000, 0x7000, None) == INVALID
+    assert lib.pa_store_kv_fp8(0, 0, 0, 0, 0, 0, 0, 2, 64, None, None, None) == 0
 
 
 def test_decode_workspace_size_host_only(lib):

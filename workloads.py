@@ -68,6 +68,34 @@ def normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
     return out.reshape(shape)
 
 
+E4M3_NAN = np.uint8(0x7F)
+
+
+def e4m3_codes(rng: np.random.Generator, shape, exp_lo: int = 4, exp_hi: int = 9) -> np.ndarray:
+    """Random E4M3 codes (uint8) for an FP8 pool: random sign, exponent field
+    uniform in [exp_lo, exp_hi] (magnitudes 2^(e-7) .. 1.875 * 2^(e-7)), random
+    mantissa; never a NaN code.  The default spans 0.125 .. 7.5, the spread
+    of quantised N(0, 1)-like data."""
+    sign = (rng.integers(0, 2, size=shape, dtype=np.uint8) << 7).astype(np.uint8)
+    e = (rng.integers(exp_lo, exp_hi + 1, size=shape, dtype=np.uint8) << 3).astype(np.uint8)
+    m = rng.integers(0, 8, size=shape, dtype=np.uint8)
+    return (sign | e | m).astype(np.uint8)
+
+
+def fp8_pools(p: "Problem", seed: int, scale_lo: float = 0.1, scale_hi: float = 0.5):
+    """FP8 stand-ins for a Problem's pools: (k_codes, v_codes, k_scale,
+    v_scale) with the pool's shape, the last (poison) page holding NaN codes,
+    and one float32 scale per KV head drawn from U[scale_lo, scale_hi]."""
+    rng = np.random.default_rng(seed)
+    kc = e4m3_codes(rng, p.k_cache.shape)
+    vc = e4m3_codes(rng, p.v_cache.shape)
+    kc[p.num_pages - 1] = E4M3_NAN
+    vc[p.num_pages - 1] = E4M3_NAN
+    ks = rng.uniform(scale_lo, scale_hi, size=p.num_kv_heads).astype(np.float32)
+    vs = rng.uniform(scale_lo, scale_hi, size=p.num_kv_heads).astype(np.float32)
+    return kc, vc, ks, vs
+
+
 @dataclass
 class Problem:
     """One batch of requests over one paged KV pool.
