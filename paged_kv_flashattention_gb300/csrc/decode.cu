@@ -56,7 +56,12 @@ PA_ERROR_WORD_ACCESSOR(error_word_decode)
 namespace {
 
 constexpr int kStageTok = 16;     // tokens per pipeline stage
-constexpr int kStages = 3;        // ring depth
+// Ring depth.  FP8 keeps 3 stages of half-length rows: the smaller ring lets
+// 4 CTAs share an SM instead of 2, which measured faster than 6 stages at 2
+// CTAs (each CTA's consumers work through one stage at a time).
+template <int EB>
+constexpr int stages_for() { return EB == 1 ? 3 : 3; }
+constexpr int kFp8MaxHeadsPerCta = 4;
 constexpr float kLazyRescale = 8.0f;  // log2 units
 
 struct DecodeArgs {
@@ -91,6 +96,7 @@ struct DecodeSmem {
     static constexpr int kRowBytes = HPC * D * EB;           // one token, CTA's KV heads (EB bytes each)
     static constexpr int kRowStride = kRowBytes + 16;        // +16 B: ldmatrix rows hit distinct banks
     static constexpr int kStageBytes = 2 * kStageTok * kRowStride;
+    static constexpr int kStages = stages_for<EB>();
     static constexpr int kRingBytes = kStages * kStageBytes;
 };
 
@@ -173,6 +179,7 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kRingBytes);
+    constexpr int kStages = S::kStages;
     uint64_t *empty = full + kStages;
     uint16_t *pbuf = reinterpret_cast<uint16_t *>(empty + kStages);   // [HPC][8 heads][16 tokens] bf16 / f16
     int32_t *prefix = reinterpret_cast<int32_t *>(pbuf + HPC * 8 * kStageTok);  // [B+1]
@@ -539,7 +546,7 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(
 template <int D, int G, int HPC, bool F8>
 cudaError_t launch_decode_t(const DecodeArgs &a, int64_t items_max, cudaStream_t stream) {
     using S = DecodeSmem<D, HPC, F8 ? 1 : 2>;
-    const size_t smem = S::kRingBytes + 2 * kStages * sizeof(uint64_t) +
+    const size_t smem = S::kRingBytes + 2 * S::kStages * sizeof(uint64_t) +
                         HPC * 8 * kStageTok * sizeof(uint16_t) + (a.num_seqs + 1) * sizeof(int32_t);
     auto kern = decode_kernel<D, G, HPC, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -560,6 +567,9 @@ cudaError_t dispatch_hpc(const DecodeArgs &a, int hpc, int64_t grid, cudaStream_
         case 1: return launch_decode_t<D, G, 1, F8>(a, grid, s);
         case 2: return launch_decode_t<D, G, 2, F8>(a, grid, s);
         case 4: return launch_decode_t<D, G, 4, F8>(a, grid, s);
+        case 8:
+            if constexpr (F8) return launch_decode_t<D, G, 8, F8>(a, grid, s);
+            else return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -582,8 +592,11 @@ DecodePlan plan_decode(const pa_decode_params &p) {
     // KV heads per CTA: the largest power of two <= 4 dividing Hkv (token
     // rows of 512 B at d = 64, 1 KiB at d = 128; a 3-stage ring of 48 or
     // 96 KiB, so two or more CTAs fit on an SM).
+    // FP8 rows are half as long: up to 8 heads, so a copy still moves >= 1 KiB
+    // at d = 128.
+    const int max_hpc = p.kv_dtype == PA_KV_FP8_E4M3 ? kFp8MaxHeadsPerCta : 4;
     int hpc = 1;
-    while (hpc * 2 <= 4 && p.num_kv_heads % (hpc * 2) == 0) hpc *= 2;
+    while (hpc * 2 <= max_hpc && p.num_kv_heads % (hpc * 2) == 0) hpc *= 2;
     plan.heads_per_cta = hpc;
     // Minimum split (the floor of T): the caller's kv_chunk, else 1/32 of the
     // longest context (>= 64 keys).  It bounds the splits of one row by
