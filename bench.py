@@ -451,6 +451,9 @@ MICRO_CASES = {
     # the same decode workloads over FP8 (E4M3) pools with per-head scales
     "llama32_1b_decode_fp8": (2, None, "decode"),
     "decode_64seq_logu_fp8": (None, None, "decode"),
+    "varlen_prefill_16x512_fp8": (3, None, "prefill"),
+    "extend_partial_hit_p16_fp8": (4, None, "prefill"),
+    "extend_partial_hit_p1_fp8": (4, "p1", "prefill"),
 }
 
 
@@ -500,7 +503,8 @@ def run_micro(args):
         unit = "GB/s"
     elif kernel == "prefill":
         fn = lambda: pa.prefill(q, kc, vc, m.page_table, m.cu_seqlens_q, m.cu_seqlens_k,
-                                m.max_seqlen_q, m.max_seqlen_k, causal=p.causal, scale=p.scale, out=out)
+                                m.max_seqlen_q, m.max_seqlen_k, causal=p.causal, scale=p.scale, out=out,
+                                **scales)
         off = p.cached_len.astype(np.int64)
         E = p.extend_len.astype(np.int64)
         work = 4 * D * Hq * int(np.sum(E * off + E * (E + 1) // 2))

@@ -150,6 +150,12 @@ pa_status pa_build_page_table(const int32_t *token_table, int64_t token_table_st
                               int32_t max_seqlen_k, int32_t page_size, int32_t *page_table,
                               int32_t page_table_stride, void *stream);
 
+/* Element type of the K/V pools read by pa_prefill and pa_decode.  FP8 pools hold E4M3
+ * codes written by pa_store_kv_fp8 with per-KV-head scales.  On FP8 pools the
+ * contractions run in f16 with fp32 accumulation: q * k_scale is rounded to
+ * f16 (|q * k_scale| must stay below 65504), P is rounded to f16. */
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+
 /*
  * pa_prefill - varlen prefill / extend attention ([T] s.10-15, [M]).
  * For request b: Lq = cu_seqlens_q[b+1] - cu_seqlens_q[b] queries (the extend
@@ -187,15 +193,12 @@ typedef struct {
     void *out;                   /* bf16 [total_q, Hq, d] */
     float *lse;                  /* optional fp32 [Hq, lse_stride]; NULL = not written */
     int64_t lse_stride;          /* >= total_q when lse != NULL */
+    int32_t kv_dtype;            /* pa_kv_dtype of k_cache / v_cache (0 = bf16) */
+    const float *k_scale;        /* PA_KV_FP8_E4M3: device fp32 [Hkv]; else unused */
+    const float *v_scale;
 } pa_prefill_params;
 
 pa_status pa_prefill(const pa_prefill_params *p, void *stream);
-
-/* Element type of the K/V pools read by pa_decode.  FP8 pools hold E4M3
- * codes written by pa_store_kv_fp8 with per-KV-head scales.  On FP8 pools the
- * contractions run in f16 with fp32 accumulation: q * k_scale is rounded to
- * f16 (|q * k_scale| must stay below 65504), P is rounded to f16. */
-typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
 
 /*
  * pa_decode - decode attention ([T] s.13 and s.16): one query token per

@@ -32,6 +32,7 @@ class PrefillParams(ctypes.Structure):
         ("num_q_heads", c_i32), ("num_kv_heads", c_i32), ("head_dim", c_i32),
         ("page_size", c_i32), ("num_pages", c_i64), ("causal", c_i32), ("scale", c_f32),
         ("out", c_p), ("lse", c_p), ("lse_stride", c_i64),
+        ("kv_dtype", c_i32), ("k_scale", c_p), ("v_scale", c_p),
     ]
 
 

@@ -196,13 +196,20 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
             cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int,
             max_seqlen_k: int, *, causal: bool = True, scale: float | None = None,
             page_size: int | None = None, out: torch.Tensor | None = None,
-            lse: torch.Tensor | None = None) -> torch.Tensor:
+            lse: torch.Tensor | None = None, k_scale: torch.Tensor | None = None,
+            v_scale: torch.Tensor | None = None) -> torch.Tensor:
     """Varlen prefill / extend attention.  q: bf16 [total_q, Hq, d];
-    returns out bf16 [total_q, Hq, d]; lse (optional) fp32 [Hq, total_q]."""
+    returns out bf16 [total_q, Hq, d]; lse (optional) fp32 [Hq, total_q].
+    Pools are bf16, or E4M3 codes (uint8 / float8_e4m3fn) with fp32
+    per-KV-head ``k_scale`` and ``v_scale``."""
     dev = q.device
     num_pages, P, Hkv, d = _pool_geometry(k_cache, v_cache, page_size)
-    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t, n, torch.bfloat16, dev)
+    _need(q, "q", torch.bfloat16, dev)
+    kvd = _kv_dtype(k_cache, v_cache)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, k_cache.dtype, dev)
+    if kvd == PA_KV_FP8_E4M3:
+        _need_scales(k_scale, v_scale, Hkv, dev)
     for t, n in ((page_table, "page_table"), (cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
         _need(t, n, torch.int32, dev, contiguous=(n != "page_table"))
     if page_table.dim() != 2 or page_table.stride(1) != 1:
@@ -224,7 +231,9 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
         max_seqlen_q=int(max_seqlen_q), max_seqlen_k=int(max_seqlen_k), num_q_heads=Hq,
         num_kv_heads=Hkv, head_dim=d, page_size=P, num_pages=num_pages, causal=int(bool(causal)),
         scale=float(1.0 / math.sqrt(d) if scale is None else scale), out=_ptr(out),
-        lse=_ptr(lse), lse_stride=(lse.stride(0) if lse is not None else 0))
+        lse=_ptr(lse), lse_stride=(lse.stride(0) if lse is not None else 0), kv_dtype=kvd,
+        k_scale=_ptr(k_scale) if kvd == PA_KV_FP8_E4M3 else None,
+        v_scale=_ptr(v_scale) if kvd == PA_KV_FP8_E4M3 else None)
     lib = _lib.load()
     _check(lib.pa_prefill(ctypes.byref(p), _stream(q)), lib)
     return out

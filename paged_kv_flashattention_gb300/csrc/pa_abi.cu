@@ -218,6 +218,10 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
     if (p->lse != nullptr && p->lse_stride <= 0) return fail(PA_ERR_INVALID, "lse_stride must be positive");
     if (p->num_pages > (int64_t)INT32_MAX / p->page_size)
         return fail(PA_ERR_UNSUPPORTED, "pool larger than 2^31 slots");
+    if (p->kv_dtype != PA_KV_BF16 && p->kv_dtype != PA_KV_FP8_E4M3)
+        return fail(PA_ERR_INVALID, "kv_dtype %d is neither PA_KV_BF16 nor PA_KV_FP8_E4M3", p->kv_dtype);
+    if (p->kv_dtype == PA_KV_FP8_E4M3 && (!p->k_scale || !p->v_scale))
+        return fail(PA_ERR_INVALID, "FP8 pools need k_scale and v_scale");
     cudaError_t e = launch_prefill(*p, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "prefill configuration not supported by this build");
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "prefill launch");

@@ -43,6 +43,15 @@
 //     columns with tcgen05.st, and at the
 //     end normalises O and writes bf16 output and the natural-log LSE.
 // TMEM (512 columns): S_k at [128k, 128k+128), O_k at [256 + 128k, +d).
+//
+// FP8 pools (E4M3 codes with a scale per KV head; the first page lists FP8 /
+// quantized KV as a dispatch axis, section 19): tcgen05 kind::f16 needs 16-bit
+// operands on both sides, so the E4M3 tiles land in a separate ring (one
+// byte per element, no swizzle) and the two otherwise idle warps of the
+// control warpgroup widen them exactly to f16 into the swizzled layout the
+// MMA reads, and turn each item's Q tiles in place into f16 q * k_scale.
+// The MMAs then run with f16 operands (P is written to TMEM as f16) and the
+// epilogue multiplies by v_scale.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -118,6 +127,8 @@ struct PrefillArgs {
     int32_t causal;
     float scale_log2;
     int32_t num_virtual;          // max_tiles * num_seqs * (Hq / T) work-item slots
+    const float *k_scale;         // FP8 pools: per-KV-head scales
+    const float *v_scale;
     int32_t *sched;               // [0] next item, [1] CTAs finished; both 0 between launches
 };
 
@@ -197,19 +208,49 @@ __device__ void prefill_sched_done(const PrefillArgs &a) {
 // tiles ahead of the MMAs: with one CTA per SM the loads from L2 are latency
 // bound, and bytes in flight set the rate (at d = 128 with two heads, 4
 // slots measured as fast as 5).
-template <int D, int T>
+template <int D, int T, bool F8>
 struct PrefillSmem {
     static constexpr int kHalves = D / 64;                 // 64-column (128-byte) halves
-    static constexpr int kTileBytes = kHalves * 128 * 128; // 128 rows x D bf16
+    static constexpr int kTileBytes = kHalves * 128 * 128; // 128 rows x D, 16-bit elements
+    static constexpr int kLTile = F8 ? kTileBytes / 2 : kTileBytes;   // a tile as loaded
     static constexpr int kQ = 0;                           // T query tiles
-    static constexpr int kRing = T * kTileBytes;
+    static constexpr int kRing = T * kTileBytes;           // ring of loaded tiles
     static constexpr int kStageBytes = 4 * T * 4096;      // 32 rows x 64 columns bf16 per warp
-    static constexpr int kSlotsFit = (232448 - 1024 - kRing - kStageBytes - 512) / kTileBytes;
+    static constexpr int kAvail = 232448 - 1024 - kRing - kStageBytes - 512;
+    // FP8: ring of widened f16 tiles (2..4 slots), loaded-tile ring from the rest
+    static constexpr int kCSlotsFit = (kAvail / 2) / kTileBytes;
+    static constexpr int kCSlots = !F8 ? 0 : (kCSlotsFit > 4 ? 4 : (kCSlotsFit < 2 ? 2 : kCSlotsFit));
+    static constexpr int kSlotsFit = (kAvail - kCSlots * kTileBytes) / kLTile;
     static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;
-    static constexpr int kStage = kRing + kSlots * kTileBytes;
+    static constexpr int kConv = kRing + kSlots * kLTile;
+    static constexpr int kStage = kConv + kCSlots * kTileBytes;
     static constexpr int kBars = kStage + kStageBytes;
     static constexpr int kTotal = kBars + 512;
 };
+
+// Eight bf16 (one 16-byte piece of a Q tile) to eight f16 of x * s.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 x, float s) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * s, __uint_as_float(w[i] & 0xffff0000u) * s);
+        o[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Two E4M3 codes (low byte first) to two f16 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two_codes));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
@@ -227,9 +268,9 @@ constexpr int kSoftmaxRegs = 184;
 constexpr int kItemRing = 4;      // items published ahead of the consumers
 constexpr int kControlRegs = 128;
 
-template <int D, int T>
+template <int D, int T, bool F8>
 __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
-    using S = PrefillSmem<D, T>;
+    using S = PrefillSmem<D, T, F8>;
     constexpr int H = S::kHalves;
     constexpr int kProducer = 4 * T;
     constexpr int kMma = 4 * T + 1;
@@ -241,13 +282,19 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBars);
     constexpr int NS = S::kSlots;
     // each gather warp has at most one load in flight and signals it when it
-    // is complete, so G < NS leaves the MMA a slot
-    constexpr int kGatherWarps = NS - 1 < kGatherWarpsMax ? NS - 1 : kGatherWarpsMax;
+    // is complete, so G < NS leaves the MMA a slot; with FP8 pools the two
+    // spare warps widen tiles instead
+    constexpr int kGatherWarps = F8 ? 1 : (NS - 1 < kGatherWarpsMax ? NS - 1 : kGatherWarpsMax);
+    constexpr int NC = F8 ? S::kCSlots : NS;  // slots the MMA reads from
+    constexpr int kConverters = F8 ? 2 : 0;
     uint64_t *q_full = bars;                 // 1: Q tiles of the item loaded
     uint64_t *q_empty = bars + 1;            // 1: every S MMA of the item done
     uint64_t *full = bars + 2;               // NS: slot loaded
-    uint64_t *empty = full + NS;             // NS: slot consumed by the MMAs
-    uint64_t *s_full = empty + NS;           // T
+    uint64_t *empty = full + NS;             // NS: slot consumed (by the MMAs, or widened)
+    uint64_t *cfull = empty + NS;            // FP8, NC: widened slot ready
+    uint64_t *cempty = cfull + (F8 ? NC : 0);  // FP8, NC: widened slot consumed by the MMAs
+    uint64_t *q_conv = cempty + (F8 ? NC : 0); // FP8, 1: Q tiles widened to f16
+    uint64_t *s_full = q_conv + 1;           // T
     uint64_t *p_full = s_full + T;           // T
     uint64_t *o_final = p_full + T;          // T: every MMA of O_k of an item (with keys) done
     constexpr int R = kItemRing;
@@ -270,7 +317,14 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         mbar_init(q_empty, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], paged16 ? 1 : 32);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], F8 ? kConverters : 1);
+        }
+        if (F8) {
+            for (int s = 0; s < NC; ++s) {
+                mbar_init(&cfull[s], kConverters);
+                mbar_init(&cempty[s], 1);
+            }
+            mbar_init(q_conv, kConverters);
         }
         for (int k = 0; k < T; ++k) {
             mbar_init(&s_full[k], 1);
@@ -279,7 +333,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         for (int k = 0; k < T; ++k) mbar_init(&o_final[k], 1);
         for (int i = 0; i < R; ++i) {
             mbar_init(&item_full[i], 1);
-            mbar_init(&item_empty[i], 1 + 4 * T + (paged16 ? 0 : kGatherWarps - 1));
+            mbar_init(&item_empty[i], 1 + 4 * T + (paged16 ? 0 : kGatherWarps - 1) + kConverters);
         }
         fence_mbar_init();
     }
@@ -304,6 +358,35 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         }
     };
     auto gather_copy = [&](const PrefillItem &it, int c, int gl, const int (&rows)[kBN / 32]) {
+        if constexpr (F8) {
+            // E4M3 rows of D bytes, copied as they are (row-major, no swizzle)
+            constexpr int kChunks = D / 16;
+            constexpr int kRowsPerIssue = 32 / kChunks;
+            uint8_t *dst = smem + S::kRing + (gl % NS) * S::kLTile;
+            const uint8_t *src = (c & 1) ? a.v_cache : a.k_cache;
+            const int key0 = (c >> 1) * kBN;
+            const int q = lane % kChunks, sub = lane / kChunks;
+#pragma unroll 1
+            for (int rr = 0; rr < kBN / 32; ++rr) {
+                int row = rr == 0 ? rows[0] : rr == 1 ? rows[1] : rr == 2 ? rows[2] : rows[3];
+                if (key0 + rr * 32 + lane < it.kv_end && (row < 0 || row >= a.num_slots)) {
+                    raise_error(PA_DEVERR_PAGE_RANGE);
+                    row = -1;
+                }
+#pragma unroll 4
+                for (int i = 0; i < 32 / kRowsPerIssue; ++i) {
+                    const int rl = i * kRowsPerIssue + sub;
+                    const int rowv = __shfl_sync(0xffffffffu, row, rl);
+                    const int r = rr * 32 + rl;
+                    if (rowv >= 0)
+                        cp_async16(dst + r * D + q * 16, src + ((int64_t)rowv * a.num_kv_heads + it.kvh) * (int64_t)D + q * 16);
+                    else
+                        *reinterpret_cast<uint4 *>(dst + r * D + q * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            cp_async_commit();
+            return;
+        }
         constexpr int kChunks = D / 8;                // 16-byte chunks per row
         constexpr int kRowsPerIssue = 32 / kChunks;   // 2 (d = 128) or 4 (d = 64)
         uint8_t *dst = smem + S::kRing + (gl % NS) * S::kTileBytes;
@@ -430,15 +513,19 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                     if (!(c & 1)) slot0 = page_slot0(it, c >> 1, page);
                     const int slot = gl % NS, round = gl / NS;
                     if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) { ok = false; break; }
-                    uint8_t *dst = smem + S::kRing + slot * S::kTileBytes;
+                    uint8_t *dst = smem + S::kRing + slot * S::kLTile;
                     // lanes 0..7 each own one 16-token page of the tile
-                    if (lane == 0) mbar_arrive_expect_tx(&full[slot], S::kTileBytes);
+                    if (lane == 0) mbar_arrive_expect_tx(&full[slot], S::kLTile);
                     __syncwarp();
                     if (lane < kBN / 16) {
                         const CUtensorMap *map = (c & 1) ? &a.vmap : &a.kmap;
+                        if constexpr (F8) {           // one (D bytes x 16 rows) box per page
+                            tma_load_3d(dst + lane * 16 * D, map, 0, it.kvh, slot0, &full[slot]);
+                        } else {
 #pragma unroll
-                        for (int hh = 0; hh < H; ++hh)
-                            tma_load_3d(dst + hh * 16384 + lane * 2048, map, hh * 64, it.kvh, slot0, &full[slot]);
+                            for (int hh = 0; hh < H; ++hh)
+                                tma_load_3d(dst + hh * 16384 + lane * 2048, map, hh * 64, it.kvh, slot0, &full[slot]);
+                        }
                     }
                     // K_j and V_j share pages; after K_j start reading the next step's
                     if (!(c & 1) && c + 2 < 2 * it.n_kv) page = page_id(it, (c >> 1) + 1);
@@ -468,20 +555,80 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             if (!gather_item(it, gl, g)) break;
             gl += 2 * it.n_kv;
         }
+      } else if (F8 && warp > kMma) {
+        // -------------------------------------- FP8 widening (2 warps) ----
+        const int cw = warp - kMma - 1;                 // 0, 1: rows [64 cw, 64 cw + 64)
+        int local = 0, gl = 0;
+        bool ok = true;
+        PrefillItem it;
+        while (ok) {
+            const int slot = local % R;
+            if (!__all_sync(0xffffffffu, mbar_wait(&item_full[slot], (local / R) & 1))) break;
+            const int v = item_idx[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[slot]);
+            if (v < 0) break;
+            prefill_item<T>(a, v, it);
+            // Q tiles: bf16 -> f16 of q * k_scale, in place
+            if (!__all_sync(0xffffffffu, mbar_wait(q_full, local & 1))) break;
+            ++local;
+            const float ksc = __ldg(a.k_scale + it.kvh);
+            for (int i = cw * 32 + lane; i < T * S::kTileBytes / 16; i += 64) {
+                uint4 *pq = reinterpret_cast<uint4 *>(sQ + i * 16);
+                *pq = bf16x8_to_f16x8_scaled(*pq, ksc);
+            }
+            fence_proxy_async_smem();                   // generic writes -> MMA (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_conv);
+            // K/V tiles: E4M3 rows -> f16 in the swizzled K-major layout
+            for (int c = 0; c < 2 * it.n_kv; ++c, ++gl) {
+                const int ls = gl % NS, cs = gl % NC;
+                ok = __all_sync(0xffffffffu, mbar_wait(&full[ls], (gl / NS) & 1));
+                if (ok && gl >= NC) ok = __all_sync(0xffffffffu, mbar_wait(&cempty[cs], ((gl / NC) - 1) & 1));
+                if (!ok) break;
+                const uint8_t *src = smem + S::kRing + ls * S::kLTile;
+                uint8_t *dst = smem + S::kConv + cs * S::kTileBytes;
+#pragma unroll 2
+                for (int i = 0; i < 64 * D / 512; ++i) {
+                    const int byte = i * 512 + lane * 16;   // within this warp's 64 rows
+                    const int rr = 64 * cw + byte / D;
+                    const int q = (byte % D) / 16;          // 16 codes: d = 16 q .. 16 q + 15
+                    const uint4 x = *reinterpret_cast<const uint4 *>(src + rr * D + q * 16);
+                    const uint4 lo = make_uint4(e4m3x2_to_f16x2(x.x), e4m3x2_to_f16x2(x.x >> 16),
+                                                e4m3x2_to_f16x2(x.y), e4m3x2_to_f16x2(x.y >> 16));
+                    const uint4 hi = make_uint4(e4m3x2_to_f16x2(x.z), e4m3x2_to_f16x2(x.z >> 16),
+                                                e4m3x2_to_f16x2(x.w), e4m3x2_to_f16x2(x.w >> 16));
+                    const int hh = q / 4, c0 = 2 * (q % 4);
+                    uint8_t *row = dst + hh * 16384 + rr * 128;
+                    *reinterpret_cast<uint4 *>(row + ((c0 ^ (rr & 7)) * 16)) = lo;
+                    *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (rr & 7)) * 16)) = hi;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&cfull[cs]);
+                    mbar_arrive(&empty[ls]);
+                }
+            }
+        }
       } else if (warp == kMma) {
         // ---------------------------------------------------------- MMA ----
         if (lane == 0) {
-            constexpr uint32_t idesc_s = umma_idesc_bf16(kBM, kBN, false);
-            constexpr uint32_t idesc_o = umma_idesc_bf16(kBM, D, true);
+            constexpr uint32_t idesc_s = F8 ? umma_idesc_f16(kBM, kBN, false) : umma_idesc_bf16(kBM, kBN, false);
+            constexpr uint32_t idesc_o = F8 ? umma_idesc_f16(kBM, D, true) : umma_idesc_bf16(kBM, D, true);
+            // the slots the MMAs read (FP8: the widened ring) and their barriers
+            uint8_t *mring = smem + (F8 ? S::kConv : S::kRing);
+            uint64_t *mfull = F8 ? cfull : full;
+            uint64_t *mempty = F8 ? cempty : empty;
             // Descriptors are built once; a k-step adds its byte offset >> 4 to
             // the 14-bit start-address field (shared addresses stay < 2^18).
             const uint64_t dq0 = umma_desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t dk0 = umma_desc_sw128(smem_u32(smem + S::kRing), 16, 1024);
-            const uint64_t dv0 = umma_desc_sw128(smem_u32(smem + S::kRing), 16384, 1024);
-            auto wait_full = [&](int c) { return mbar_wait(&full[c % NS], (c / NS) & 1); };
+            const uint64_t dk0 = umma_desc_sw128(smem_u32(mring), 16, 1024);
+            const uint64_t dv0 = umma_desc_sw128(smem_u32(mring), 16384, 1024);
+            auto wait_full = [&](int c) { return mbar_wait(&mfull[c % NC], (c / NC) & 1); };
             auto issue_s = [&](int k, int c) {            // S_k from the K tile of load c
                 const uint64_t dq = dq0 + (uint64_t)((k * S::kTileBytes) >> 4);
-                const uint64_t dk = dk0 + (uint64_t)(((c % NS) * S::kTileBytes) >> 4);
+                const uint64_t dk = dk0 + (uint64_t)(((c % NC) * S::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t o = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
@@ -500,17 +647,17 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                 if (v < 0) break;
                 prefill_item<T>(a, v, it);
                 const int n_kv = it.n_kv;
-                if (!mbar_wait(q_full, local & 1)) break;
+                if (!mbar_wait(F8 ? q_conv : q_full, local & 1)) break;
                 if (n_kv > 0) {
                     if (!wait_full(gl)) break;
                     tc_fence_after();
                     for (int k = 0; k < T; ++k) issue_s(k, gl);
-                    umma_commit(&empty[gl % NS]);                        // K_0 consumed
+                    umma_commit(&mempty[gl % NC]);                       // K_0 consumed
                 }
                 if (n_kv <= 1) umma_commit(q_empty);                     // every S of the item issued
                 for (int j = 0; ok && j < n_kv; ++j) {
                     const int cv = gl + 2 * j + 1;
-                    const uint64_t dv = dv0 + (uint64_t)(((cv % NS) * S::kTileBytes) >> 4);
+                    const uint64_t dv = dv0 + (uint64_t)(((cv % NC) * S::kTileBytes) >> 4);
                     for (int k = 0; k < T; ++k) {
                         if (!mbar_wait(&p_full[k], (gs + j) & 1)) { ok = false; break; }
                         if (k == 0 && !wait_full(cv)) { ok = false; break; }
@@ -520,7 +667,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                         for (int kk = 0; kk < kBN / 16; ++kk)
                             umma_ts(o_tm, tmem + 128 * k + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                                     (j > 0 || kk > 0) ? 1u : 0u);
-                        if (k == T - 1) umma_commit(&empty[cv % NS]);    // V_j consumed
+                        if (k == T - 1) umma_commit(&mempty[cv % NC]);   // V_j consumed
                         if (j + 1 == n_kv) umma_commit(&o_final[k]);     // O_k of the item complete
                         if (j + 1 < n_kv) {
                             if (k == 0) {
@@ -529,7 +676,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                             }
                             issue_s(k, cv + 1);
                             if (k == T - 1) {
-                                umma_commit(&empty[(cv + 1) % NS]);      // K_{j+1} consumed
+                                umma_commit(&mempty[(cv + 1) % NC]);     // K_{j+1} consumed
                                 if (j + 2 == n_kv) umma_commit(q_empty);  // last S of the item
                             }
                         }
@@ -634,7 +781,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                     p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                 }
                 acc[c & 3] = add2(acc[c & 3], p);
-                pk[c] = pack_bf16x2(p.x, p.y);
+                pk[c] = F8 ? pack_f16x2(p.x, p.y) : pack_bf16x2(p.x, p.y);
             }
             const float2 s01 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
             l_run += s01.x + s01.y;
@@ -651,7 +798,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         if (ok) {
             const int64_t tok = (int64_t)it.q0 + qi;
             const int h = it.h0 + k;
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float inv = (l_run > 0.f ? 1.f / l_run : 0.f) * (F8 ? __ldg(a.v_scale + it.kvh) : 1.f);
             // Through the warp's staging buffer, 64 columns at a time: each
             // thread writes its row (16-byte pieces, XOR-swizzled by row so
             // the writes and reads below are free of bank conflicts), then the
@@ -746,12 +893,26 @@ bool make_map(CUtensorMap *m, const void *base, int d, int heads, int64_t rows, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int T>
+// 3-D E4M3 map (d, heads, rows) with a (d, 1, box_rows) box, no swizzle.
+bool make_map_fp8(CUtensorMap *m, const void *base, int d, int heads, int64_t rows, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)heads * d};
+    cuuint32_t box[3] = {(cuuint32_t)d, 1, (cuuint32_t)box_rows};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int T, bool F8>
 cudaError_t launch_t(const PrefillArgs &a, dim3 grid, cudaStream_t stream) {
-    using S = PrefillSmem<D, T>;
+    using S = PrefillSmem<D, T, F8>;
+    static_assert(S::kSlots >= 2 && (!F8 || S::kCSlots >= 2), "ring too small");
     // One CTA per SM (it allocates all 512 TMEM columns).
     const int smem = (S::kTotal + 1024) > 120 * 1024 ? (S::kTotal + 1024) : 120 * 1024;
-    auto kern = prefill_kernel<D, T>;
+    auto kern = prefill_kernel<D, T, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, 128 * (T + 1), smem, stream>>>(a);
@@ -791,10 +952,14 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     PrefillArgs a{};
     const int64_t num_slots = p.num_pages * p.page_size;
     if (!make_map(&a.qmap, p.q, p.head_dim, p.num_q_heads, p.total_q, kBM)) return cudaErrorNotSupported;
+    const bool f8 = p.kv_dtype == PA_KV_FP8_E4M3;
     if (p.page_size == 16) {
-        if (!make_map(&a.kmap, p.k_cache, p.head_dim, p.num_kv_heads, num_slots, 16)) return cudaErrorNotSupported;
-        if (!make_map(&a.vmap, p.v_cache, p.head_dim, p.num_kv_heads, num_slots, 16)) return cudaErrorNotSupported;
+        auto mk = f8 ? make_map_fp8 : make_map;
+        if (!mk(&a.kmap, p.k_cache, p.head_dim, p.num_kv_heads, num_slots, 16)) return cudaErrorNotSupported;
+        if (!mk(&a.vmap, p.v_cache, p.head_dim, p.num_kv_heads, num_slots, 16)) return cudaErrorNotSupported;
     }
+    a.k_scale = p.k_scale;
+    a.v_scale = p.v_scale;
     a.k_cache = static_cast<const uint8_t *>(p.k_cache);
     a.v_cache = static_cast<const uint8_t *>(p.v_cache);
     a.page_table = p.page_table;
@@ -824,9 +989,14 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (each holds all 512 TMEM columns)
     dim3 grid((unsigned)(virt < num_sms() ? virt : num_sms()));
+    if (f8) {
+        if (p.head_dim == 128)
+            return T == 2 ? launch_t<128, 2, true>(a, grid, stream) : launch_t<128, 1, true>(a, grid, stream);
+        return T == 2 ? launch_t<64, 2, true>(a, grid, stream) : launch_t<64, 1, true>(a, grid, stream);
+    }
     if (p.head_dim == 128)
-        return T == 2 ? launch_t<128, 2>(a, grid, stream) : launch_t<128, 1>(a, grid, stream);
-    return T == 2 ? launch_t<64, 2>(a, grid, stream) : launch_t<64, 1>(a, grid, stream);
+        return T == 2 ? launch_t<128, 2, false>(a, grid, stream) : launch_t<128, 1, false>(a, grid, stream);
+    return T == 2 ? launch_t<64, 2, false>(a, grid, stream) : launch_t<64, 1, false>(a, grid, stream);
 }
 
 cudaError_t launch_exp2_selftest(const float *x, float *y, int64_t n, cudaStream_t stream) {

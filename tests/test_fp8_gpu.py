@@ -85,6 +85,16 @@ class FP8Problem:
                         k_scale=self.k_scale, v_scale=self.v_scale)
         return out, lse
 
+    def prefill(self):
+        import paged_kv_flashattention_gb300 as pa
+        Tq, Hq = self.q.shape[0], self.p.num_q_heads
+        lse = torch.empty((Hq, max(Tq, 1)), dtype=torch.float32, device=self.q.device)
+        m = self.meta
+        out = pa.prefill(self.q, self.k_cache, self.v_cache, m.page_table, m.cu_seqlens_q, m.cu_seqlens_k,
+                         m.max_seqlen_q, m.max_seqlen_k, causal=self.p.causal, scale=self.p.scale,
+                         page_size=self.p.page_size, lse=lse, k_scale=self.k_scale, v_scale=self.v_scale)
+        return out, lse
+
     def oracle(self, rows=None):
         p = self.p
         cu_q, cu_k, _, pt = _meta(p)
@@ -136,3 +146,59 @@ def test_decode_fp8_long_contexts(cuda_device):
     p = W.small_problem(503, Lk - 1, np.ones_like(Lk), num_q_heads=32, num_kv_heads=8,
                         head_dim=128, page_size=16)
     _decode_fp8_check(p, cuda_device, 504, what="fp8 long contexts")
+
+
+def _sample_rows(p, frac, seed):
+    """Every request's first and last 3 rows, plus a random fraction; all heads."""
+    rng = np.random.default_rng(seed)
+    cu = np.concatenate([[0], np.cumsum(p.extend_len)])
+    toks = set()
+    for b in range(p.num_seqs):
+        toks.update(range(cu[b], min(cu[b] + 3, cu[b + 1])))
+        toks.update(range(max(cu[b], cu[b + 1] - 3), cu[b + 1]))
+    T = int(cu[-1])
+    toks.update(int(t) for t in rng.choice(T, size=max(1, int(T * frac)), replace=False))
+    toks = np.array(sorted(int(t) for t in toks), np.int64)
+    heads = np.arange(p.num_q_heads, dtype=np.int64)
+    return np.stack(np.meshgrid(toks, heads, indexing="ij"), axis=-1).reshape(-1, 2)
+
+
+def _prefill_fp8_check(p, dev, seed, rows=None, what=""):
+    f = FP8Problem(p, dev, seed)
+    out, lse = f.prefill()
+    torch.cuda.synchronize()
+    if rows is None:
+        ref, ref_lse = f.oracle()
+        return compare(out, ref, what or p.name, lse_gpu=lse[:, :ref.shape[0]].T.contiguous(), lse_ref=ref_lse)
+    ref, ref_lse = f.oracle(rows=rows)
+    t = torch.from_numpy(rows[:, 0]).to(dev)
+    h = torch.from_numpy(rows[:, 1]).to(dev)
+    return compare(out[t, h], ref, what or p.name, lse_gpu=lse[h, t], lse_ref=ref_lse)
+
+
+def test_varlen_prefill_fp8_16x512(cuda_device):
+    """16 requests x 512 prompt tokens over FP8 pools, every output row."""
+    _prefill_fp8_check(W.config(3), cuda_device, 701)
+
+
+@pytest.mark.parametrize("variant", [None, "p1"])
+def test_extend_partial_hit_fp8(cuda_device, variant):
+    p = W.config(4, variant)
+    _prefill_fp8_check(p, cuda_device, 702, rows=_sample_rows(p, 0.2, 7), what=f"{p.name} fp8")
+
+
+PREFILL_EDGE = [
+    ([0, 0, 0, 0, 0], [1, 15, 16, 17, 129]),
+    ([3, 16, 127, 128, 1000], [1, 16, 1, 129, 255]),
+    ([0, 7, 0], [300, 0, 128]),
+]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (32, 4)])
+@pytest.mark.parametrize("page", [1, 16])
+def test_prefill_fp8_edge_matrix(cuda_device, d, hq, hkv, page):
+    for n, (cached, ext) in enumerate(PREFILL_EDGE):
+        p = W.small_problem(2500 + 7 * n + d + hq + page, cached, ext, num_q_heads=hq,
+                            num_kv_heads=hkv, head_dim=d, page_size=page)
+        _prefill_fp8_check(p, cuda_device, 800 + n, what=f"fp8 prefill d{d} g{hq // hkv} P{page} case{n}")
