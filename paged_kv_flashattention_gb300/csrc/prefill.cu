@@ -217,13 +217,23 @@ struct PrefillSmem {
     static constexpr int kRing = T * kTileBytes;           // ring of loaded tiles
     static constexpr int kStageBytes = 4 * T * 4096;      // 32 rows x 64 columns bf16 per warp
     static constexpr int kAvail = 232448 - 1024 - kRing - kStageBytes - 512;
-    // FP8: ring of widened f16 tiles (2..4 slots), loaded-tile ring from the rest
+    // FP8, d = 128 (in place): an E4M3 tile lands in the upper half of its f16
+    // slot (row r's 128 codes where the f16 row r of the upper 64 columns
+    // goes) and is widened where it lies, so the slots serve both rings.
+    // FP8, d = 64: a ring of widened f16 tiles (2..4 slots) and a separate
+    // ring of loaded tiles from the rest.
+    static constexpr bool kInPlace = F8 && D == 128;
+    static constexpr int kFitTiles = kAvail / kTileBytes;
     static constexpr int kCSlotsFit = (kAvail / 2) / kTileBytes;
-    static constexpr int kCSlots = !F8 ? 0 : (kCSlotsFit > 4 ? 4 : (kCSlotsFit < 2 ? 2 : kCSlotsFit));
-    static constexpr int kSlotsFit = (kAvail - kCSlots * kTileBytes) / kLTile;
+    static constexpr int kCSlots = !F8 ? 0
+                                 : kInPlace ? (kFitTiles > 8 ? 8 : kFitTiles)
+                                            : (kCSlotsFit > 4 ? 4 : (kCSlotsFit < 2 ? 2 : kCSlotsFit));
+    static constexpr int kSlotsFit = kInPlace ? kCSlots : (kAvail - kCSlots * kTileBytes) / kLTile;
     static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;
-    static constexpr int kConv = kRing + kSlots * kLTile;
-    static constexpr int kStage = kConv + kCSlots * kTileBytes;
+    static constexpr int kLStride = kInPlace ? kTileBytes : kLTile;       // landing slot stride
+    static constexpr int kLOff = kInPlace ? kTileBytes - kLTile : 0;      // landing offset in a slot
+    static constexpr int kConv = kInPlace ? kRing : kRing + kSlots * kLTile;
+    static constexpr int kStage = kInPlace ? kRing + kCSlots * kTileBytes : kConv + kCSlots * kTileBytes;
     static constexpr int kBars = kStage + kStageBytes;
     static constexpr int kTotal = kBars + 512;
 };
@@ -287,6 +297,8 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     constexpr int kGatherWarps = F8 ? 1 : (NS - 1 < kGatherWarpsMax ? NS - 1 : kGatherWarpsMax);
     constexpr int NC = F8 ? S::kCSlots : NS;  // slots the MMA reads from
     constexpr int kConverters = F8 ? 2 : 0;
+    constexpr bool kInPlace = S::kInPlace;
+    auto land = [&](int slot) { return smem + S::kRing + slot * S::kLStride + S::kLOff; };
     uint64_t *q_full = bars;                 // 1: Q tiles of the item loaded
     uint64_t *q_empty = bars + 1;            // 1: every S MMA of the item done
     uint64_t *full = bars + 2;               // NS: slot loaded
@@ -317,7 +329,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         mbar_init(q_empty, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], paged16 ? 1 : 32);
-            mbar_init(&empty[s], F8 ? kConverters : 1);
+            mbar_init(&empty[s], (F8 && !kInPlace) ? kConverters : 1);
         }
         if (F8) {
             for (int s = 0; s < NC; ++s) {
@@ -362,7 +374,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             // E4M3 rows of D bytes, copied as they are (row-major, no swizzle)
             constexpr int kChunks = D / 16;
             constexpr int kRowsPerIssue = 32 / kChunks;
-            uint8_t *dst = smem + S::kRing + (gl % NS) * S::kLTile;
+            uint8_t *dst = land(gl % NS);
             const uint8_t *src = (c & 1) ? a.v_cache : a.k_cache;
             const int key0 = (c >> 1) * kBN;
             const int q = lane % kChunks, sub = lane / kChunks;
@@ -513,7 +525,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                     if (!(c & 1)) slot0 = page_slot0(it, c >> 1, page);
                     const int slot = gl % NS, round = gl / NS;
                     if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) { ok = false; break; }
-                    uint8_t *dst = smem + S::kRing + slot * S::kLTile;
+                    uint8_t *dst = land(slot);
                     // lanes 0..7 each own one 16-token page of the tile
                     if (lane == 0) mbar_arrive_expect_tx(&full[slot], S::kLTile);
                     __syncwarp();
@@ -573,6 +585,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             if (!__all_sync(0xffffffffu, mbar_wait(q_full, local & 1))) break;
             ++local;
             const float ksc = __ldg(a.k_scale + it.kvh);
+#pragma unroll 4
             for (int i = cw * 32 + lane; i < T * S::kTileBytes / 16; i += 64) {
                 uint4 *pq = reinterpret_cast<uint4 *>(sQ + i * 16);
                 *pq = bf16x8_to_f16x8_scaled(*pq, ksc);
@@ -584,30 +597,45 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             for (int c = 0; c < 2 * it.n_kv; ++c, ++gl) {
                 const int ls = gl % NS, cs = gl % NC;
                 ok = __all_sync(0xffffffffu, mbar_wait(&full[ls], (gl / NS) & 1));
-                if (ok && gl >= NC) ok = __all_sync(0xffffffffu, mbar_wait(&cempty[cs], ((gl / NC) - 1) & 1));
+                // (in place the slot was free before it was loaded)
+                if (ok && !kInPlace && gl >= NC)
+                    ok = __all_sync(0xffffffffu, mbar_wait(&cempty[cs], ((gl / NC) - 1) & 1));
                 if (!ok) break;
-                const uint8_t *src = smem + S::kRing + ls * S::kLTile;
+                const uint8_t *src = land(ls);
                 uint8_t *dst = smem + S::kConv + cs * S::kTileBytes;
-#pragma unroll 2
-                for (int i = 0; i < 64 * D / 512; ++i) {
-                    const int byte = i * 512 + lane * 16;   // within this warp's 64 rows
-                    const int rr = 64 * cw + byte / D;
-                    const int q = (byte % D) / 16;          // 16 codes: d = 16 q .. 16 q + 15
-                    const uint4 x = *reinterpret_cast<const uint4 *>(src + rr * D + q * 16);
-                    const uint4 lo = make_uint4(e4m3x2_to_f16x2(x.x), e4m3x2_to_f16x2(x.x >> 16),
-                                                e4m3x2_to_f16x2(x.y), e4m3x2_to_f16x2(x.y >> 16));
-                    const uint4 hi = make_uint4(e4m3x2_to_f16x2(x.z), e4m3x2_to_f16x2(x.z >> 16),
-                                                e4m3x2_to_f16x2(x.w), e4m3x2_to_f16x2(x.w >> 16));
-                    const int hh = q / 4, c0 = 2 * (q % 4);
-                    uint8_t *row = dst + hh * 16384 + rr * 128;
-                    *reinterpret_cast<uint4 *>(row + ((c0 ^ (rr & 7)) * 16)) = lo;
-                    *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (rr & 7)) * 16)) = hi;
+                // groups of 4 x 512 bytes: all reads of a group, then (in
+                // place, after the warp has read them) the writes, which
+                // overwrite only rows of the same group
+                constexpr int kGroup = 4;
+#pragma unroll 1
+                for (int i0 = 0; i0 < 64 * D / 512; i0 += kGroup) {
+                    uint4 x[kGroup];
+#pragma unroll
+                    for (int u = 0; u < kGroup; ++u) {
+                        const int byte = (i0 + u) * 512 + lane * 16;   // within this warp's 64 rows
+                        x[u] = *reinterpret_cast<const uint4 *>(src + (64 * cw + byte / D) * D + (byte % D));
+                    }
+                    if (kInPlace) __syncwarp();
+#pragma unroll
+                    for (int u = 0; u < kGroup; ++u) {
+                        const int byte = (i0 + u) * 512 + lane * 16;
+                        const int rr = 64 * cw + byte / D;
+                        const int q = (byte % D) / 16;      // 16 codes: d = 16 q .. 16 q + 15
+                        const uint4 lo = make_uint4(e4m3x2_to_f16x2(x[u].x), e4m3x2_to_f16x2(x[u].x >> 16),
+                                                    e4m3x2_to_f16x2(x[u].y), e4m3x2_to_f16x2(x[u].y >> 16));
+                        const uint4 hi = make_uint4(e4m3x2_to_f16x2(x[u].z), e4m3x2_to_f16x2(x[u].z >> 16),
+                                                    e4m3x2_to_f16x2(x[u].w), e4m3x2_to_f16x2(x[u].w >> 16));
+                        const int hh = q / 4, c0 = 2 * (q % 4);
+                        uint8_t *row = dst + hh * 16384 + rr * 128;
+                        *reinterpret_cast<uint4 *>(row + ((c0 ^ (rr & 7)) * 16)) = lo;
+                        *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (rr & 7)) * 16)) = hi;
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&cfull[cs]);
-                    mbar_arrive(&empty[ls]);
+                    if (!kInPlace) mbar_arrive(&empty[ls]);
                 }
             }
         }
@@ -619,7 +647,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             // the slots the MMAs read (FP8: the widened ring) and their barriers
             uint8_t *mring = smem + (F8 ? S::kConv : S::kRing);
             uint64_t *mfull = F8 ? cfull : full;
-            uint64_t *mempty = F8 ? cempty : empty;
+            uint64_t *mempty = (F8 && !kInPlace) ? cempty : empty;   // in place: frees the loaded slot too
             // Descriptors are built once; a k-step adds its byte offset >> 4 to
             // the 14-bit start-address field (shared addresses stay < 2^18).
             const uint64_t dq0 = umma_desc_sw128(smem_u32(sQ), 16, 1024);
