@@ -66,6 +66,12 @@ def _bind(lib):
     lib.oracle_e4m3_encode.restype = ctypes.c_uint8
     lib.oracle_store_kv_fp8.argtypes = [P, P, P, i64, P, P, i64, i32, i32, P, P]
     lib.oracle_store_kv_fp8.restype = ctypes.c_int
+    lib.oracle_rope_table.argtypes = [P, P, i32, i32, dbl]
+    lib.oracle_rope_table.restype = ctypes.c_int
+    lib.oracle_rope_rotate.argtypes = [P, P, i64, i32, i32, i32, ctypes.c_int, P, P, i32, P]
+    lib.oracle_rope_rotate.restype = ctypes.c_int
+    lib.oracle_round_bf16.argtypes = [P, i64, P]
+    lib.oracle_round_bf16.restype = ctypes.c_int
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     return lib
@@ -165,6 +171,38 @@ def store_kv_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, *, lib=
     assert k.size == T * Hkv * d and v.size == T * Hkv * d and ks.size == Hkv and vs.size == Hkv
     _check(_load(lib).oracle_store_kv_fp8(_ptr(k), _ptr(v), _ptr(sm), T, _ptr(k_cache), _ptr(v_cache),
                                           slots, Hkv, d, _ptr(ks), _ptr(vs)), "oracle_store_kv_fp8")
+
+
+def rope_table(max_pos: int, rot_dim: int, base: float, *, lib=None):
+    """(cos, sin) float64 [max_pos, rot_dim/2] of angle p * base^(-2i/rot_dim)."""
+    h = int(rot_dim) // 2
+    c = np.zeros((int(max_pos), h), np.float64)
+    s_ = np.zeros((int(max_pos), h), np.float64)
+    _check(_load(lib).oracle_rope_table(_ptr(c), _ptr(s_), int(max_pos), int(rot_dim), float(base)),
+           "oracle_rope_table")
+    return c, s_
+
+
+def rope_rotate(x, positions, cos, sin, *, rot_dim: int, interleaved: bool = False, lib=None):
+    """Rotary embedding of bf16 bits x [T, H, d] at positions [T]; exact
+    float64 result [T, H, d] (elements past rot_dim unchanged)."""
+    x = _c(x, np.uint16)
+    pos = _c(positions, np.int32)
+    c = _c(cos, np.float64)
+    s_ = _c(sin, np.float64)
+    T, H, d = x.shape
+    out = np.zeros((T, H, d), np.float64)
+    _check(_load(lib).oracle_rope_rotate(_ptr(x), _ptr(pos), T, H, d, int(rot_dim), int(bool(interleaved)),
+                                         _ptr(c), _ptr(s_), c.shape[0], _ptr(out)), "oracle_rope_rotate")
+    return out
+
+
+def round_bf16(x, *, lib=None) -> np.ndarray:
+    """Nearest bf16 bits (ties to even) of float64 values, in one rounding."""
+    xf = _c(x, np.float64)
+    out = np.zeros(xf.shape, np.uint16)
+    _check(_load(lib).oracle_round_bf16(_ptr(xf), xf.size, _ptr(out)), "oracle_round_bf16")
+    return out
 
 
 def page_table_from_token_table(token_table, table_idx, max_seqlen_k: int, page_size: int,

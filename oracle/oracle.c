@@ -51,6 +51,22 @@
  *    rounded to the nearest E4M3 value, ties to the even code, magnitudes of
  *    448 and above saturating to 448; attention then reads code * scale.
  *
+ *  - Rotary position embedding before the store (oracle_rope_table,
+ *    oracle_rope_rotate, oracle_round_bf16).  The first page's layer graph
+ *    has "RoPE + KV cache store" as one step after the QKV projection
+ *    (section 2), RoPE variants / scaling / offset as a dispatch axis
+ *    (section 19) and "scaled RoPE" / "long offset" as edge cases (section
+ *    24); the mini-sglang page applies the rotary to q and k with the batch's
+ *    positions right before the attention backend ("the layer does not know
+ *    the backend").  The pages do not define the rotation, so the reading is
+ *    the standard rotary embedding: for a rotated width r (<= d) and pair
+ *    index i < r/2 the angle is pos * base^(-2i/r); pairs are (i, i + r/2)
+ *    ("rotate half") or (2i, 2i+1) ("interleaved"); a pair (a, b) becomes
+ *    (a cos - b sin, b cos + a sin); elements r .. d-1 are unchanged.  The
+ *    rotation can also be driven by a given cos/sin table (scaled variants).
+ *    Outputs are exact in double; oracle_round_bf16 rounds a double to the
+ *    nearest bf16 (ties to even) in one step.
+ *
  * All arithmetic on floating point is IEEE double.  bf16 inputs are widened
  * exactly (a bf16 value is the top 16 bits of an IEEE single).
  */
@@ -392,4 +408,77 @@ int oracle_attention_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_
     kv_pools kv = {k_cache, v_cache, 1, k_scale, v_scale};
     return attention_all(q, &kv, page_table, pt_stride, cu_q, cu_k, num_seqs, Hq, Hkv, d, P,
                          num_pages, causal, scale, rows, nrows, out, lse);
+}
+
+/* ---------------------------------------------------------------- RoPE */
+
+/* cos / sin tables [max_pos, r/2]: angle(p, i) = p * base^(-2i/r). */
+int oracle_rope_table(double *cos_t, double *sin_t, int32_t max_pos, int32_t r, double base)
+{
+    if (max_pos < 0 || r <= 0 || r % 2 || !(base > 0.0)) return ORACLE_EINVAL;
+    int32_t h = r / 2;
+    for (int32_t p = 0; p < max_pos; ++p) {
+        for (int32_t i = 0; i < h; ++i) {
+            double ang = (double)p * pow(base, -2.0 * (double)i / (double)r);
+            cos_t[(int64_t)p * h + i] = cos(ang);
+            sin_t[(int64_t)p * h + i] = sin(ang);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Rotate x: [T, H, d] bf16 bits, token t at position positions[t], with the
+ * tables [max_pos, r/2]; out: [T, H, d] double (exact products and sums). */
+int oracle_rope_rotate(const uint16_t *x, const int32_t *positions, int64_t T, int32_t H, int32_t d,
+                       int32_t r, int interleaved, const double *cos_t, const double *sin_t,
+                       int32_t max_pos, double *out)
+{
+    if (T < 0 || H <= 0 || d <= 0 || r <= 0 || r > d || r % 2) return ORACLE_EINVAL;
+    int32_t h = r / 2;
+    for (int64_t t = 0; t < T; ++t) {
+        int32_t p = positions[t];
+        if (p < 0 || p >= max_pos) return ORACLE_ERANGE;
+        for (int32_t hd = 0; hd < H; ++hd) {
+            const uint16_t *xr = x + (t * H + hd) * (int64_t)d;
+            double *o = out + (t * H + hd) * (int64_t)d;
+            for (int32_t c = 0; c < d; ++c) o[c] = widen_bf16(xr[c]);
+            for (int32_t i = 0; i < h; ++i) {
+                int32_t ia = interleaved ? 2 * i : i;
+                int32_t ib = interleaved ? 2 * i + 1 : i + h;
+                double a = widen_bf16(xr[ia]), b = widen_bf16(xr[ib]);
+                double cs = cos_t[(int64_t)p * h + i], sn = sin_t[(int64_t)p * h + i];
+                o[ia] = a * cs - b * sn;
+                o[ib] = b * cs + a * sn;
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Nearest bf16 (8 significant bits, ties to even) of each double, as bits. */
+int oracle_round_bf16(const double *x, int64_t n, uint16_t *out)
+{
+    for (int64_t k = 0; k < n; ++k) {
+        double v = x[k];
+        float f;
+        if (isnan(v)) {
+            f = NAN;
+        } else if (v == 0.0 || isinf(v)) {
+            f = (float)v;
+        } else {
+            int e;
+            frexp(v, &e);                          /* |v| in [2^(e-1), 2^e) */
+            int q = e - 8;                         /* quantum of 8 significant bits */
+            if (q < -133) q = -133;                /* bf16 subnormal quantum */
+            double scaled = ldexp(v, -q);
+            double rr = nearbyint(scaled);         /* ties to even */
+            double rv = ldexp(rr, q);
+            f = (float)rv;                         /* exact: 8 significant bits */
+            if (fabs(rv) > 3.3895313892515355e38) f = v > 0 ? INFINITY : -INFINITY;
+        }
+        uint32_t u;
+        memcpy(&u, &f, sizeof u);
+        out[k] = (uint16_t)(u >> 16);
+    }
+    return ORACLE_OK;
 }

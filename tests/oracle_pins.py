@@ -26,6 +26,12 @@ the store, and by the identity "attention over FP8 pools = attention over
 bf16 pools holding the same values" (every E4M3 value times a power-of-two
 scale is a bf16 value, so both paths see identical numbers).
 
+The rotary embedding is pinned by numpy's cos / sin of p * base^(-2i/r) for
+the table, by complex multiplication (pairs as complex numbers times e^(i
+angle)) for the rotation, by its defining property (q(m) . k(n) depends only
+on m - n) and by position 0 being the identity; the bf16 rounding by the
+input generator's float32 -> bf16 rounding on float32 values and exact ties.
+
 The hand-worked golden cases live in tests/golden/.
 """
 from __future__ import annotations
@@ -537,7 +543,73 @@ def check_attention_fp8_exact_values(lib=None):
     assert np.array_equal(o8, ob) and np.array_equal(l8, lb), "FP8 attention differs from bf16 on equal values"
 
 
-ALL_CHECKS = [check_e4m3_codec, check_store_fp8, check_attention_fp8_exact_values, check_store, check_metadata, check_golden, check_brute_force, check_equal_scores,
+def check_rope_table(lib=None):
+    """cos / sin table against numpy on the same angles."""
+    for r, base in ((128, 10000.0), (64, 500000.0), (16, 10.0)):
+        c, s_ = oracle.rope_table(300, r, base, lib=lib)
+        p = np.arange(300, dtype=np.float64)[:, None]
+        i = np.arange(r // 2, dtype=np.float64)[None, :]
+        ang = p * np.power(base, -2.0 * i / r)
+        assert np.allclose(c, np.cos(ang), rtol=0, atol=1e-13), "RoPE cos table"
+        assert np.allclose(s_, np.sin(ang), rtol=0, atol=1e-13), "RoPE sin table"
+
+
+def _rope_case(seed, T=6, H=3, d=32):
+    rng = np.random.default_rng(seed)
+    x = W.normal_bf16(rng, (T, H, d))
+    pos = rng.integers(0, 200, size=T).astype(np.int32)
+    return x, pos
+
+
+def check_rope_complex(lib=None):
+    """Each rotated pair equals (a + i b) * e^(i angle) by numpy complex
+    multiplication, for both pairings and a partial rotated width."""
+    x, pos = _rope_case(41)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64)
+    for r, inter in ((32, False), (32, True), (16, False)):
+        c, s_ = oracle.rope_table(200, r, 10000.0, lib=lib)
+        got = oracle.rope_rotate(x, pos, c, s_, rot_dim=r, interleaved=inter, lib=lib)
+        h = r // 2
+        ia = np.arange(h) * 2 if inter else np.arange(h)
+        ib = ia + 1 if inter else ia + h
+        z = (xf[:, :, ia] + 1j * xf[:, :, ib]) * np.exp(1j * np.arctan2(s_[pos], c[pos]))[:, None, :]
+        assert np.allclose(got[:, :, ia], z.real, rtol=0, atol=1e-12), "RoPE real part"
+        assert np.allclose(got[:, :, ib], z.imag, rtol=0, atol=1e-12), "RoPE imaginary part"
+        rest = np.setdiff1d(np.arange(xf.shape[2]), np.concatenate([ia, ib]))
+        assert np.array_equal(got[:, :, rest], xf[:, :, rest]), "elements past the rotated width change"
+
+
+def check_rope_relative_position(lib=None):
+    """q(m) . k(n) depends only on m - n; position 0 is the identity."""
+    rng = np.random.default_rng(43)
+    q = W.normal_bf16(rng, (1, 1, 64))
+    k = W.normal_bf16(rng, (1, 1, 64))
+    c, s_ = oracle.rope_table(400, 64, 10000.0, lib=lib)
+    dots = []
+    for m, n in ((10, 3), (107, 100), (397, 390)):
+        qm = oracle.rope_rotate(q, [m], c, s_, rot_dim=64, lib=lib)
+        kn = oracle.rope_rotate(k, [n], c, s_, rot_dim=64, lib=lib)
+        dots.append(float(np.sum(qm * kn)))
+    assert max(dots) - min(dots) < 1e-10, f"RoPE dot products depend on absolute position: {dots}"
+    q0 = oracle.rope_rotate(q, [0], c, s_, rot_dim=64, lib=lib)
+    assert np.array_equal(q0, W.bf16_bits_to_f32(q).astype(np.float64))
+
+
+def check_round_bf16(lib=None):
+    """One-step bf16 rounding equals float32 -> bf16 rounding on float32
+    inputs, including exact ties, signs and subnormals."""
+    rng = np.random.default_rng(47)
+    f = (rng.standard_normal(5000) * 10.0 ** rng.uniform(-30, 30, 5000)).astype(np.float32)
+    ties = (W.bf16_bits_to_f32(W.f32_to_bf16_bits(f)).astype(np.float64) +
+            np.ldexp(1.0, np.frexp(f.astype(np.float64))[1] - 9)).astype(np.float32)
+    special = np.array([0.0, -0.0, 1.00390625, 1.01171875, 2.0 ** -130, 2.0 ** -133, 3 * 2.0 ** -134], np.float32)
+    x = np.concatenate([f, ties, special])
+    got = oracle.round_bf16(x.astype(np.float64), lib=lib)
+    assert np.array_equal(got, W.f32_to_bf16_bits(x)), "bf16 rounding differs from float32 -> bf16"
+
+
+ALL_CHECKS = [check_rope_table, check_rope_complex, check_rope_relative_position, check_round_bf16,
+              check_e4m3_codec, check_store_fp8, check_attention_fp8_exact_values, check_store, check_metadata, check_golden, check_brute_force, check_equal_scores,
               check_single_key, check_dominant_key, check_empty, check_sdpa_library,
               check_decode_is_last_prefill_row, check_extend_is_prefill_tail,
               check_gqa_equals_repeated_mha, check_page_size_equivalence,

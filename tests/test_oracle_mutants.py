@@ -34,6 +34,11 @@ MUTANTS = [
     ("fp8_scale_head_0", "* (double)scale[kvh];", "* (double)scale[0];", 1),
     ("fp8_store_multiplies", "widen_bf16_f32(k[src]) / k_scale[h]", "widen_bf16_f32(k[src]) * k_scale[h]", 1),
     ("fp8_k_read_with_v_scale", "kv_value(kv->k, kv->fp8, kv->k_scale,", "kv_value(kv->k, kv->fp8, kv->v_scale,", 1),
+    ("rope_sign", "o[ia] = a * cs - b * sn;", "o[ia] = a * cs + b * sn;", 1),
+    ("rope_pairs_adjacent", "int32_t ib = interleaved ? 2 * i + 1 : i + h;", "int32_t ib = interleaved ? 2 * i + 1 : i + 1;", 1),
+    ("rope_frequency_halved", "pow(base, -2.0 * (double)i / (double)r)", "pow(base, -1.0 * (double)i / (double)r)", 1),
+    ("rope_cos_sin_swapped", "cos_t[(int64_t)p * h + i] = cos(ang);", "cos_t[(int64_t)p * h + i] = sin(ang);", 1),
+    ("bf16_ties_away", "double rr = nearbyint(scaled);", "double rr = round(scaled);", 1),
 ]
 
 
