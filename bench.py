@@ -445,6 +445,8 @@ MICRO_CASES = {
     "extend_partial_hit_p16": (4, None, "prefill"),
     "extend_partial_hit_p1": (4, "p1", "prefill"),
     "store_16x512": (3, None, "store"),
+    # fused RoPE + store of the same 8192 tokens (q rotated in place)
+    "rope_store_16x512": (3, None, "rope"),
     # a smaller mixed-batch decode: 64 sequences, contexts log-uniform
     # [512, 32768], ~2 GB pool (inputs still far larger than L2)
     "decode_64seq_logu": (None, None, "decode"),
@@ -509,6 +511,14 @@ def run_micro(args):
         E = p.extend_len.astype(np.int64)
         work = 4 * D * Hq * int(np.sum(E * off + E * (E + 1) // 2))
         unit = "TFLOP/s"
+    elif kernel == "rope":
+        table = pa.rope_cos_sin_table(int(p.device_len.max()) + 1, D, 10000.0).to(dev)
+        pos = torch.from_numpy(np.concatenate([np.arange(c, c + e) for c, e in zip(p.cached_len, p.extend_len)])
+                               .astype(np.int32)).to(dev)
+        fn = lambda: pa.rope_store_kv(q, kn, vn, pos, table, sm, kc, vc, q_out=q)
+        # q read + written, k and v read, two pool rows written
+        work = 2 * q.numel() * 2 + 2 * 2 * kn.numel() * 2
+        unit = "GB/s"
     else:
         fn = lambda: pa.store_kv(kn, vn, sm, kc, vc)
         work = 2 * 2 * kn.numel() * 2

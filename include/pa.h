@@ -4,6 +4,8 @@
  * Exact attention over a paged KV cache, as a serving engine runs it:
  *   pa_store_kv          write the new tokens' K/V rows into the paged pool
  *   pa_store_kv_fp8      the same into an FP8 (E4M3) pool with per-head scales
+ *   pa_rope_store_kv     rotary embedding of q and k fused with the K/V store
+ *   pa_rope_cos_sin_table  the rotary cos/sin table (host)
  *   pa_build_seqlens     per-request boundaries from the three lengths (host)
  *   pa_build_page_table  per-request page table from the token-granular table
  *   pa_prefill           varlen causal prefill / extend attention
@@ -75,6 +77,7 @@ typedef enum {
 #define PA_DEVERR_PAGE_RANGE 1   /* a page id / slot outside the pool was skipped */
 #define PA_DEVERR_SEQLENS 2      /* cu_seqlens / cache_seqlens inconsistent */
 #define PA_DEVERR_TIMEOUT 4      /* a bounded wait in a kernel gave up */
+#define PA_DEVERR_POSITION 8     /* a RoPE position outside the cos/sin table */
 
 int pa_abi_version(void);
 const char *pa_status_string(int status);
@@ -84,6 +87,12 @@ const char *pa_last_error(void);
 /* Read and clear the device error word of the current device.  Synchronises
  * `stream` first.  *bits receives an OR of PA_DEVERR_* (0 = clean). */
 pa_status pa_device_error(int32_t *bits, void *stream);
+
+/* Element type of the K/V pools read by pa_prefill and pa_decode.  FP8 pools hold E4M3
+ * codes written by pa_store_kv_fp8 with per-KV-head scales.  On FP8 pools the
+ * contractions run in f16 with fp32 accumulation: q * k_scale is rounded to
+ * f16 (|q * k_scale| must stay below 65504), P is rounded to f16. */
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
 
 /*
  * pa_store_kv - KV-cache store ([T] s.1-2, "RoPE + KV cache store"):
@@ -121,6 +130,58 @@ pa_status pa_store_kv_fp8(const void *k, const void *v, const int32_t *slot_mapp
                           const float *v_scale, void *stream);
 
 /*
+ * pa_rope_cos_sin_table - rotary table on the HOST ([T] s.2 "RoPE + KV cache
+ * store"; the pages do not define the rotation, this library's reading is
+ * the standard rotary embedding): for p < max_pos and i < rot_dim / 2,
+ *   cos_sin[p * rot_dim + i]               = cos(p * base^(-2i / rot_dim))
+ *   cos_sin[p * rot_dim + rot_dim / 2 + i] = sin(p * base^(-2i / rot_dim))
+ * computed in double and rounded to float.  cos_sin: host fp32
+ * [max_pos, rot_dim], owned by the caller (copy it to the device once).
+ * Scaled variants are other tables of the same shape.
+ */
+pa_status pa_rope_cos_sin_table(float *cos_sin, int32_t max_pos, int32_t rot_dim, double base);
+
+/*
+ * pa_rope_store_kv - rotary embedding of q and k fused with the K/V store
+ * ([T] s.2: "RoPE + KV cache store" as one step after the QKV projection;
+ * [M]: the rotary is applied with the batch positions just before the
+ * attention backend stores K/V).  For token t at position pos = positions[t]
+ * and every pair (i, i + rot_dim/2) (or (2i, 2i+1) when interleaved) of the
+ * first rot_dim elements of each q and k head, with c, s the table's entries
+ * for pair i:  (a, b) -> (a*c - b*s, b*c + a*s), each product and the sum
+ * rounded in fp32, the result rounded to bf16; elements past rot_dim are
+ * copied.  Rotated q goes to q_out (which may be q itself); rotated k and v
+ * are stored to row slot_mapping[t] exactly as pa_store_kv (bf16 pools) or
+ * pa_store_kv_fp8 (FP8 pools, from the bf16 rotated k) store them; a
+ * negative slot stores nothing (q is still rotated).  A position outside
+ * [0, max_pos) writes nothing for that token and raises PA_DEVERR_POSITION.
+ */
+typedef struct {
+    const void *q;               /* bf16 [num_tokens, Hq, head_dim] */
+    void *q_out;                 /* bf16 [num_tokens, Hq, head_dim]; may equal q */
+    const void *k;               /* bf16 [num_tokens, Hkv, head_dim] (not modified) */
+    const void *v;               /* bf16 [num_tokens, Hkv, head_dim] */
+    const int32_t *positions;    /* device int32 [num_tokens] */
+    const float *cos_sin;        /* device fp32 [max_pos, rot_dim] (pa_rope_cos_sin_table layout) */
+    int32_t max_pos;
+    int32_t rot_dim;             /* multiple of 16, <= head_dim */
+    int32_t interleaved;         /* 0: pairs (i, i + rot_dim/2); 1: pairs (2i, 2i+1) */
+    const int32_t *slot_mapping; /* device int32 [num_tokens], as for pa_store_kv */
+    int64_t num_tokens;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;            /* multiple of 16 */
+    void *k_cache;               /* [num_slots, Hkv, head_dim] bf16, or E4M3 codes */
+    void *v_cache;
+    int64_t num_slots;
+    int32_t kv_dtype;            /* pa_kv_dtype of the pools */
+    const float *k_scale;        /* FP8 pools: device fp32 [Hkv] */
+    const float *v_scale;
+} pa_rope_store_params;
+
+pa_status pa_rope_store_kv(const pa_rope_store_params *p, void *stream);
+
+/*
  * pa_build_seqlens - host-side metadata ([M], "from ledger to tensors").
  * All pointers are HOST memory.  From cached_len[b] and extend_len[b]:
  *   cu_seqlens_q  [num_seqs+1] = exclusive prefix sum of extend_len
@@ -150,11 +211,6 @@ pa_status pa_build_page_table(const int32_t *token_table, int64_t token_table_st
                               int32_t max_seqlen_k, int32_t page_size, int32_t *page_table,
                               int32_t page_table_stride, void *stream);
 
-/* Element type of the K/V pools read by pa_prefill and pa_decode.  FP8 pools hold E4M3
- * codes written by pa_store_kv_fp8 with per-KV-head scales.  On FP8 pools the
- * contractions run in f16 with fp32 accumulation: q * k_scale is rounded to
- * f16 (|q * k_scale| must stay below 65504), P is rounded to f16. */
-typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
 
 /*
  * pa_prefill - varlen prefill / extend attention ([T] s.10-15, [M]).

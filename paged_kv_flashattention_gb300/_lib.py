@@ -48,6 +48,16 @@ class DecodeParams(ctypes.Structure):
     ]
 
 
+class RopeStoreParams(ctypes.Structure):
+    _fields_ = [
+        ("q", c_p), ("q_out", c_p), ("k", c_p), ("v", c_p), ("positions", c_p), ("cos_sin", c_p),
+        ("max_pos", c_i32), ("rot_dim", c_i32), ("interleaved", c_i32), ("slot_mapping", c_p),
+        ("num_tokens", c_i64), ("num_q_heads", c_i32), ("num_kv_heads", c_i32), ("head_dim", c_i32),
+        ("k_cache", c_p), ("v_cache", c_p), ("num_slots", c_i64), ("kv_dtype", c_i32),
+        ("k_scale", c_p), ("v_scale", c_p),
+    ]
+
+
 # name -> (restype, argtypes)
 SIGNATURES = {
     "pa_abi_version": (ctypes.c_int, []),
@@ -56,6 +66,8 @@ SIGNATURES = {
     "pa_device_error": (ctypes.c_int, [ctypes.POINTER(c_i32), c_p]),
     "pa_store_kv": (ctypes.c_int, [c_p, c_p, c_p, c_i64, c_p, c_p, c_i64, c_i32, c_i32, c_p]),
     "pa_store_kv_fp8": (ctypes.c_int, [c_p, c_p, c_p, c_i64, c_p, c_p, c_i64, c_i32, c_i32, c_p, c_p, c_p]),
+    "pa_rope_cos_sin_table": (ctypes.c_int, [c_p, c_i32, c_i32, ctypes.c_double]),
+    "pa_rope_store_kv": (ctypes.c_int, [ctypes.POINTER(RopeStoreParams), c_p]),
     "pa_build_seqlens": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p]),
     "pa_build_page_table": (ctypes.c_int, [c_p, c_i64, c_p, c_i32, c_i32, c_i32, c_p, c_i32, c_p]),
     "pa_prefill": (ctypes.c_int, [ctypes.POINTER(PrefillParams), c_p]),

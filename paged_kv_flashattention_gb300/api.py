@@ -137,6 +137,58 @@ def store_kv_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                                num_slots, Hkv, d, _ptr(k_scale), _ptr(v_scale), _stream(k_cache)), lib)
 
 
+def rope_cos_sin_table(max_pos: int, rot_dim: int, base: float = 10000.0) -> torch.Tensor:
+    """Host fp32 [max_pos, rot_dim] rotary table (cos of the rot_dim/2 angles
+    p * base^(-2i/rot_dim), then their sin), computed by the C library."""
+    t = torch.empty((int(max_pos), int(rot_dim)), dtype=torch.float32)
+    lib = _lib.load()
+    _check(lib.pa_rope_cos_sin_table(t.data_ptr() if t.numel() else None, int(max_pos), int(rot_dim),
+                                     float(base)), lib)
+    return t
+
+
+def rope_store_kv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, positions: torch.Tensor,
+                  cos_sin: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                  v_cache: torch.Tensor, *, q_out: torch.Tensor | None = None,
+                  interleaved: bool = False, k_scale: torch.Tensor | None = None,
+                  v_scale: torch.Tensor | None = None) -> torch.Tensor:
+    """Rotary embedding of q and k at ``positions`` fused with the K/V store.
+    q bf16 [T, Hq, d]; k, v bf16 [T, Hkv, d]; cos_sin fp32 [max_pos, rot_dim]
+    on the device; pools bf16 or E4M3 (with ``k_scale``/``v_scale``).  Returns
+    the rotated q (``q_out``, which may be ``q``)."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, dev)
+    _need(positions, "positions", torch.int32, dev)
+    _need(slot_mapping, "slot_mapping", torch.int32, dev)
+    _need(cos_sin, "cos_sin", torch.float32, dev)
+    kvd = _kv_dtype(k_cache, v_cache)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, k_cache.dtype, dev)
+    T, Hq, d = q.shape
+    Hkv = k_cache.shape[-2]
+    if k_cache.shape[-1] != d or k.numel() != T * Hkv * d or v.numel() != T * Hkv * d:
+        raise ValueError("k/v/pool shapes do not match q")
+    if positions.numel() != T or slot_mapping.numel() != T:
+        raise ValueError("positions and slot_mapping must hold one entry per token")
+    if kvd == PA_KV_FP8_E4M3:
+        _need_scales(k_scale, v_scale, Hkv, dev)
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    _need(q_out, "q_out", torch.bfloat16, dev)
+    p = _lib.RopeStoreParams(
+        q=_ptr(q), q_out=_ptr(q_out), k=_ptr(k), v=_ptr(v), positions=_ptr(positions),
+        cos_sin=_ptr(cos_sin), max_pos=cos_sin.shape[0], rot_dim=cos_sin.shape[1],
+        interleaved=int(bool(interleaved)), slot_mapping=_ptr(slot_mapping), num_tokens=T,
+        num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, k_cache=_ptr(k_cache), v_cache=_ptr(v_cache),
+        num_slots=k_cache.numel() // (Hkv * d), kv_dtype=kvd,
+        k_scale=_ptr(k_scale) if kvd == PA_KV_FP8_E4M3 else None,
+        v_scale=_ptr(v_scale) if kvd == PA_KV_FP8_E4M3 else None)
+    lib = _lib.load()
+    _check(lib.pa_rope_store_kv(ctypes.byref(p), _stream(q)), lib)
+    return q_out
+
+
 def build_seqlens(cached_len, extend_len):
     """Host metadata: (cu_seqlens_q, cu_seqlens_k, cache_seqlens, max_q, max_k)
     as int32 numpy arrays (the C entry point does the arithmetic)."""

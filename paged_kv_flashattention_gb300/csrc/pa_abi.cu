@@ -2,6 +2,7 @@
 // host, error reporting, and dispatch to the kernels.  Nothing here touches
 // device memory except pa_device_error (which reads the error words) and no
 // call allocates memory.
+#include <cmath>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -137,6 +138,48 @@ pa_status pa_store_kv_fp8(const void *k, const void *v, const int32_t *slot_mapp
                                         num_kv_heads, head_dim, k_scale, v_scale,
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "store_kv_fp8 launch");
+}
+
+pa_status pa_rope_cos_sin_table(float *cos_sin, int32_t max_pos, int32_t rot_dim, double base) {
+    g_last_error[0] = 0;
+    if (max_pos < 0 || rot_dim <= 0 || rot_dim % 2 != 0) return fail(PA_ERR_INVALID, "max_pos >= 0 and an even rot_dim > 0 are required");
+    if (!(base > 0.0) || base != base) return fail(PA_ERR_INVALID, "base must be positive");
+    if (max_pos == 0) return PA_OK;
+    if (!cos_sin) return fail(PA_ERR_INVALID, "NULL pointer");
+    const int h = rot_dim / 2;
+    for (int32_t p = 0; p < max_pos; ++p) {
+        for (int i = 0; i < h; ++i) {
+            const double ang = (double)p * std::pow(base, -2.0 * (double)i / (double)rot_dim);
+            cos_sin[(int64_t)p * rot_dim + i] = (float)std::cos(ang);
+            cos_sin[(int64_t)p * rot_dim + h + i] = (float)std::sin(ang);
+        }
+    }
+    return PA_OK;
+}
+
+pa_status pa_rope_store_kv(const pa_rope_store_params *p, void *stream) {
+    g_last_error[0] = 0;
+    if (p == nullptr) return fail(PA_ERR_INVALID, "params is NULL");
+    if (p->num_tokens < 0 || p->num_slots < 0 || p->max_pos < 0) return fail(PA_ERR_INVALID, "negative sizes");
+    if (p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0)
+        return fail(PA_ERR_INVALID, "head counts and head_dim must be positive");
+    if (p->head_dim % 16 != 0) return fail(PA_ERR_UNSUPPORTED, "head_dim %d is not a multiple of 16", p->head_dim);
+    if (p->rot_dim <= 0 || p->rot_dim % 16 != 0 || p->rot_dim > p->head_dim)
+        return fail(PA_ERR_UNSUPPORTED, "rot_dim %d must be a positive multiple of 16 <= head_dim", p->rot_dim);
+    if (p->interleaved != 0 && p->interleaved != 1) return fail(PA_ERR_INVALID, "interleaved must be 0 or 1");
+    if (p->kv_dtype != PA_KV_BF16 && p->kv_dtype != PA_KV_FP8_E4M3)
+        return fail(PA_ERR_INVALID, "kv_dtype %d is neither PA_KV_BF16 nor PA_KV_FP8_E4M3", p->kv_dtype);
+    if (p->num_tokens == 0) return PA_OK;
+    if (!p->q || !p->q_out || !p->k || !p->v || !p->positions || !p->cos_sin || !p->slot_mapping ||
+        !p->k_cache || !p->v_cache)
+        return fail(PA_ERR_INVALID, "NULL pointer");
+    if (p->kv_dtype == PA_KV_FP8_E4M3 && (!p->k_scale || !p->v_scale))
+        return fail(PA_ERR_INVALID, "FP8 pools need k_scale and v_scale");
+    if (!aligned16(p->q) || !aligned16(p->q_out) || !aligned16(p->k) || !aligned16(p->v) ||
+        !aligned16(p->k_cache) || !aligned16(p->v_cache) || !aligned16(p->cos_sin))
+        return fail(PA_ERR_INVALID, "q, q_out, k, v, the pools and the table must be 16-byte aligned");
+    cudaError_t e = launch_rope_store(*p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "rope_store launch");
 }
 
 pa_status pa_build_seqlens(const int32_t *cached_len, const int32_t *extend_len, int32_t num_seqs,

@@ -14,9 +14,23 @@
 // hardware's round-to-nearest-even with saturation to +-448).  One warp per
 // token as above; a lane converts 8 elements (16 bytes in, 8 bytes out).
 //
+// Fused RoPE + store: the layer graph's "RoPE + KV cache store" step (same
+// page, section 2) in one pass, as the mini-sglang page applies the rotary to
+// q and k with the batch positions right before the backend stores K/V.  The
+// rotation is the standard rotary embedding driven by a cos/sin table row
+// per position (so scaled variants only change the table): a pair (a, b) of
+// width-r elements becomes (a cos - b sin, b cos + a sin) in fp32 with
+// separately rounded products and sum, rounded to bf16; pairs are (i, i +
+// r/2) or (2i, 2i + 1).  The rotated q goes to q_out, the rotated k (bf16)
+// and v are stored exactly as pa_store_kv / pa_store_kv_fp8 would store
+// them.  One warp per token; a lane handles 16 rotated elements (two 16-byte
+// pieces) or 8 copied ones at a time.
+//
 // Page table: "code-series sgl-project mini-sglang 07", "from ledger to
 // tensors": the global table is token granular; a request's row is sliced
 // with step page_size up to max_seqlen_k and floor-divided by page_size.
+#include <cuda_bf16.h>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -104,6 +118,150 @@ __global__ void __launch_bounds__(256) store_kv_fp8_kernel(const uint4 *__restri
     }
 }
 
+struct RopeStoreArgs {
+    const uint4 *q;
+    uint4 *q_out;
+    const uint4 *k;
+    const uint4 *v;
+    const int32_t *positions;
+    const float *cos_sin;         // [max_pos, rot_dim]: cos of the rot_dim/2 angles, then sin
+    int32_t max_pos;
+    int32_t rot_dim;
+    int32_t interleaved;
+    const int32_t *slot_mapping;
+    int64_t num_tokens;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    uint8_t *k_cache;
+    uint8_t *v_cache;
+    int64_t num_slots;
+    const float *k_scale;
+    const float *v_scale;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t bf16_pair(float lo, float hi) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
+// Rotate 8 pairs held as a[8] (first elements) and b[8] (second elements).
+__device__ __forceinline__ void rotate8(float (&a)[8], float (&b)[8], const float *c, const float *s) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float cj = c[j], sj = s[j];
+        const float na = __fsub_rn(__fmul_rn(a[j], cj), __fmul_rn(b[j], sj));
+        const float nb = __fadd_rn(__fmul_rn(b[j], cj), __fmul_rn(a[j], sj));
+        a[j] = na;
+        b[j] = nb;
+    }
+}
+
+__device__ __forceinline__ void unpack8(uint4 x, float (&f)[8]) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = bf16_lo(w[i]);
+        f[2 * i + 1] = bf16_hi(w[i]);
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    return make_uint4(bf16_pair(f[0], f[1]), bf16_pair(f[2], f[3]), bf16_pair(f[4], f[5]), bf16_pair(f[6], f[7]));
+}
+
+// Store 8 bf16 values (as bits) into a pool row piece: bf16 bits, or E4M3 codes.
+template <bool F8>
+__device__ __forceinline__ void store8(uint8_t *pool, int64_t elem, uint4 bits, float scale) {
+    if constexpr (F8) *reinterpret_cast<uint2 *>(pool + elem) = quantize8(bits, scale);
+    else *reinterpret_cast<uint4 *>(pool + elem * 2) = bits;
+}
+
+template <bool F8>
+__global__ void __launch_bounds__(256) rope_store_kernel(const RopeStoreArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int D = a.head_dim, r = a.rot_dim, h = r / 2;
+    const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+    const int rot_units = r / 16, copy_units = (D - r) / 8;
+    const int units = rot_units + copy_units;            // per head
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.num_tokens;
+         t += warps_total) {
+        const int pos = a.positions[t];
+        if (pos < 0 || pos >= a.max_pos) {                 // nothing of this token is written
+            if (lane == 0) raise_error(PA_DEVERR_POSITION);
+            continue;
+        }
+        const int64_t slot = a.slot_mapping[t];
+        const bool store = slot >= 0 && slot < a.num_slots;
+        if (slot >= a.num_slots && lane == 0) raise_error(PA_DEVERR_PAGE_RANGE);
+        const float *cs = a.cos_sin + (int64_t)pos * r;
+        // q heads then k heads, `units` pieces each
+        for (int f = lane; f < (Hq + Hkv) * units; f += 32) {
+            const int hd = f / units, u = f % units;
+            const bool is_q = hd < Hq;
+            const int kvh = hd - Hq;
+            const uint4 *src = is_q ? a.q + ((t * Hq + hd) * D) / 8 : a.k + ((t * Hkv + kvh) * D) / 8;
+            uint4 out0, out1;
+            int e0, e1 = -1;                                // element offsets within the head
+            if (u < rot_units) {
+                float x0[8], x1[8], ra[8], rb[8];
+                if (a.interleaved) {                        // elements 16u .. 16u + 15, pairs (2j, 2j+1)
+                    e0 = 16 * u;
+                    e1 = e0 + 8;
+                    unpack8(src[e0 / 8], x0);
+                    unpack8(src[e1 / 8], x1);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        ra[j] = x0[2 * j]; rb[j] = x0[2 * j + 1];
+                        ra[4 + j] = x1[2 * j]; rb[4 + j] = x1[2 * j + 1];
+                    }
+                } else {                                    // elements 8u .. 8u + 7 and h + 8u ..
+                    e0 = 8 * u;
+                    e1 = h + 8 * u;
+                    unpack8(src[e0 / 8], ra);
+                    unpack8(src[e1 / 8], rb);
+                }
+                rotate8(ra, rb, cs + 8 * u, cs + h + 8 * u);
+                if (a.interleaved) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        x0[2 * j] = ra[j]; x0[2 * j + 1] = rb[j];
+                        x1[2 * j] = ra[4 + j]; x1[2 * j + 1] = rb[4 + j];
+                    }
+                    out0 = pack8(x0);
+                    out1 = pack8(x1);
+                } else {
+                    out0 = pack8(ra);
+                    out1 = pack8(rb);
+                }
+            } else {                                        // past the rotated width: unchanged
+                e0 = r + 8 * (u - rot_units);
+                out0 = src[e0 / 8];
+            }
+            if (is_q) {
+                uint4 *dst = a.q_out + ((t * Hq + hd) * D) / 8;
+                dst[e0 / 8] = out0;
+                if (e1 >= 0) dst[e1 / 8] = out1;
+            } else if (store) {
+                const int64_t row = (slot * Hkv + kvh) * (int64_t)D;
+                const float sc = F8 ? __ldg(a.k_scale + kvh) : 1.f;
+                store8<F8>(a.k_cache, row + e0, out0, sc);
+                if (e1 >= 0) store8<F8>(a.k_cache, row + e1, out1, sc);
+            }
+        }
+        if (store) {                                        // v: copied or quantised
+            for (int f = lane; f < Hkv * (D / 8); f += 32) {
+                const int kvh = f / (D / 8), c = f % (D / 8);
+                const uint4 x = __ldg(a.v + ((t * Hkv + kvh) * D) / 8 + c);
+                store8<F8>(a.v_cache, (slot * Hkv + kvh) * (int64_t)D + 8 * c, x, F8 ? __ldg(a.v_scale + kvh) : 1.f);
+            }
+        }
+    }
+}
+
 __global__ void build_page_table_kernel(const int32_t *__restrict__ token_table, int64_t tt_stride,
                                         const int32_t *__restrict__ table_idx, int32_t num_seqs,
                                         int32_t ncols, int32_t page_size, int32_t *page_table,
@@ -137,6 +295,39 @@ cudaError_t launch_store_kv_fp8(const void *k, const void *v, const int32_t *slo
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
         static_cast<uint2 *>(k_cache), static_cast<uint2 *>(v_cache), num_slots,
         num_kv_heads * head_dim / 8, head_dim, k_scale, v_scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope_store(const pa_rope_store_params &p, cudaStream_t stream) {
+    if (p.num_tokens == 0) return cudaSuccess;
+    RopeStoreArgs a{};
+    a.q = static_cast<const uint4 *>(p.q);
+    a.q_out = static_cast<uint4 *>(p.q_out);
+    a.k = static_cast<const uint4 *>(p.k);
+    a.v = static_cast<const uint4 *>(p.v);
+    a.positions = p.positions;
+    a.cos_sin = p.cos_sin;
+    a.max_pos = p.max_pos;
+    a.rot_dim = p.rot_dim;
+    a.interleaved = p.interleaved;
+    a.slot_mapping = p.slot_mapping;
+    a.num_tokens = p.num_tokens;
+    a.num_q_heads = p.num_q_heads;
+    a.num_kv_heads = p.num_kv_heads;
+    a.head_dim = p.head_dim;
+    a.k_cache = static_cast<uint8_t *>(p.k_cache);
+    a.v_cache = static_cast<uint8_t *>(p.v_cache);
+    a.num_slots = p.num_slots;
+    a.k_scale = p.k_scale;
+    a.v_scale = p.v_scale;
+    const int warps_per_block = 8;
+    int64_t blocks = (p.num_tokens + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = (int64_t)num_sms() * 16;
+    if (blocks > cap) blocks = cap;
+    if (p.kv_dtype == PA_KV_FP8_E4M3)
+        rope_store_kernel<true><<<(unsigned)blocks, warps_per_block * 32, 0, stream>>>(a);
+    else
+        rope_store_kernel<false><<<(unsigned)blocks, warps_per_block * 32, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

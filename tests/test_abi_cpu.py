@@ -151,3 +151,27 @@ def test_decode_workspace_size_host_only(lib):
     p.kv_chunk = 4096
     small = lib.pa_decode_workspace_size(ctypes.byref(p))
     assert 0 < small < n and small >= 64 * 32 * 2 * (64 + 1) * 4
+
+
+def test_rope_table_host(lib):
+    """The host rotary table equals the oracle's fp64 table rounded to fp32
+    (within half an fp32 step of values <= 1)."""
+    import paged_kv_flashattention_gb300 as pa
+    for r, base in ((128, 10000.0), (64, 500000.0)):
+        t = pa.rope_cos_sin_table(2048, r, base).numpy().astype(np.float64)
+        c, s = oracle.rope_table(2048, r, base)
+        assert np.abs(t[:, :r // 2] - c).max() <= 2.0 ** -25 and np.abs(t[:, r // 2:] - s).max() <= 2.0 ** -25
+    with pytest.raises(pa.PagedAttentionError):
+        pa.rope_cos_sin_table(16, 7, 10000.0)
+
+
+def test_rope_store_rejects_before_launch(lib):
+    from paged_kv_flashattention_gb300 import _lib
+    base = dict(q=0x1000, q_out=0x1000, k=0x2000, v=0x3000, positions=0x4000, cos_sin=0x5000, max_pos=64,
+                rot_dim=128, interleaved=0, slot_mapping=0x6000, num_tokens=4, num_q_heads=8,
+                num_kv_heads=2, head_dim=128, k_cache=0x7000, v_cache=0x8000, num_slots=64, kv_dtype=0)
+    for kw, status in ((dict(rot_dim=72), UNSUPPORTED), (dict(rot_dim=256), UNSUPPORTED),
+                       (dict(interleaved=2), INVALID), (dict(kv_dtype=1), INVALID),
+                       (dict(q=0x1008), INVALID), (dict(head_dim=72), UNSUPPORTED)):
+        p = _lib.RopeStoreParams(**{**base, **kw})
+        assert lib.pa_rope_store_kv(ctypes.byref(p), None) == status, kw
