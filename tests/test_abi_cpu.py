@@ -175,3 +175,12 @@ def test_rope_store_rejects_before_launch(lib):
                        (dict(q=0x1008), INVALID), (dict(head_dim=72), UNSUPPORTED)):
         p = _lib.RopeStoreParams(**{**base, **kw})
         assert lib.pa_rope_store_kv(ctypes.byref(p), None) == status, kw
+
+
+def test_graph_bucket_selection():
+    from paged_kv_flashattention_gb300.graphs import bucket_for
+    assert bucket_for((1, 2, 4, 8, 16), 5) == 8
+    assert bucket_for((16, 1, 4), 1) == 1
+    assert bucket_for((1, 2, 4), 4) == 4
+    with pytest.raises(ValueError):
+        bucket_for((1, 2, 4), 5)
