@@ -55,10 +55,10 @@ def _bind(lib):
     lib.oracle_seqlens.argtypes = [P, P, i32, P, P, P, P, P]
     lib.oracle_seqlens.restype = ctypes.c_int
     lib.oracle_attention.argtypes = [P, P, P, P, i64, P, P, i32, i32, i32, i32, i32,
-                                     i64, ctypes.c_int, dbl, P, i64, P, P]
+                                     i64, ctypes.c_int, i32, dbl, P, i64, P, P]
     lib.oracle_attention.restype = ctypes.c_int
     lib.oracle_attention_fp8.argtypes = [P, P, P, P, P, P, i64, P, P, i32, i32, i32, i32, i32,
-                                         i64, ctypes.c_int, dbl, P, i64, P, P]
+                                         i64, ctypes.c_int, i32, dbl, P, i64, P, P]
     lib.oracle_attention_fp8.restype = ctypes.c_int
     lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_value.restype = dbl
@@ -235,7 +235,8 @@ def seqlens(cached_len, extend_len, *, lib=None):
 
 def attention(q, k_cache, v_cache, page_table, cu_seqlens_q, cu_seqlens_k, *,
               num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
-              causal: bool, scale: float, rows=None, k_scale=None, v_scale=None, lib=None):
+              causal: bool, scale: float, rows=None, k_scale=None, v_scale=None, window_left: int = -1,
+              lib=None):
     """fp64 attention over paged K/V.
 
     q: uint16 [Tq, Hq, d]; caches: uint16 [num_pages*page_size, Hkv, d] (any
@@ -273,19 +274,19 @@ def attention(q, k_cache, v_cache, page_table, cu_seqlens_q, cu_seqlens_k, *,
         assert ks.size == Hkv and vs.size == Hkv
         _check(_load(lib).oracle_attention_fp8(
             _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(pt), pt.shape[1], _ptr(cq), _ptr(ck),
-            B, Hq, Hkv, d, P, num_pages, int(bool(causal)), float(scale), rp, nr,
+            B, Hq, Hkv, d, P, num_pages, int(bool(causal)), int(window_left), float(scale), rp, nr,
             _ptr(out), _ptr(lse)), "oracle_attention_fp8")
         return out, lse
     _check(_load(lib).oracle_attention(
         _ptr(q), _ptr(kc), _ptr(vc), _ptr(pt), pt.shape[1], _ptr(cq), _ptr(ck), B,
-        Hq, Hkv, d, P, num_pages, int(bool(causal)), float(scale), rp, nr,
+        Hq, Hkv, d, P, num_pages, int(bool(causal)), int(window_left), float(scale), rp, nr,
         _ptr(out), _ptr(lse)), "oracle_attention")
     return out, lse
 
 
 def decode(q, k_cache, v_cache, page_table, cache_seqlens, *, num_q_heads: int,
            num_kv_heads: int, head_dim: int, page_size: int, scale: float, rows=None,
-           k_scale=None, v_scale=None, lib=None):
+           k_scale=None, v_scale=None, window_left: int = -1, lib=None):
     """Decode attention: one query token per sequence attending to all
     cache_seqlens[b] keys (the new token already stored).  q: [B, Hq, d]."""
     cs = np.asarray(cache_seqlens, dtype=np.int64)
@@ -295,8 +296,8 @@ def decode(q, k_cache, v_cache, page_table, cache_seqlens, *, num_q_heads: int,
     cu_k[1:] = np.cumsum(cs)
     return attention(q, k_cache, v_cache, page_table, cu_q, cu_k.astype(np.int32),
                      num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
-                     page_size=page_size, causal=False, scale=scale, rows=rows, k_scale=k_scale,
-                     v_scale=v_scale, lib=lib)
+                     page_size=page_size, causal=True, scale=scale, rows=rows, k_scale=k_scale,
+                     v_scale=v_scale, window_left=window_left, lib=lib)
 
 
 from . import online  # noqa: E402,F401  (re-export)

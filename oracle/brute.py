@@ -36,7 +36,7 @@ def gather_request(cache_rows, page_row, length: int, page_size: int, kv_head: i
 
 
 def attention(q, k_cache, v_cache, page_table, cu_q, cu_k, *, num_q_heads, num_kv_heads,
-              head_dim, page_size, causal, scale):
+              head_dim, page_size, causal, scale, window_left=-1):
     """q: nested [Tq][Hq][d] bf16 bits (or a numpy array); caches indexable as
     cache[slot][kv_head] -> d bits.  Returns nested lists O[Tq][Hq][d]."""
     group = num_q_heads // num_kv_heads
@@ -53,7 +53,8 @@ def attention(q, k_cache, v_cache, page_table, cu_q, cu_k, *, num_q_heads, num_k
                     qv = [_bf16(x) for x in q[q0 + i][h]]
                     # absolute position of this query among the request's keys
                     pos = (Lk - Lq) + i
-                    keys = [j for j in range(Lk) if (not causal) or j <= pos]
+                    keys = [j for j in range(Lk) if ((not causal) or j <= pos)
+                            and (window_left < 0 or pos - j <= window_left)]
                     if not keys:
                         continue            # empty: output stays 0
                     e = [math.exp(scale * math.fsum(a * c for a, c in zip(qv, K[j]))) for j in keys]

@@ -29,7 +29,12 @@
  *    Lk - Lq + i and sees keys 0 .. Lk - Lq + i (a cached prefix of Lk - Lq
  *    tokens followed by the Lq extend tokens).  A query row with no visible
  *    key returns O = 0 and lse = -inf (the "KV: empty" edge case of section
- *    24 of the first page).
+ *    24 of the first page).  A sliding window (the first page lists
+ *    "causal, sliding window, custom sparse" masks as a dispatch axis,
+ *    section 19) bounds the visible keys from below: with window_left >= 0
+ *    a query at absolute position p sees only keys j >= p - window_left
+ *    (so window_left + 1 keys at most when causal); window_left < 0 means
+ *    no window.
  *
  *  - oracle_page_table_from_token_table: the metadata step of the
  *    mini-sglang page, "from ledger to tensors": the global table is token
@@ -274,7 +279,7 @@ static int attention_row(const uint16_t *q, const kv_pools *kv,
                          const int32_t *page_table, int64_t pt_stride,
                          const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
                          int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
-                         int causal, double scale, int64_t t, int32_t h,
+                         int causal, int32_t window_left, double scale, int64_t t, int32_t h,
                          double *o, double *lse, double *s_row)
 {
     /* request b owning query token t */
@@ -293,15 +298,20 @@ static int attention_row(const uint16_t *q, const kv_pools *kv,
         if (lim < n_vis) n_vis = lim;
         if (n_vis < 0) n_vis = 0;
     }
+    int64_t j_lo = 0;                      /* sliding window: keys >= off + i - window_left */
+    if (window_left >= 0) {
+        j_lo = off + i - window_left;
+        if (j_lo < 0) j_lo = 0;
+    }
     int32_t g = Hq / Hkv;
     int32_t kvh = h / g;
     const uint16_t *qrow = q + (t * Hq + h) * (int64_t)d;
 
     for (int c = 0; c < d; ++c) o[c] = 0.0;
-    if (n_vis <= 0) { *lse = -INFINITY; return ORACLE_OK; }
+    if (n_vis <= j_lo) { *lse = -INFINITY; return ORACLE_OK; }
 
     /* pass 0: materialise the score row S[j] = scale * q . K_j */
-    for (int64_t j = 0; j < n_vis; ++j) {
+    for (int64_t j = j_lo; j < n_vis; ++j) {
         int64_t page = page_table[b * pt_stride + j / P];
         if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
         int64_t row = page * P + j % P;
@@ -313,10 +323,10 @@ static int attention_row(const uint16_t *q, const kv_pools *kv,
     }
     /* pass 1: row maximum */
     double m = -INFINITY;
-    for (int64_t j = 0; j < n_vis; ++j) if (s_row[j] > m) m = s_row[j];
+    for (int64_t j = j_lo; j < n_vis; ++j) if (s_row[j] > m) m = s_row[j];
     /* pass 2: exponentials, their sum, and P.V */
     double l = 0.0;
-    for (int64_t j = 0; j < n_vis; ++j) {
+    for (int64_t j = j_lo; j < n_vis; ++j) {
         double p = exp(s_row[j] - m);
         l += p;
         int64_t page = page_table[b * pt_stride + j / P];
@@ -338,8 +348,8 @@ static int attention_all(const uint16_t *q, const kv_pools *kv,
                          const int32_t *page_table, int64_t pt_stride,
                          const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
                          int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
-                         int causal, double scale, const int64_t *rows, int64_t nrows,
-                         double *out, double *lse)
+                         int causal, int32_t window_left, double scale, const int64_t *rows,
+                         int64_t nrows, double *out, double *lse)
 {
     if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || P <= 0 || Hq % Hkv) return ORACLE_EINVAL;
     int64_t Tq = num_seqs > 0 ? cu_q[num_seqs] : 0;
@@ -370,7 +380,7 @@ static int attention_all(const uint16_t *q, const kv_pools *kv,
                     continue;
                 }
                 int st = attention_row(q, kv, page_table, pt_stride, cu_q, cu_k,
-                                       num_seqs, Hq, Hkv, d, P, num_pages, causal, scale, t, h,
+                                       num_seqs, Hq, Hkv, d, P, num_pages, causal, window_left, scale, t, h,
                                        out + r * (int64_t)d, lse + r, s_row);
                 if (st != ORACLE_OK) {
 #pragma omp atomic write
@@ -387,12 +397,12 @@ int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t 
                      const int32_t *page_table, int64_t pt_stride,
                      const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
                      int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
-                     int causal, double scale, const int64_t *rows, int64_t nrows,
-                     double *out, double *lse)
+                     int causal, int32_t window_left, double scale, const int64_t *rows,
+                     int64_t nrows, double *out, double *lse)
 {
     kv_pools kv = {k_cache, v_cache, 0, NULL, NULL};
     return attention_all(q, &kv, page_table, pt_stride, cu_q, cu_k, num_seqs, Hq, Hkv, d, P,
-                         num_pages, causal, scale, rows, nrows, out, lse);
+                         num_pages, causal, window_left, scale, rows, nrows, out, lse);
 }
 
 /* The same over E4M3 pools (codes [num_pages*P, Hkv, d]) with per-KV-head
@@ -402,12 +412,12 @@ int oracle_attention_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_
                          const int32_t *page_table, int64_t pt_stride,
                          const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
                          int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
-                         int causal, double scale, const int64_t *rows, int64_t nrows,
-                         double *out, double *lse)
+                         int causal, int32_t window_left, double scale, const int64_t *rows,
+                         int64_t nrows, double *out, double *lse)
 {
     kv_pools kv = {k_cache, v_cache, 1, k_scale, v_scale};
     return attention_all(q, &kv, page_table, pt_stride, cu_q, cu_k, num_seqs, Hq, Hkv, d, P,
-                         num_pages, causal, scale, rows, nrows, out, lse);
+                         num_pages, causal, window_left, scale, rows, nrows, out, lse);
 }
 
 /* ---------------------------------------------------------------- RoPE */

@@ -105,13 +105,14 @@ def edge_problems(head_dim=8, page_size=4):
     return out
 
 
-def _brute(p: W.Problem, kc, vc, lib=None):
+def _brute(p: W.Problem, kc, vc, lib=None, window_left=-1, causal=None):
     cu_q, cu_k, _, pt = _meta(p, lib)
     kcr = kc.reshape(-1, p.num_kv_heads, p.head_dim)
     vcr = vc.reshape(-1, p.num_kv_heads, p.head_dim)
     return np.array(brute.attention(p.q, kcr, vcr, pt, cu_q, cu_k, num_q_heads=p.num_q_heads,
                                     num_kv_heads=p.num_kv_heads, head_dim=p.head_dim,
-                                    page_size=p.page_size, causal=p.causal, scale=p.scale),
+                                    page_size=p.page_size, causal=p.causal if causal is None else causal,
+                                    scale=p.scale, window_left=window_left),
                     dtype=np.float64).reshape(-1, p.num_q_heads, p.head_dim)
 
 
@@ -608,7 +609,72 @@ def check_round_bf16(lib=None):
     assert np.array_equal(got, W.f32_to_bf16_bits(x)), "bf16 rounding differs from float32 -> bf16"
 
 
-ALL_CHECKS = [check_rope_table, check_rope_complex, check_rope_relative_position, check_round_bf16,
+def _oracle_window(p, kc, vc, window_left, causal=None, lib=None, rows=None):
+    cu_q, cu_k, _, pt = _meta(p, lib)
+    return oracle.attention(p.q, kc, vc, pt, cu_q, cu_k, num_q_heads=p.num_q_heads,
+                            num_kv_heads=p.num_kv_heads, head_dim=p.head_dim, page_size=p.page_size,
+                            causal=p.causal if causal is None else causal, scale=p.scale,
+                            window_left=window_left, rows=rows, lib=lib)
+
+
+def check_window_brute_force(lib=None):
+    """Sliding windows of several widths, causal and not, against the brute
+    force (which filters keys by p - j <= window_left)."""
+    for P in (1, 4):
+        for p in edge_problems(page_size=P):
+            kc, vc = stored_caches(p, lib)
+            for w in (0, 1, 3, 7):
+                for causal in (True, False):
+                    o, _ = _oracle_window(p, kc, vc, w, causal, lib)
+                    ob = _brute(p, kc, vc, lib, window_left=w, causal=causal)
+                    _assert_close(o, ob, 1e-12, f"window {w} causal {causal} P={P}")
+
+
+def check_window_closed_forms(lib=None):
+    """A window of 0 under the causal mask leaves each row its own key (O = V
+    of its position, lse = its score); a window covering every key changes
+    nothing."""
+    p = W.small_problem(57, [5, 0, 9], [3, 4, 2], num_q_heads=4, num_kv_heads=2, head_dim=8, page_size=4)
+    kc, vc = stored_caches(p, lib)
+    o0, l0 = _oracle_window(p, kc, vc, 0, True, lib)
+    cu_q, cu_k, _, pt = _meta(p, lib)
+    g = p.num_q_heads // p.num_kv_heads
+    for b in range(p.num_seqs):
+        Lq, Lk = int(p.extend_len[b]), int(p.device_len[b])
+        for i in range(Lq):
+            t, pos = int(cu_q[b]) + i, Lk - Lq + i
+            slot = int(pt[b, pos // p.page_size]) * p.page_size + pos % p.page_size
+            for h in range(p.num_q_heads):
+                kv = h // g
+                vrow = W.bf16_bits_to_f32(vc.reshape(-1, p.num_kv_heads, p.head_dim)[slot, kv]).astype(np.float64)
+                krow = W.bf16_bits_to_f32(kc.reshape(-1, p.num_kv_heads, p.head_dim)[slot, kv]).astype(np.float64)
+                qrow = W.bf16_bits_to_f32(p.q[t, h]).astype(np.float64)
+                assert np.array_equal(o0[t, h], vrow), "window 0 must return the own value"
+                assert abs(l0[t, h] - p.scale * math.fsum(qrow * krow)) < 1e-12
+    on, ln = _oracle_window(p, kc, vc, -1, True, lib)
+    ow, lw = _oracle_window(p, kc, vc, int(p.device_len.max()), True, lib)
+    assert np.array_equal(on, ow) and np.array_equal(ln, lw), "a window over every key must change nothing"
+
+
+def check_window_is_truncated_cache(lib=None):
+    """Decode with window w over a token-granular table equals decode without
+    a window over the same table row with its first L - 1 - w entries cut."""
+    p = W.small_problem(59, [30, 12, 50], [1, 1, 1], num_q_heads=4, num_kv_heads=2, head_dim=8, page_size=1)
+    kc, vc = stored_caches(p, lib)
+    _, _, cs, pt = _meta(p, lib)
+    w = 9
+    o, l = oracle.decode(p.q, kc, vc, pt, cs, num_q_heads=4, num_kv_heads=2, head_dim=8, page_size=1,
+                         scale=p.scale, window_left=w, lib=lib)
+    for b in range(p.num_seqs):
+        L = int(cs[b])
+        s0 = max(0, L - 1 - w)
+        ob, lb = oracle.decode(p.q[b:b + 1], kc, vc, pt[b:b + 1, s0:L], [L - s0], num_q_heads=4,
+                               num_kv_heads=2, head_dim=8, page_size=1, scale=p.scale, lib=lib)
+        assert np.array_equal(o[b], ob[0]) and np.array_equal(l[b], lb[0]), "window != truncated cache"
+
+
+ALL_CHECKS = [check_window_brute_force, check_window_closed_forms, check_window_is_truncated_cache,
+              check_rope_table, check_rope_complex, check_rope_relative_position, check_round_bf16,
               check_e4m3_codec, check_store_fp8, check_attention_fp8_exact_values, check_store, check_metadata, check_golden, check_brute_force, check_equal_scores,
               check_single_key, check_dominant_key, check_empty, check_sdpa_library,
               check_decode_is_last_prefill_row, check_extend_is_prefill_tail,

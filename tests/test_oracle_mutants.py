@@ -23,7 +23,7 @@ MUTANTS = [
     ("lse_missing_max", "*lse = m + log(l);", "*lse = log(l);", 1),
     ("values_from_k_cache", "o[c] += p * kv_value(kv->v,", "o[c] += p * kv_value(kv->k,", 1),
     ("exp_sign_flipped", "double p = exp(s_row[j] - m);", "double p = exp(m - s_row[j]);", 1),
-    ("last_key_dropped", "for (int64_t j = 0; j < n_vis; ++j) {\n        double p", "for (int64_t j = 0; j + 1 < n_vis; ++j) {\n        double p", 1),
+    ("last_key_dropped", "for (int64_t j = j_lo; j < n_vis; ++j) {\n        double p", "for (int64_t j = j_lo; j + 1 < n_vis; ++j) {\n        double p", 1),
     ("cu_k_prefix_wrong", "cu_k[b + 1] = (int32_t)sk;", "cu_k[b + 1] = (int32_t)sq;", 1),
     ("page_table_no_divide", "int64_t q = slot / page_size;", "int64_t q = slot;", 1),
     ("store_swaps_k_v", "memcpy(k_cache + slot * row_elems, k + t * row_elems", "memcpy(k_cache + slot * row_elems, v + t * row_elems", 1),
@@ -39,6 +39,9 @@ MUTANTS = [
     ("rope_frequency_halved", "pow(base, -2.0 * (double)i / (double)r)", "pow(base, -1.0 * (double)i / (double)r)", 1),
     ("rope_cos_sin_swapped", "cos_t[(int64_t)p * h + i] = cos(ang);", "cos_t[(int64_t)p * h + i] = sin(ang);", 1),
     ("bf16_ties_away", "double rr = nearbyint(scaled);", "double rr = round(scaled);", 1),
+    ("window_off_by_one", "j_lo = off + i - window_left;", "j_lo = off + i - window_left + 1;", 1),
+    ("window_from_query_index", "j_lo = off + i - window_left;", "j_lo = i - window_left;", 1),
+    ("window_ignored", "if (window_left >= 0) {\n        j_lo", "if (0) {\n        j_lo", 1),
 ]
 
 
