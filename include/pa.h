@@ -252,6 +252,8 @@ typedef struct {
     int32_t kv_dtype;            /* pa_kv_dtype of k_cache / v_cache (0 = bf16) */
     const float *k_scale;        /* PA_KV_FP8_E4M3: device fp32 [Hkv]; else unused */
     const float *v_scale;
+    int32_t sliding_window;      /* 0 = none; W > 0: a query at position p sees only keys
+                                    j >= p - (W - 1) ([T] s.19 "sliding window" mask) */
 } pa_prefill_params;
 
 pa_status pa_prefill(const pa_prefill_params *p, void *stream);
@@ -293,6 +295,8 @@ typedef struct {
     int32_t kv_dtype;            /* pa_kv_dtype of k_cache / v_cache (0 = bf16) */
     const float *k_scale;        /* PA_KV_FP8_E4M3: device fp32 [Hkv]; else unused */
     const float *v_scale;        /* (element = value(code) * scale[kv head]) */
+    int32_t sliding_window;      /* 0 = none; W > 0: only the last W keys of each sequence
+                                    are read and attended to */
 } pa_decode_params;
 
 /* Bytes of workspace pa_decode needs for these parameters (always > 0: a

@@ -32,7 +32,7 @@ class PrefillParams(ctypes.Structure):
         ("num_q_heads", c_i32), ("num_kv_heads", c_i32), ("head_dim", c_i32),
         ("page_size", c_i32), ("num_pages", c_i64), ("causal", c_i32), ("scale", c_f32),
         ("out", c_p), ("lse", c_p), ("lse_stride", c_i64),
-        ("kv_dtype", c_i32), ("k_scale", c_p), ("v_scale", c_p),
+        ("kv_dtype", c_i32), ("k_scale", c_p), ("v_scale", c_p), ("sliding_window", c_i32),
     ]
 
 
@@ -45,6 +45,7 @@ class DecodeParams(ctypes.Structure):
         ("page_size", c_i32), ("num_pages", c_i64), ("scale", c_f32),
         ("out", c_p), ("lse", c_p), ("workspace", c_p), ("workspace_bytes", c_size),
         ("kv_chunk", c_i32), ("kv_dtype", c_i32), ("k_scale", c_p), ("v_scale", c_p),
+        ("sliding_window", c_i32),
     ]
 
 

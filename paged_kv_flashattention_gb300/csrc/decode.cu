@@ -87,6 +87,7 @@ struct DecodeArgs {
     float *lse_part;
     const float *k_scale;         // FP8 pools: per-KV-head scales
     const float *v_scale;
+    int32_t window;               // sliding window W (0 = none): the last W keys
     int32_t *ws_header;           // [0] = T
     int32_t *ws_prefix;           // [B+1] exclusive prefix of the sequence lengths
 };
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
             raise_error(PA_DEVERR_SEQLENS);
             L = L < 0 ? 0 : a.max_seqlen_k;
         }
+        if (a.window > 0 && L > a.window) L = a.window;     // only the last W keys are read
         prefix[b + 1] = L;
     }
     if (threadIdx.x == 0) {
@@ -246,6 +248,10 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
         int b, hg, k0, k1, split;
         while (walk.next(b, hg, k0, k1, split)) {
             const int32_t *pt = a.page_table + (int64_t)b * a.pt_stride;
+            // with a sliding window the row's tokens start s0 keys in
+            int Lb = a.cache_seqlens[b];
+            Lb = Lb < 0 ? 0 : (Lb > a.max_seqlen_k ? a.max_seqlen_k : Lb);
+            const int s0 = Lb - (prefix[b + 1] - prefix[b]);
             for (int t0 = k0; t0 < k1; t0 += kStageTok, ++stage_ctr) {
                 const int slot = stage_ctr % kStages;
                 const int round = stage_ctr / kStages;
@@ -255,7 +261,7 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
                 __syncwarp();
                 const int tok = lane & 15;
                 if (tok < n) {
-                    const int j = t0 + tok;
+                    const int j = s0 + t0 + tok;
                     int64_t page = pt[j / a.page_size];
                     if (page < 0 || page >= a.num_pages) {   // never read outside the pool
                         raise_error(PA_DEVERR_PAGE_RANGE);
@@ -637,6 +643,7 @@ cudaError_t launch_decode(const pa_decode_params &p, const DecodePlan &plan, cud
     a.lse = p.lse;
     a.k_scale = p.k_scale;
     a.v_scale = p.v_scale;
+    a.window = p.sliding_window;
     {
         // workspace: [T | pad to 256][prefix B+1 | pad][O partials][lse partials]
         uint8_t *ws = static_cast<uint8_t *>(p.workspace);

@@ -130,11 +130,14 @@ struct PrefillArgs {
     const float *k_scale;         // FP8 pools: per-KV-head scales
     const float *v_scale;
     int32_t *sched;               // [0] next item, [1] CTAs finished; both 0 between launches
+    int32_t window;               // sliding window W (0 = none): keys >= position - (W - 1)
 };
 
 // One work item: a 128-row query tile of T query heads of one request.
 struct PrefillItem {
     int b, tile, h0, kvh, q0, Lk, off, rows_here, kv_end, n_kv, min_vis;
+    int j0;       // first 128-key step (a sliding window skips the ones before)
+    int lo_max;   // keys below this are outside some row's window: mask there
 };
 
 // Item v of the virtual list (k-th tile from the end of request b, head group
@@ -167,6 +170,17 @@ __device__ __forceinline__ bool prefill_item(const PrefillArgs &a, int v, Prefil
     // keys every row of the tile sees: steps entirely below this need no mask
     const int mv = a.causal ? min(it.Lk, it.off + it.tile * kBM + 1) : it.Lk;
     it.min_vis = mv < 0 ? 0 : mv;
+    // sliding window: row i sees keys >= off + i - (W - 1); the first row's
+    // bound fixes the first step, the last row's where masking stops
+    it.j0 = 0;
+    it.lo_max = 0;
+    if (a.window > 0) {
+        const int lo_first = it.off + it.tile * kBM - (a.window - 1);
+        it.j0 = lo_first > 0 ? lo_first / kBN : 0;
+        it.lo_max = lo_first + it.rows_here - 1;
+        it.n_kv -= it.j0;
+        if (it.n_kv < 0) it.n_kv = 0;
+    }
     return true;
 }
 
@@ -362,7 +376,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     // row at d = 128), as one copy group.
     auto gather_rows = [&](const PrefillItem &it, int c, int (&rows)[kBN / 32]) {
         const int32_t *pt = a.page_table + (int64_t)it.b * a.pt_stride;
-        const int key0 = (c >> 1) * kBN;
+        const int key0 = (it.j0 + (c >> 1)) * kBN;
 #pragma unroll
         for (int rr = 0; rr < kBN / 32; ++rr) {
             const int key = key0 + rr * 32 + lane;
@@ -376,7 +390,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             constexpr int kRowsPerIssue = 32 / kChunks;
             uint8_t *dst = land(gl % NS);
             const uint8_t *src = (c & 1) ? a.v_cache : a.k_cache;
-            const int key0 = (c >> 1) * kBN;
+            const int key0 = (it.j0 + (c >> 1)) * kBN;
             const int q = lane % kChunks, sub = lane / kChunks;
 #pragma unroll 1
             for (int rr = 0; rr < kBN / 32; ++rr) {
@@ -403,7 +417,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         constexpr int kRowsPerIssue = 32 / kChunks;   // 2 (d = 128) or 4 (d = 64)
         uint8_t *dst = smem + S::kRing + (gl % NS) * S::kTileBytes;
         const uint8_t *src = (c & 1) ? a.v_cache : a.k_cache;
-        const int key0 = (c >> 1) * kBN;
+        const int key0 = (it.j0 + (c >> 1)) * kBN;
         const int q = lane % kChunks;                 // this lane's chunk of a row
         const int hh = q / 8;
         const int sub = lane / kChunks;
@@ -485,11 +499,11 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         // the id is outside the pool.  Split so that the read is in flight
         // while the producer waits for a ring slot.
         auto page_id = [&](const PrefillItem &it, int j) {
-            const int kk = j * kBN + lane * 16;
+            const int kk = (it.j0 + j) * kBN + lane * 16;
             return (lane < kBN / 16 && kk < it.kv_end) ? a.page_table[(int64_t)it.b * a.pt_stride + kk / 16] : -1;
         };
         auto page_slot0 = [&](const PrefillItem &it, int j, int page) {
-            const int kk = j * kBN + lane * 16;
+            const int kk = (it.j0 + j) * kBN + lane * 16;
             if (lane >= kBN / 16 || kk >= it.kv_end) return a.num_slots;
             if (page >= 0 && (int64_t)page * 16 < a.num_slots) return page * 16;
             raise_error(PA_DEVERR_PAGE_RANGE);
@@ -756,12 +770,13 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) tmem_ld32(s_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
             tmem_wait_ld();
-            const int kbase = j * kBN;
-            if (kbase + kBN > min_vis) {                // tile reaches the diagonal / end: mask
+            const int kbase = (it.j0 + j) * kBN;
+            if (kbase + kBN > min_vis || kbase < it.lo_max) {   // diagonal / end / window edge: mask
                 const int lim = row_valid ? vis_end - kbase : kBN;
+                const int lo = (row_valid && a.window > 0) ? off + qi - (a.window - 1) - kbase : 0;
 #pragma unroll
                 for (int c = 0; c < kBN; ++c)
-                    if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+                    if (c >= lim || c < lo) sr[c] = __float_as_uint(-INFINITY);
             }
             // row maximum of the raw scores (scale > 0 commutes with max)
             float mx[8];
@@ -988,6 +1003,7 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     }
     a.k_scale = p.k_scale;
     a.v_scale = p.v_scale;
+    a.window = p.sliding_window;
     a.k_cache = static_cast<const uint8_t *>(p.k_cache);
     a.v_cache = static_cast<const uint8_t *>(p.v_cache);
     a.page_table = p.page_table;

@@ -44,7 +44,8 @@ class DecodeGraphRunner:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, *, num_q_heads: int,
                  max_seqlen_k: int, buckets=(1, 2, 4, 8, 16, 32, 64, 128, 256),
                  page_size: int | None = None, scale: float | None = None, kv_chunk: int = 0,
-                 k_scale: torch.Tensor | None = None, v_scale: torch.Tensor | None = None):
+                 k_scale: torch.Tensor | None = None, v_scale: torch.Tensor | None = None,
+                 sliding_window: int = 0):
         self.k_cache, self.v_cache = k_cache, v_cache
         self.k_scale, self.v_scale = k_scale, v_scale
         self.device = k_cache.device
@@ -53,6 +54,7 @@ class DecodeGraphRunner:
         self.max_seqlen_k = int(max_seqlen_k)
         self.scale = float(1.0 / math.sqrt(d) if scale is None else scale)
         self.kv_chunk = int(kv_chunk)
+        self.sliding_window = int(sliding_window)
         self.buckets = tuple(sorted(set(int(b) for b in buckets)))
         max_b = self.buckets[-1]
         ncols = max(1, -(-self.max_seqlen_k // P))
@@ -73,7 +75,7 @@ class DecodeGraphRunner:
         api.decode(self.q[:b], self.k_cache, self.v_cache, self.page_table[:b], self.cache_seqlens[:b],
                    self.max_seqlen_k, scale=self.scale, page_size=self.page_size, out=self.out[:b],
                    lse=self.lse[:b], workspace=self.workspace, kv_chunk=self.kv_chunk,
-                   k_scale=self.k_scale, v_scale=self.v_scale)
+                   k_scale=self.k_scale, v_scale=self.v_scale, sliding_window=self.sliding_window)
 
     def capture(self) -> None:
         """Capture one graph per bucket (the buffers hold empty requests, so

@@ -103,6 +103,7 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(causal=2), INVALID),
     (dict(page_table_stride=1), INVALID),
     (dict(scale=float("nan")), INVALID),
+    (dict(sliding_window=-3), INVALID),
 ])
 def test_prefill_rejects_before_launch(lib, kw, status):
     assert _prefill(lib, **kw) == status
@@ -120,6 +121,7 @@ def test_prefill_rejects_before_launch(lib, kw, status):
     (dict(num_seqs=20000), UNSUPPORTED),
     (dict(kv_dtype=2), INVALID),
     (dict(kv_dtype=1), INVALID),                              # FP8 without scales
+    (dict(sliding_window=-1), INVALID),
 ])
 def test_decode_rejects_before_launch(lib, kw, status):
     assert _decode(lib, **kw) == status
