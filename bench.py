@@ -176,12 +176,21 @@ class MixedBatch:
         self.store_bytes = 2 * 2 * Tn * self.Hkv * self.D * 2
         self.step_bytes = self.decode_bytes + self.prefill_bytes + self.store_bytes
         self.launches_per_step = 6   # store, 2 page tables, prefill, decode split + combine
+        self.num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.prefill_sms = 12        # overlapped schedule (0: phases in sequence)
         from paged_kv_flashattention_gb300.metadata import MetadataBuilder
         self.meta_dec = MetadataBuilder(dev, d.num_seqs)
         self.meta_pre = MetadataBuilder(dev, p.num_seqs)
 
-    def step(self, timing: bool = False):
+    def step(self, timing: bool = False, concurrent: bool | None = None):
+        """One pass of the path.  concurrent (the default unless timing):
+        prefill runs on ``prefill_sms`` SMs and decode, launched as its
+        programmatic dependent, on the others at the same time (prefill is
+        tensor-bound, decode HBM-bound).  timing: the phases one after the
+        other, with events between them."""
         torch, pa = self.torch, self.pa
+        if concurrent is None:
+            concurrent = not timing and self.prefill_sms > 0
         ev = None
         if timing:
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
@@ -194,11 +203,14 @@ class MixedBatch:
         if timing:
             ev[1].record()
         pa.prefill(self.q_pre, self.k_cache, self.v_cache, mp.page_table, mp.cu_seqlens_q, mp.cu_seqlens_k,
-                   mp.max_seqlen_q, mp.max_seqlen_k, causal=True, out=self.out_pre)
+                   mp.max_seqlen_q, mp.max_seqlen_k, causal=True, out=self.out_pre,
+                   max_ctas=self.prefill_sms if concurrent else 0)
         if timing:
             ev[2].record()
         pa.decode(self.q_dec, self.k_cache, self.v_cache, md.page_table, md.cache_seqlens, md.max_seqlen_k,
-                  out=self.out_dec, workspace=self.workspace)
+                  out=self.out_dec, workspace=self.workspace,
+                  max_ctas=2 * (self.num_sms - self.prefill_sms) if concurrent else 0,
+                  overlap_previous=concurrent)
         if timing:
             ev[3].record()
         self._keep = (md, mp)
@@ -231,6 +243,7 @@ def run_gpu(args):
     peaks, peak_src = load_peaks()
 
     mb = MixedBatch(dev)
+    mb.prefill_sms = args.prefill_sms
     torch.cuda.synchronize()
 
     def barrier():
@@ -241,18 +254,24 @@ def run_gpu(args):
     for _ in range(args.warmup):
         mb.step()
     barrier()
-    # ---- timed device steps (per-phase events recorded on the same stream)
-    phase = {"store_meta": [], "prefill": [], "decode": []}
+    # ---- timed device steps: the headline (prefill and decode overlapped)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    evs = []
     with ClockSampler(local) as clk:
         start.record()
         for _ in range(args.steps):
-            evs.append(mb.step(timing=True))
+            mb.step()
         end.record()
         torch.cuda.synchronize()
     barrier()
     total_ms = start.elapsed_time(end)
+    # ---- the same steps with the phases in sequence, for the per-kernel
+    # numbers (events recorded between the launches on the same stream)
+    phase = {"store_meta": [], "prefill": [], "decode": []}
+    evs = []
+    for _ in range(args.steps):
+        evs.append(mb.step(timing=True))
+    torch.cuda.synchronize()
+    barrier()
     for e in evs:
         phase["store_meta"].append(e[0].elapsed_time(e[1]))
         phase["prefill"].append(e[1].elapsed_time(e[2]))
@@ -350,6 +369,8 @@ def run_gpu(args):
                    f"{mb.decode_bytes / 1e9:.2f} GB per step; no flush)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "step": "store_kv + metadata (2 batches) + prefill + decode(split+combine)",
+                   "schedule": (f"prefill on {mb.prefill_sms} SMs overlapped with decode on the other "
+                                f"{mb.num_sms - mb.prefill_sms}" if mb.prefill_sms > 0 else "phases in sequence"),
                    "step_bytes": mb.step_bytes},
         "roofline": {"bound": "hbm", "kernel": "decode pass (split-KV kernel + LSE combine)",
                      "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -616,6 +637,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target wall time of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-sms", type=int, default=12,
+                    help="SMs the prefill gets while decode runs beside it (0 = one after the other)")
     ap.add_argument("--ref-seqs", type=int, default=24, help="decode sequences per reference step")
     ap.add_argument("--micro", choices=sorted(MICRO_CASES), default=None,
                     help="time one kernel on one workload instead of the full step")

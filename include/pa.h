@@ -254,6 +254,9 @@ typedef struct {
     const float *v_scale;
     int32_t sliding_window;      /* 0 = none; W > 0: a query at position p sees only keys
                                     j >= p - (W - 1) ([T] s.19 "sliding window" mask) */
+    int32_t max_ctas;            /* 0 = one persistent CTA per SM; n > 0: at most n CTAs
+                                    (each holds a whole SM), leaving the other SMs to a
+                                    concurrent launch, e.g. pa_decode on another stream */
 } pa_prefill_params;
 
 pa_status pa_prefill(const pa_prefill_params *p, void *stream);
@@ -297,6 +300,13 @@ typedef struct {
     const float *v_scale;        /* (element = value(code) * scale[kv head]) */
     int32_t sliding_window;      /* 0 = none; W > 0: only the last W keys of each sequence
                                     are read and attended to */
+    int32_t max_ctas;            /* 0 = every resident CTA slot; n > 0: at most n CTAs */
+    int32_t overlap_previous;    /* 1: the split kernel may start while the previous kernel
+                                    in the stream still runs (a programmatic dependent: it
+                                    starts once every CTA of that kernel has signalled, as
+                                    pa_prefill's do on entry).  Only valid when this decode
+                                    reads nothing that kernel writes; with max_ctas on both
+                                    calls, prefill and decode then share the SMs.  0 = no. */
 } pa_decode_params;
 
 /* Bytes of workspace pa_decode needs for these parameters (always > 0: a

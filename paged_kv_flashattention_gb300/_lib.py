@@ -33,6 +33,7 @@ class PrefillParams(ctypes.Structure):
         ("page_size", c_i32), ("num_pages", c_i64), ("causal", c_i32), ("scale", c_f32),
         ("out", c_p), ("lse", c_p), ("lse_stride", c_i64),
         ("kv_dtype", c_i32), ("k_scale", c_p), ("v_scale", c_p), ("sliding_window", c_i32),
+        ("max_ctas", c_i32),
     ]
 
 
@@ -45,7 +46,7 @@ class DecodeParams(ctypes.Structure):
         ("page_size", c_i32), ("num_pages", c_i64), ("scale", c_f32),
         ("out", c_p), ("lse", c_p), ("workspace", c_p), ("workspace_bytes", c_size),
         ("kv_chunk", c_i32), ("kv_dtype", c_i32), ("k_scale", c_p), ("v_scale", c_p),
-        ("sliding_window", c_i32),
+        ("sliding_window", c_i32), ("max_ctas", c_i32), ("overlap_previous", c_i32),
     ]
 
 

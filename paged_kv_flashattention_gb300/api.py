@@ -249,7 +249,8 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
             max_seqlen_k: int, *, causal: bool = True, scale: float | None = None,
             page_size: int | None = None, out: torch.Tensor | None = None,
             lse: torch.Tensor | None = None, k_scale: torch.Tensor | None = None,
-            v_scale: torch.Tensor | None = None, sliding_window: int = 0) -> torch.Tensor:
+            v_scale: torch.Tensor | None = None, sliding_window: int = 0,
+            max_ctas: int = 0) -> torch.Tensor:
     """Varlen prefill / extend attention.  q: bf16 [total_q, Hq, d];
     returns out bf16 [total_q, Hq, d]; lse (optional) fp32 [Hq, total_q].
     Pools are bf16, or E4M3 codes (uint8 / float8_e4m3fn) with fp32
@@ -285,14 +286,16 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
         scale=float(1.0 / math.sqrt(d) if scale is None else scale), out=_ptr(out),
         lse=_ptr(lse), lse_stride=(lse.stride(0) if lse is not None else 0), kv_dtype=kvd,
         k_scale=_ptr(k_scale) if kvd == PA_KV_FP8_E4M3 else None,
-        v_scale=_ptr(v_scale) if kvd == PA_KV_FP8_E4M3 else None, sliding_window=int(sliding_window))
+        v_scale=_ptr(v_scale) if kvd == PA_KV_FP8_E4M3 else None, sliding_window=int(sliding_window),
+        max_ctas=int(max_ctas))
     lib = _lib.load()
     _check(lib.pa_prefill(ctypes.byref(p), _stream(q)), lib)
     return out
 
 
 def _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k, scale, page_size,
-                   out, lse, workspace, kv_chunk, k_scale=None, v_scale=None, sliding_window=0):
+                   out, lse, workspace, kv_chunk, k_scale=None, v_scale=None, sliding_window=0,
+                   max_ctas=0, overlap_previous=False):
     num_pages, P, Hkv, d = _pool_geometry(k_cache, v_cache, page_size)
     B, Hq, dq = q.shape
     if dq != d:
@@ -310,7 +313,8 @@ def _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k,
                                                     if workspace is not None else 0),
         kv_chunk=int(kv_chunk), kv_dtype=kvd,
         k_scale=_ptr(k_scale) if kvd == PA_KV_FP8_E4M3 else None,
-        v_scale=_ptr(v_scale) if kvd == PA_KV_FP8_E4M3 else None, sliding_window=int(sliding_window))
+        v_scale=_ptr(v_scale) if kvd == PA_KV_FP8_E4M3 else None, sliding_window=int(sliding_window),
+        max_ctas=int(max_ctas), overlap_previous=int(bool(overlap_previous)))
 
 
 def decode_workspace_size(q_shape, k_cache: torch.Tensor, max_seqlen_k: int, *,
@@ -339,7 +343,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_t
            page_size: int | None = None, out: torch.Tensor | None = None,
            lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
            kv_chunk: int = 0, k_scale: torch.Tensor | None = None,
-           v_scale: torch.Tensor | None = None, sliding_window: int = 0) -> torch.Tensor:
+           v_scale: torch.Tensor | None = None, sliding_window: int = 0,
+           max_ctas: int = 0, overlap_previous: bool = False) -> torch.Tensor:
     """Split-KV decode: q bf16 [B, Hq, d] -> out bf16 [B, Hq, d]; lse fp32 [B, Hq].
     Pools are bf16, or E4M3 codes (uint8 / float8_e4m3fn) with fp32 per-KV-head
     ``k_scale`` and ``v_scale``.  ``workspace`` (a uint8 CUDA tensor) is
@@ -362,7 +367,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_t
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     p = _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k, scale, page_size,
-                       out, lse, workspace, kv_chunk, k_scale, v_scale, sliding_window)
+                       out, lse, workspace, kv_chunk, k_scale, v_scale, sliding_window, max_ctas,
+                       overlap_previous)
     lib = _lib.load()
     _check(lib.pa_decode(ctypes.byref(p), _stream(q)), lib)
     return out

@@ -88,6 +88,8 @@ struct DecodeArgs {
     const float *k_scale;         // FP8 pools: per-KV-head scales
     const float *v_scale;
     int32_t window;               // sliding window W (0 = none): the last W keys
+    int32_t max_ctas;             // host only: cap on the persistent grid (0 = every SM)
+    int32_t overlap_previous;     // host only: launch as a programmatic dependent
     int32_t *ws_header;           // [0] = T
     int32_t *ws_prefix;           // [B+1] exclusive prefix of the sequence lengths
 };
@@ -562,7 +564,24 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int64_t items_max, cudaStream_t
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     int64_t grid = (int64_t)num_sms() * per_sm;
+    if (a.max_ctas > 0 && grid > a.max_ctas) grid = a.max_ctas;
     if (grid > items_max) grid = items_max;
+    if (a.overlap_previous) {
+        // A programmatic dependent of the previous kernel in the stream: it is
+        // scheduled as soon as every CTA of that kernel has signalled (the
+        // prefill kernel does so on entry) and never waits for its results.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3((HPC + 1) * 32);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, a);
+    }
     kern<<<(unsigned)grid, (HPC + 1) * 32, smem, stream>>>(a);
     return cudaGetLastError();
 }
@@ -644,6 +663,8 @@ cudaError_t launch_decode(const pa_decode_params &p, const DecodePlan &plan, cud
     a.k_scale = p.k_scale;
     a.v_scale = p.v_scale;
     a.window = p.sliding_window;
+    a.max_ctas = p.max_ctas;
+    a.overlap_previous = p.overlap_previous;
     {
         // workspace: [T | pad to 256][prefix B+1 | pad][O partials][lse partials]
         uint8_t *ws = static_cast<uint8_t *>(p.workspace);

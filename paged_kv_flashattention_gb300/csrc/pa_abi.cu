@@ -266,6 +266,7 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
     if (p->kv_dtype == PA_KV_FP8_E4M3 && (!p->k_scale || !p->v_scale))
         return fail(PA_ERR_INVALID, "FP8 pools need k_scale and v_scale");
     if (p->sliding_window < 0) return fail(PA_ERR_INVALID, "sliding_window must be >= 0");
+    if (p->max_ctas < 0) return fail(PA_ERR_INVALID, "max_ctas must be >= 0");
     cudaError_t e = launch_prefill(*p, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "prefill configuration not supported by this build");
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "prefill launch");
@@ -287,6 +288,8 @@ static pa_status check_decode(const pa_decode_params *p) {
     if (p->kv_dtype == PA_KV_FP8_E4M3 && p->num_seqs > 0 && (!p->k_scale || !p->v_scale))
         return fail(PA_ERR_INVALID, "FP8 pools need k_scale and v_scale");
     if (p->sliding_window < 0) return fail(PA_ERR_INVALID, "sliding_window must be >= 0");
+    if (p->max_ctas < 0) return fail(PA_ERR_INVALID, "max_ctas must be >= 0");
+    if (p->overlap_previous != 0 && p->overlap_previous != 1) return fail(PA_ERR_INVALID, "overlap_previous must be 0 or 1");
     return PA_OK;
 }
 

@@ -295,6 +295,9 @@ constexpr int kControlRegs = 128;
 template <int D, int T, bool F8>
 __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
     using S = PrefillSmem<D, T, F8>;
+    // A kernel launched after this one as a programmatic dependent (decode
+    // sharing the GPU) may start once every CTA of this grid is resident.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int H = S::kHalves;
     constexpr int kProducer = 4 * T;
     constexpr int kMma = 4 * T + 1;
@@ -1032,7 +1035,9 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     cudaError_t e = prefill_sched(&a.sched);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (each holds all 512 TMEM columns)
-    dim3 grid((unsigned)(virt < num_sms() ? virt : num_sms()));
+    int64_t ctas = num_sms();
+    if (p.max_ctas > 0 && p.max_ctas < ctas) ctas = p.max_ctas;   // leave SMs to a concurrent launch
+    dim3 grid((unsigned)(virt < ctas ? virt : ctas));
     if (f8) {
         if (p.head_dim == 128)
             return T == 2 ? launch_t<128, 2, true>(a, grid, stream) : launch_t<128, 1, true>(a, grid, stream);

@@ -183,3 +183,29 @@ def test_prefill_concurrent_streams(cuda_device):
     ref1, _ = oracle_ref(probs[1], rows=rows)
     o1 = outs[1][torch.from_numpy(rows[:, 0]).to(cuda_device), torch.from_numpy(rows[:, 1]).to(cuda_device)]
     compare(o1, ref1, "stream 1")
+
+
+def test_prefill_and_decode_overlapped(cuda_device):
+    """Prefill on a few SMs with decode launched as its programmatic
+    dependent on the rest (the benchmark's schedule): both agree with the
+    oracle, and so does a decode capped to a handful of CTAs."""
+    import paged_kv_flashattention_gb300 as pa
+    pp, pd = W.config(3), W.config(2)
+    dp, dd = DeviceProblem(pp, cuda_device), DeviceProblem(pd, cuda_device)
+    dp.store()
+    dd.store()
+    mp, md = dp.metadata(), dd.metadata()
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    out_p = pa.prefill(dp.q, dp.k_cache, dp.v_cache, mp.page_table, mp.cu_seqlens_q, mp.cu_seqlens_k,
+                       mp.max_seqlen_q, mp.max_seqlen_k, causal=True, scale=pp.scale, max_ctas=12)
+    out_d = pa.decode(dd.q, dd.k_cache, dd.v_cache, md.page_table, md.cache_seqlens, md.max_seqlen_k,
+                      scale=pd.scale, max_ctas=2 * (sms - 12), overlap_previous=True)
+    small = pa.decode(dd.q, dd.k_cache, dd.v_cache, md.page_table, md.cache_seqlens, md.max_seqlen_k,
+                      scale=pd.scale, max_ctas=5)
+    torch.cuda.synchronize()
+    ref_p, _ = oracle_ref(pp)
+    ref_d, _ = oracle_ref(pd)
+    compare(out_p, ref_p, "prefill on 12 SMs")
+    compare(out_d, ref_d, "decode overlapped with prefill")
+    compare(small, ref_d, "decode on 5 CTAs")
