@@ -144,7 +144,7 @@ struct PrefillItem {
 // hp), k-major: every request's later, longer tiles come before its earlier
 // ones, so persistent CTAs taking items round robin start with the longest
 // work.  Returns false for a hole (request b has fewer than k + 1 tiles).
-template <int T>
+template <int T, bool WIN = false>
 __device__ __forceinline__ bool prefill_item(const PrefillArgs &a, int v, PrefillItem &it) {
     const int groups = a.num_q_heads / T;
     const int hp = v % groups;
@@ -174,7 +174,7 @@ __device__ __forceinline__ bool prefill_item(const PrefillArgs &a, int v, Prefil
     // bound fixes the first step, the last row's where masking stops
     it.j0 = 0;
     it.lo_max = 0;
-    if (a.window > 0) {
+    if (WIN && a.window > 0) {
         const int lo_first = it.off + it.tile * kBM - (a.window - 1);
         it.j0 = lo_first > 0 ? lo_first / kBN : 0;
         it.lo_max = lo_first + it.rows_here - 1;
@@ -292,7 +292,9 @@ constexpr int kSoftmaxRegs = 184;
 constexpr int kItemRing = 4;      // items published ahead of the consumers
 constexpr int kControlRegs = 128;
 
-template <int D, int T, bool F8>
+// WIN: the sliding-window instantiation (windowless launches keep the window
+// arithmetic out of their registers).
+template <int D, int T, bool F8, bool WIN>
 __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
     using S = PrefillSmem<D, T, F8>;
     // A kernel launched after this one as a programmatic dependent (decode
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         // earlier: a CTA that holds an item it has not started keeps it from
         // CTAs that are idle at the end).
         for (int v; (v = take(local)) >= 0;) {
-            prefill_item<T>(a, v, it);
+            prefill_item<T, WIN>(a, v, it);
             // load 2j is K_j, 2j + 1 is V_j; gl counts loads over the CTA's
             // life.  The Q tiles are loaded once the previous item's last S
             // MMA is done.
@@ -580,7 +582,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             if (lane == 0) mbar_arrive(&item_empty[slot]);
             ++local;
             if (v < 0) break;
-            prefill_item<T>(a, v, it);
+            prefill_item<T, WIN>(a, v, it);
             if (!gather_item(it, gl, g)) break;
             gl += 2 * it.n_kv;
         }
@@ -597,7 +599,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             __syncwarp();
             if (lane == 0) mbar_arrive(&item_empty[slot]);
             if (v < 0) break;
-            prefill_item<T>(a, v, it);
+            prefill_item<T, WIN>(a, v, it);
             // Q tiles: bf16 -> f16 of q * k_scale, in place
             if (!__all_sync(0xffffffffu, mbar_wait(q_full, local & 1))) break;
             ++local;
@@ -690,7 +692,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                 const int v = item_idx[slot];
                 mbar_arrive(&item_empty[slot]);
                 if (v < 0) break;
-                prefill_item<T>(a, v, it);
+                prefill_item<T, WIN>(a, v, it);
                 const int n_kv = it.n_kv;
                 if (!mbar_wait(F8 ? q_conv : q_full, local & 1)) break;
                 if (n_kv > 0) {
@@ -755,7 +757,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         if (lane == 0) mbar_arrive(&item_empty[slot]);
         ++local;
         if (v < 0) break;
-        prefill_item<T>(a, v, it);
+        prefill_item<T, WIN>(a, v, it);
         const int n_kv = it.n_kv, Lk = it.Lk, off = it.off, min_vis = it.min_vis;
         const int qi = it.tile * kBM + r;             // query index within the request
         const bool row_valid = r < it.rows_here;
@@ -774,9 +776,9 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             for (int c = 0; c < kBN / 32; ++c) tmem_ld32(s_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
             tmem_wait_ld();
             const int kbase = (it.j0 + j) * kBN;
-            if (kbase + kBN > min_vis || kbase < it.lo_max) {   // diagonal / end / window edge: mask
+            if (kbase + kBN > min_vis || (WIN && kbase < it.lo_max)) {   // diagonal / end / window edge: mask
                 const int lim = row_valid ? vis_end - kbase : kBN;
-                const int lo = (row_valid && a.window > 0) ? off + qi - (a.window - 1) - kbase : 0;
+                const int lo = (WIN && row_valid && a.window > 0) ? off + qi - (a.window - 1) - kbase : 0;
 #pragma unroll
                 for (int c = 0; c < kBN; ++c)
                     if (c >= lim || c < lo) sr[c] = __float_as_uint(-INFINITY);
@@ -785,10 +787,17 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             float mx[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i]);
+            // elements 0-7 above, then pairs of 8-element blocks, then the
+            // last block on its own (kBN - 8 is not a multiple of 16)
+            constexpr int kPairEnd = 8 + 16 * ((kBN - 8) / 16);
 #pragma unroll
-            for (int c = 8; c < kBN; c += 16)
+            for (int c = 8; c < kPairEnd; c += 16)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+#pragma unroll
+            for (int c = kPairEnd; c < kBN; c += 8)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(sr[c + i]));
             const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
             const float m_cand = mt * a.scale_log2;
             // lazy maximum: move it only when the tile maximum exceeds it by
@@ -952,13 +961,13 @@ bool make_map_fp8(CUtensorMap *m, const void *base, int d, int heads, int64_t ro
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int T, bool F8>
+template <int D, int T, bool F8, bool WIN>
 cudaError_t launch_t(const PrefillArgs &a, dim3 grid, cudaStream_t stream) {
     using S = PrefillSmem<D, T, F8>;
     static_assert(S::kSlots >= 2 && (!F8 || S::kCSlots >= 2), "ring too small");
     // One CTA per SM (it allocates all 512 TMEM columns).
     const int smem = (S::kTotal + 1024) > 120 * 1024 ? (S::kTotal + 1024) : 120 * 1024;
-    auto kern = prefill_kernel<D, T, F8>;
+    auto kern = prefill_kernel<D, T, F8, WIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, 128 * (T + 1), smem, stream>>>(a);
@@ -993,6 +1002,18 @@ cudaError_t prefill_sched(int32_t **ptr) {
 }
 
 }  // namespace
+
+template <bool WIN>
+cudaError_t dispatch_f8(const PrefillArgs &a, bool f8, int d, int T, dim3 grid, cudaStream_t stream) {
+    if (f8) {
+        if (d == 128)
+            return T == 2 ? launch_t<128, 2, true, WIN>(a, grid, stream) : launch_t<128, 1, true, WIN>(a, grid, stream);
+        return T == 2 ? launch_t<64, 2, true, WIN>(a, grid, stream) : launch_t<64, 1, true, WIN>(a, grid, stream);
+    }
+    if (d == 128)
+        return T == 2 ? launch_t<128, 2, false, WIN>(a, grid, stream) : launch_t<128, 1, false, WIN>(a, grid, stream);
+    return T == 2 ? launch_t<64, 2, false, WIN>(a, grid, stream) : launch_t<64, 1, false, WIN>(a, grid, stream);
+}
 
 cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     PrefillArgs a{};
@@ -1038,14 +1059,8 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     int64_t ctas = num_sms();
     if (p.max_ctas > 0 && p.max_ctas < ctas) ctas = p.max_ctas;   // leave SMs to a concurrent launch
     dim3 grid((unsigned)(virt < ctas ? virt : ctas));
-    if (f8) {
-        if (p.head_dim == 128)
-            return T == 2 ? launch_t<128, 2, true>(a, grid, stream) : launch_t<128, 1, true>(a, grid, stream);
-        return T == 2 ? launch_t<64, 2, true>(a, grid, stream) : launch_t<64, 1, true>(a, grid, stream);
-    }
-    if (p.head_dim == 128)
-        return T == 2 ? launch_t<128, 2, false>(a, grid, stream) : launch_t<128, 1, false>(a, grid, stream);
-    return T == 2 ? launch_t<64, 2, false>(a, grid, stream) : launch_t<64, 1, false>(a, grid, stream);
+    return a.window > 0 ? dispatch_f8<true>(a, f8, p.head_dim, T, grid, stream)
+                        : dispatch_f8<false>(a, f8, p.head_dim, T, grid, stream);
 }
 
 cudaError_t launch_exp2_selftest(const float *x, float *y, int64_t n, cudaStream_t stream) {
