@@ -133,11 +133,14 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)
 
 // Two E4M3 codes (low byte first) to two f16 (exact: every E4M3 value is an
 // f16 value).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two_codes));
-    return r;
+// All four codes of a register (bytes 0-1 and 2-3) to two f16x2 registers,
+// the 32-bit register split into its 16-bit halves inside the asm.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t four_codes, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi) : "r"(four_codes));
 }
+
 
 __device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
     return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
@@ -366,8 +369,9 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
                     ldsm_x4(r, ks + a_tok * S::kRowStride + kp * 32 + a_dim * 2);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint32_t af[4] = {e4m3x2_to_f16x2(r[2 * h]), e4m3x2_to_f16x2(r[2 * h + 1]),
-                                                e4m3x2_to_f16x2(r[2 * h] >> 16), e4m3x2_to_f16x2(r[2 * h + 1] >> 16)};
+                        uint32_t af[4];
+                        e4m3x4_to_f16x4(r[2 * h], af[0], af[2]);
+                        e4m3x4_to_f16x4(r[2 * h + 1], af[1], af[3]);
                         mma_f16_16816(sc, af, qb[2 * kp + h][0], qb[2 * kp + h][1]);
                     }
                 }
@@ -436,8 +440,9 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t p0 = __byte_perm(r[2 * h], 0u, 0x3120);
                         const uint32_t p1 = __byte_perm(r[2 * h + 1], 0u, 0x3120);
-                        const uint32_t vf[4] = {e4m3x2_to_f16x2(p0), e4m3x2_to_f16x2(p0 >> 16),
-                                                e4m3x2_to_f16x2(p1), e4m3x2_to_f16x2(p1 >> 16)};
+                        uint32_t vf[4];
+                        e4m3x4_to_f16x4(p0, vf[0], vf[1]);
+                        e4m3x4_to_f16x4(p1, vf[2], vf[3]);
                         mma_f16_16816(oacc[2 * mp + h], vf, pb0, pb1);
                     }
                 }

@@ -264,11 +264,12 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 x, float s) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Two E4M3 codes (low byte first) to two f16 (exact).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two_codes));
-    return r;
+// Four E4M3 codes (bytes 0-3) to four f16 in two registers (exact); the
+// 32-bit register is split into its 16-bit halves inside the asm.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t four_codes, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi) : "r"(four_codes));
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -640,10 +641,11 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                         const int byte = (i0 + u) * 512 + lane * 16;
                         const int rr = 64 * cw + byte / D;
                         const int q = (byte % D) / 16;      // 16 codes: d = 16 q .. 16 q + 15
-                        const uint4 lo = make_uint4(e4m3x2_to_f16x2(x[u].x), e4m3x2_to_f16x2(x[u].x >> 16),
-                                                    e4m3x2_to_f16x2(x[u].y), e4m3x2_to_f16x2(x[u].y >> 16));
-                        const uint4 hi = make_uint4(e4m3x2_to_f16x2(x[u].z), e4m3x2_to_f16x2(x[u].z >> 16),
-                                                    e4m3x2_to_f16x2(x[u].w), e4m3x2_to_f16x2(x[u].w >> 16));
+                        uint4 lo, hi;
+                        e4m3x4_to_f16x4(x[u].x, lo.x, lo.y);
+                        e4m3x4_to_f16x4(x[u].y, lo.z, lo.w);
+                        e4m3x4_to_f16x4(x[u].z, hi.x, hi.y);
+                        e4m3x4_to_f16x4(x[u].w, hi.z, hi.w);
                         const int hh = q / 4, c0 = 2 * (q % 4);
                         uint8_t *row = dst + hh * 16384 + rr * 128;
                         *reinterpret_cast<uint4 *>(row + ((c0 ^ (rr & 7)) * 16)) = lo;

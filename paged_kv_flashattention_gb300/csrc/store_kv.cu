@@ -198,9 +198,11 @@ __global__ void __launch_bounds__(256) rope_store_kernel(const RopeStoreArgs a) 
         const bool store = slot >= 0 && slot < a.num_slots;
         if (slot >= a.num_slots && lane == 0) raise_error(PA_DEVERR_PAGE_RANGE);
         const float *cs = a.cos_sin + (int64_t)pos * r;
-        // q heads then k heads, `units` pieces each
+        // q heads then k heads, `units` pieces each; (head, piece) of item f
+        // advanced incrementally instead of divided out per item
+        int hd = lane / units, u = lane % units;
+        const int dhd = 32 / units, du = 32 % units;
         for (int f = lane; f < (Hq + Hkv) * units; f += 32) {
-            const int hd = f / units, u = f % units;
             const bool is_q = hd < Hq;
             const int kvh = hd - Hq;
             const uint4 *src = is_q ? a.q + ((t * Hq + hd) * D) / 8 : a.k + ((t * Hkv + kvh) * D) / 8;
@@ -250,6 +252,12 @@ __global__ void __launch_bounds__(256) rope_store_kernel(const RopeStoreArgs a) 
                 const float sc = F8 ? __ldg(a.k_scale + kvh) : 1.f;
                 store8<F8>(a.k_cache, row + e0, out0, sc);
                 if (e1 >= 0) store8<F8>(a.k_cache, row + e1, out1, sc);
+            }
+            u += du;
+            hd += dhd;
+            if (u >= units) {
+                u -= units;
+                ++hd;
             }
         }
         if (store) {                                        // v: copied or quantised
