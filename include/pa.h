@@ -305,7 +305,8 @@ typedef struct {
                                     in the stream still runs (a programmatic dependent: it
                                     starts once every CTA of that kernel has signalled, as
                                     pa_prefill's do on entry).  Only valid when this decode
-                                    reads nothing that kernel writes; with max_ctas on both
+                                    reads nothing that kernel writes and that kernel does
+                                    not use this workspace; with max_ctas on both
                                     calls, prefill and decode then share the SMs.  0 = no. */
 } pa_decode_params;
 

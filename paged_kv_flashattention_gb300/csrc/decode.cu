@@ -506,6 +506,10 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(
     constexpr int VPL = D / 32;
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    // after decode this kernel runs as its programmatic dependent: wait until
+    // that grid has completed and its partials are visible (a no-op when
+    // launched normally)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (row >= num_rows) return;
     int n = max_splits;
     if (splits_per_row != nullptr) {
@@ -529,17 +533,29 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(
     for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
     float den = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < n; ++s) {
-            const float ls = lrow[s];
-            const float w = (ls == -INFINITY) ? 0.f : __expf(ls - M);
-            den += w;
-            const float *orow = o_part + ((int64_t)row * max_splits + s) * D + lane * VPL;
-            if constexpr (VPL == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(orow);
-                acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(orow);
-                acc[0] += w * v.x; acc[1] += w * v.y;
+        // four splits at a time: their loads are independent and go out together
+        constexpr int U = 4;
+        for (int s0 = 0; s0 < n; s0 += U) {
+            float ls[U], v[U][VPL];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int s = s0 + u;
+                ls[u] = s < n ? lrow[s] : -INFINITY;
+                const float *orow = o_part + ((int64_t)row * max_splits + (s < n ? s : 0)) * D + lane * VPL;
+                if constexpr (VPL == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(orow);
+                    v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2 *>(orow);
+                    v[u][0] = x.x; v[u][1] = x.y;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float w = (ls[u] == -INFINITY) ? 0.f : __expf(ls[u] - M);
+                den += w;
+#pragma unroll
+                for (int e = 0; e < VPL; ++e) acc[e] += w * v[u][e];
             }
         }
     }
@@ -710,15 +726,25 @@ cudaError_t launch_lse_combine(const float *o_partial, const float *lse_partial,
     const int rows_per_block = 8;
     const int blocks = (num_rows + rows_per_block - 1) / rows_per_block;
     auto *o = static_cast<__nv_bfloat16 *>(out);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(rows_per_block * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    // after the split kernel (seg_header given) the combine is its
+    // programmatic dependent: its launch is prepared while the split kernel's
+    // last CTAs finish, and griddepcontrol.wait holds it until they have
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = seg_header != nullptr ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (head_dim == 64)
-        lse_combine_kernel<64><<<blocks, rows_per_block * 32, 0, stream>>>(
-            o_partial, lse_partial, splits_per_row, seg_header, seg_prefix, head_groups,
-            heads_per_group, heads_per_seq, num_rows, max_splits, o, lse_out);
-    else
-        lse_combine_kernel<128><<<blocks, rows_per_block * 32, 0, stream>>>(
-            o_partial, lse_partial, splits_per_row, seg_header, seg_prefix, head_groups,
-            heads_per_group, heads_per_seq, num_rows, max_splits, o, lse_out);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, lse_combine_kernel<64>, o_partial, lse_partial, splits_per_row,
+                                  seg_header, seg_prefix, head_groups, heads_per_group, heads_per_seq,
+                                  num_rows, max_splits, o, lse_out);
+    return cudaLaunchKernelEx(&cfg, lse_combine_kernel<128>, o_partial, lse_partial, splits_per_row,
+                              seg_header, seg_prefix, head_groups, heads_per_group, heads_per_seq,
+                              num_rows, max_splits, o, lse_out);
 }
 
 // ---------------------------------------------------------------------------

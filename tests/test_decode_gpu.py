@@ -114,6 +114,35 @@ def test_decode_physical_permutation_invariance(cuda_device):
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
+def test_decode_workspace_reuse(cuda_device):
+    """One zero-filled workspace serves a run of calls with other length mixes
+    and split sizes.  Outputs start as NaN, so a split row whose merge did not
+    run (an arrival count left over from an earlier call) shows up."""
+    import paged_kv_flashattention_gb300 as pa
+    rng = np.random.default_rng(5)
+    cases = []
+    for i, chunk in enumerate((16, 0, 64, 16, 32)):
+        L = rng.integers(1, 900, size=12).astype(np.int32)
+        p = W.small_problem(500 + i, L - 1, np.ones_like(L), num_q_heads=16, num_kv_heads=4,
+                            head_dim=128, page_size=16)
+        d = DeviceProblem(p, cuda_device)
+        d.store()
+        cases.append((p, d, chunk, oracle_ref(p)))
+    need = max(pa.decode_workspace_size(d.q.shape, d.k_cache, d.metadata().max_seqlen_k, kv_chunk=c)
+               for _, d, c, _ in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device=cuda_device)
+    for rep in range(2):
+        for p, d, chunk, (ref, ref_lse) in cases:
+            m = d.metadata()
+            out = torch.full_like(d.q, float("nan"))
+            lse = torch.full((p.num_seqs, p.num_q_heads), float("nan"), dtype=torch.float32,
+                             device=cuda_device)
+            pa.decode(d.q, d.k_cache, d.v_cache, m.page_table, m.cache_seqlens, m.max_seqlen_k,
+                      scale=p.scale, out=out, lse=lse, workspace=ws, kv_chunk=chunk)
+            torch.cuda.synchronize()
+            compare(out, ref, f"reuse {rep} C{chunk}", lse_gpu=lse, lse_ref=ref_lse)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_lse_combine(cuda_device, d):
     import paged_kv_flashattention_gb300 as pa
