@@ -362,7 +362,8 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (F8) {
                 // one ldmatrix.x4 = two k-steps: matrices (tokens 0-7 | 8-15) x
-                // (codes 32 kp .. +15 | 32 kp + 16 .. +31) as b16 pairs
+                // (codes 32 kp .. +15 | 32 kp + 16 .. +31) as b16 pairs.  One
+                // chain of MMAs (two chains measured slower here)
 #pragma unroll
                 for (int kp = 0; kp < KS / 2; ++kp) {
                     uint32_t r[4];
@@ -376,12 +377,19 @@ __global__ void __launch_bounds__((HPC + 1) * 32) decode_kernel(const DecodeArgs
                     }
                 }
             } else {
+                // even and odd k-steps in two accumulators: two chains of
+                // dependent MMAs half as long, added at the end
+                float sc1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int kk = 0; kk < KS; ++kk) {
-                    uint32_t af[4];
+                for (int kk = 0; kk < KS; kk += 2) {
+                    uint32_t af[4], ag[4];
                     ldsm_x4(af, ks + a_tok * S::kRowStride + (kk * 16 + a_dim) * 2);
+                    ldsm_x4(ag, ks + a_tok * S::kRowStride + (kk * 16 + 16 + a_dim) * 2);
                     mma_bf16_16816(sc, af, qb[kk][0], qb[kk][1]);
+                    mma_bf16_16816(sc1, ag, qb[kk + 1][0], qb[kk + 1][1]);
                 }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sc[i] += sc1[i];
             }
             // log2 domain; tokens past n masked
             float x[4];
