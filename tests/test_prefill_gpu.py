@@ -90,6 +90,36 @@ def test_prefill_deterministic(cuda_device):
     assert torch.equal(la, lb)
 
 
+@pytest.mark.parametrize("page", [1, 16])
+def test_prefill_physical_permutation_invariance(cuda_device, page):
+    """The same logical K/V on other physical pages (slots for page size 1)
+    gives the identical output and LSE: the page-table indexing is exact and
+    the kernel's arithmetic depends on the logical order only."""
+    import paged_kv_flashattention_gb300 as pa
+    p = W.small_problem(91 + page, [300, 17, 0, 1000], [40, 130, 200, 7], num_q_heads=16,
+                        num_kv_heads=4, head_dim=128, page_size=page)
+    d = DeviceProblem(p, cuda_device)
+    d.store()
+    out1, lse1 = d.prefill()
+    m = d.metadata()
+    # the poison page stays last, so unused table entries still point at it
+    perm = np.concatenate([np.random.default_rng(4).permutation(p.num_pages - 1), [p.num_pages - 1]])
+    permt = torch.from_numpy(perm).to(cuda_device)
+    kc2 = torch.empty_like(d.k_cache)
+    vc2 = torch.empty_like(d.v_cache)
+    kc2[permt] = d.k_cache
+    vc2[permt] = d.v_cache
+    tt = p.token_table.astype(np.int64)
+    tt2 = (perm[tt // page] * page + tt % page).astype(np.int32)
+    pt2 = pa.build_page_table(torch.from_numpy(tt2).to(cuda_device), d.table_idx, m.max_seqlen_k, page)
+    lse2 = torch.empty_like(lse1)
+    out2 = pa.prefill(d.q, kc2, vc2, pt2, m.cu_seqlens_q, m.cu_seqlens_k, m.max_seqlen_q,
+                      m.max_seqlen_k, causal=True, scale=p.scale, lse=lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+
+
 def test_decode_via_prefill_matches_decode(cuda_device):
     """A decode batch run through prefill (Lq = 1 per request, cu_seqlens_q =
     arange) agrees with the decode kernel and with the oracle."""
