@@ -270,7 +270,9 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream);
  * kv_chunk keys.  A sequence that spans several ranges gets one partial
  * (O_s, lse_s) per range in the workspace; a second, log-sum-exp combine
  * launch merges them into `out` (it always runs; a row with one partial is
- * copied).  The split layout depends only on the device-side cache_seqlens,
+ * copied).  The combine is launched as a programmatic dependent of the split
+ * kernel: its launch is prepared while the split kernel finishes, and it
+ * waits for that grid's completion before it reads a partial.  The split layout depends only on the device-side cache_seqlens,
  * so it is the same on every call with the same lengths (run-to-run
  * deterministic).
  */
