@@ -245,7 +245,7 @@ typedef struct {
     int32_t page_size;
     int64_t num_pages;
     int32_t causal;              /* 0 or 1 */
-    float scale;                 /* usually 1/sqrt(head_dim) */
+    float scale;                 /* finite and > 0, usually 1/sqrt(head_dim) */
     void *out;                   /* bf16 [total_q, Hq, d] */
     float *lse;                  /* optional fp32 [Hq, lse_stride]; NULL = not written */
     int64_t lse_stride;          /* >= total_q when lse != NULL */
@@ -290,7 +290,7 @@ typedef struct {
     int32_t head_dim;
     int32_t page_size;
     int64_t num_pages;
-    float scale;
+    float scale;                 /* finite and > 0 */
     void *out;                   /* bf16 [num_seqs, Hq, d] */
     float *lse;                  /* optional fp32 [num_seqs, Hq]; NULL = not written */
     void *workspace;             /* device, >= pa_decode_workspace_size(p) bytes */

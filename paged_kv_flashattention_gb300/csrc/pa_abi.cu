@@ -248,7 +248,10 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
     if (p->max_seqlen_q > p->max_seqlen_k && p->max_seqlen_k > 0)
         return fail(PA_ERR_INVALID, "max_seqlen_q %d > max_seqlen_k %d", p->max_seqlen_q, p->max_seqlen_k);
     if (p->causal != 0 && p->causal != 1) return fail(PA_ERR_INVALID, "causal must be 0 or 1");
-    if (!(p->scale == p->scale)) return fail(PA_ERR_INVALID, "scale is NaN");
+    // The prefill softmax takes its row maximum over the raw scores, which is
+    // the maximum of the scaled scores only for scale > 0 (and 0 * -inf on a
+    // masked key would be NaN); decode keeps the same rule.
+    if (!(p->scale > 0.f) || p->scale == INFINITY) return fail(PA_ERR_INVALID, "scale must be finite and > 0");
     if (p->total_q < 0) return fail(PA_ERR_INVALID, "total_q < 0");
     if (p->num_seqs == 0 || p->max_seqlen_q == 0 || p->total_q == 0) return PA_OK;
     const int64_t ncols = ((int64_t)p->max_seqlen_k + p->page_size - 1) / p->page_size;
@@ -280,7 +283,10 @@ static pa_status check_decode(const pa_decode_params *p) {
         return fail(PA_ERR_INVALID, "negative sizes or empty pool");
     if (p->num_seqs > 16384) return fail(PA_ERR_UNSUPPORTED, "more than 16384 sequences in one decode call");
     if (p->kv_chunk < 0 || p->kv_chunk % 16 != 0) return fail(PA_ERR_INVALID, "kv_chunk must be a non-negative multiple of 16");
-    if (!(p->scale == p->scale)) return fail(PA_ERR_INVALID, "scale is NaN");
+    // The prefill softmax takes its row maximum over the raw scores, which is
+    // the maximum of the scaled scores only for scale > 0 (and 0 * -inf on a
+    // masked key would be NaN); decode keeps the same rule.
+    if (!(p->scale > 0.f) || p->scale == INFINITY) return fail(PA_ERR_INVALID, "scale must be finite and > 0");
     if (p->num_pages > (int64_t)INT32_MAX / p->page_size)
         return fail(PA_ERR_UNSUPPORTED, "pool larger than 2^31 slots");
     if (p->kv_dtype != PA_KV_BF16 && p->kv_dtype != PA_KV_FP8_E4M3)

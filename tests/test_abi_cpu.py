@@ -103,6 +103,9 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(causal=2), INVALID),
     (dict(page_table_stride=1), INVALID),
     (dict(scale=float("nan")), INVALID),
+    (dict(scale=0.0), INVALID),
+    (dict(scale=-0.1), INVALID),
+    (dict(scale=float("inf")), INVALID),
     (dict(sliding_window=-3), INVALID),
 ])
 def test_prefill_rejects_before_launch(lib, kw, status):
@@ -122,6 +125,8 @@ def test_prefill_rejects_before_launch(lib, kw, status):
     (dict(kv_dtype=2), INVALID),
     (dict(kv_dtype=1), INVALID),                              # FP8 without scales
     (dict(sliding_window=-1), INVALID),
+    (dict(scale=-0.125), INVALID),
+    (dict(scale=float("inf")), INVALID),
 ])
 def test_decode_rejects_before_launch(lib, kw, status):
     assert _decode(lib, **kw) == status
