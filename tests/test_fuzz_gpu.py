@@ -1,7 +1,7 @@
 """Seeded random parity cases that mix the features the other GPU tests cover
 one at a time: prefill or decode, bf16 or FP8 pools, page size 1 or 16,
 head_dim 64 or 128, GQA groups 1 to 8, sliding windows, causal or not,
-forced split sizes.  Each case is checked against the fp64 oracle with the
+forced split sizes, prefill requests with no new tokens.  Each case is checked against the fp64 oracle with the
 contract's tolerances (max abs <= 2e-2, mean abs <= 1e-3, lse within 2e-3)."""
 import numpy as np
 import pytest
@@ -40,6 +40,8 @@ def _case(seed, big=False):
         c["B"] = min(c["B"], 8)                 # keeps the oracle's share of the test short
         c["cached"] = [int(x) if rng.integers(0, 3) else 0 for x in rng.integers(0, 700 * scale, size=c["B"])]
         c["extend"] = [int(x) for x in rng.integers(1, 300 if not big else 500, size=c["B"])]
+        if c["B"] > 1 and rng.integers(0, 3) == 0:     # a request with no new tokens
+            c["extend"][int(rng.integers(0, c["B"]))] = 0
     return c
 
 
