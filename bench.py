@@ -20,7 +20,7 @@ roofline = the decode pass (split kernel + combine) against measured HBM
            reported beside it.
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
-workload (the reference arm of this build).
+workload (the benchmark's reference arm).
 """
 from __future__ import annotations
 

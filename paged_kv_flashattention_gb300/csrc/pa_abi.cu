@@ -271,7 +271,7 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
     if (p->sliding_window < 0) return fail(PA_ERR_INVALID, "sliding_window must be >= 0");
     if (p->max_ctas < 0) return fail(PA_ERR_INVALID, "max_ctas must be >= 0");
     cudaError_t e = launch_prefill(*p, static_cast<cudaStream_t>(stream));
-    if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "prefill configuration not supported by this build");
+    if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "prefill configuration not supported by this library");
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "prefill launch");
 }
 
