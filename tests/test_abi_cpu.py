@@ -160,6 +160,17 @@ def test_decode_workspace_size_host_only(lib):
     assert 0 < small < n and small >= 64 * 32 * 2 * (64 + 1) * 4
 
 
+@pytest.mark.parametrize("max_k,want", [(1, 64), (1000, 64), (2048, 64), (4096, 128), (5000, 160),
+                                         (32768, 1024)])
+def test_decode_automatic_split(lib, max_k, want):
+    """kv_chunk = 0 takes 1/32 of the longest context, a multiple of 16, at
+    least 64 keys."""
+    from paged_kv_flashattention_gb300 import _lib
+    p = _lib.DecodeParams(num_seqs=8, max_seqlen_k=max_k, num_q_heads=32, num_kv_heads=8,
+                          head_dim=128, page_size=16, num_pages=10000, scale=0.1, kv_chunk=0)
+    assert lib.pa_decode_kv_chunk(ctypes.byref(p)) == want
+
+
 def test_rope_table_host(lib):
     """The host rotary table equals the oracle's fp64 table rounded to fp32
     (within half an fp32 step of values <= 1)."""
