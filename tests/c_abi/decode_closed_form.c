@@ -1,15 +1,19 @@
 /*
  * A plain C program that uses libpa.so through include/pa.h alone (no Python,
  * no C++): it stores the newest token of two sequences with pa_store_kv, then
- * runs pa_decode and pa_decode_noalloc on a case whose answer has a closed form.
+ * runs pa_decode, pa_decode_noalloc and pa_prefill on cases whose answers have
+ * a closed form.
  *
- * Every key of the used pages is the same vector, so all scores of a sequence
- * are equal and attention is the plain mean of its V rows.  V row j of a
- * sequence holds the value j in every element, so the output is (L - 1) / 2
- * everywhere, exactly, and lse = score + ln L, where score = scale * q . k.
- * Unused page-table entries point at a page full of NaN, so any read through a
- * wrong entry shows up in the output.  Splits of 16 keys force the
- * split-and-merge path.
+ * Every key of the used pages is the same vector, so all visible scores of a
+ * query are equal and attention is the plain mean of the visible V rows.  V
+ * row j of a sequence holds the value j in every element.  Decode sees all L
+ * keys: the output is (L - 1) / 2 everywhere, and lse = score + ln L, where
+ * score = scale * q . k.  Prefill of the last Lq keys of each sequence: the
+ * query at position p sees keys 0 .. p, so its output is p / 2 and its lse
+ * score + ln(p + 1).  Unused page-table entries point at a page full of NaN,
+ * so any read through a wrong entry shows up in the output (slots past a
+ * sequence's end inside its last page hold zeros: the prefill reads whole
+ * pages).  Splits of 16 keys force decode's split-and-merge path.
  *
  * Exit status 0 = every check passed.
  */
@@ -33,6 +37,7 @@
 #define STRIDE 3
 
 static const int kLen[B] = {20, 40};
+static const int kLq[B] = {5, 12};          /* prefill: the last Lq keys are the queries */
 static const int kPages[B][STRIDE] = {{3, 1, POISON}, {0, 5, 2}};
 
 static uint16_t bf16(float x) {       /* exact for the small values used here */
@@ -101,8 +106,13 @@ int main(void) {
     const size_t pool_elems = (size_t)PAGES * P * row;
     uint16_t *hk = malloc(pool_elems * 2), *hv = malloc(pool_elems * 2);
     for (size_t i = 0; i < pool_elems; ++i) hk[i] = hv[i] = 0x7FC0;   /* NaN */
-    /* the pages of each sequence: K = 1, V = key index; the last key is left
-       NaN here and written by pa_store_kv below */
+    /* the pages of each sequence: K = 1, V = key index, zeros past the end;
+       the last key is left NaN here and written by pa_store_kv below */
+    for (int b = 0; b < B; ++b)
+        for (int j = kLen[b]; j < (kLen[b] + P - 1) / P * P; ++j) {
+            const size_t slot = (size_t)kPages[b][j / P] * P + j % P;
+            for (size_t e = 0; e < row; ++e) hk[slot * row + e] = hv[slot * row + e] = 0;
+        }
     for (int b = 0; b < B; ++b)
         for (int j = 0; j + 1 < kLen[b]; ++j) {
             const size_t slot = (size_t)kPages[b][j / P] * P + j % P;
@@ -196,11 +206,83 @@ int main(void) {
         CK(cudaMemcpy(hlse, lse, sizeof hlse, cudaMemcpyDeviceToHost));
         bad += check(hout, hlse, p.scale, pass == 0 ? "pa_decode" : "pa_decode_noalloc");
     }
+
+    /* prefill / extend of the last Lq keys of each sequence */
+    enum { TQ = 5 + 12 };
+    int32_t hcuq[B + 1] = {0, kLq[0], kLq[0] + kLq[1]}, hcuk[B + 1] = {0, kLen[0], kLen[0] + kLen[1]};
+    uint16_t hqp[TQ * HQ * D], houtp[TQ * HQ * D];
+    float hlsep[HQ * TQ];
+    for (int i = 0; i < TQ * HQ * D; ++i) hqp[i] = bf16(0.5f);
+    void *qp, *outp;
+    int32_t *cuq, *cuk;
+    float *lsep;
+    CK(cudaMalloc(&qp, sizeof hqp));
+    CK(cudaMalloc(&outp, sizeof houtp));
+    CK(cudaMalloc((void **)&lsep, sizeof hlsep));
+    CK(cudaMalloc((void **)&cuq, sizeof hcuq));
+    CK(cudaMalloc((void **)&cuk, sizeof hcuk));
+    CK(cudaMemcpy(qp, hqp, sizeof hqp, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(cuq, hcuq, sizeof hcuq, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(cuk, hcuk, sizeof hcuk, cudaMemcpyHostToDevice));
+    CK(cudaMemset(outp, 0xFF, sizeof houtp));
+    CK(cudaMemset(lsep, 0xFF, sizeof hlsep));
+    pa_prefill_params f;
+    memset(&f, 0, sizeof f);
+    f.q = qp;
+    f.k_cache = k_cache;
+    f.v_cache = v_cache;
+    f.page_table = pt;
+    f.page_table_stride = STRIDE;
+    f.total_q = TQ;
+    f.cu_seqlens_q = cuq;
+    f.cu_seqlens_k = cuk;
+    f.num_seqs = B;
+    f.max_seqlen_q = 12;
+    f.max_seqlen_k = 40;
+    f.num_q_heads = HQ;
+    f.num_kv_heads = HKV;
+    f.head_dim = D;
+    f.page_size = P;
+    f.num_pages = PAGES;
+    f.causal = 1;
+    f.scale = 0.125f;
+    f.out = outp;
+    f.lse = lsep;
+    f.lse_stride = TQ;
+    f.kv_dtype = PA_KV_BF16;
+    PK(pa_prefill(&f, NULL));
+    int32_t bits = 0;
+    PK(pa_device_error(&bits, NULL));
+    if (bits != 0) {
+        fprintf(stderr, "prefill: device error bits %d\n", bits);
+        return 1;
+    }
+    CK(cudaMemcpy(houtp, outp, sizeof houtp, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(hlsep, lsep, sizeof hlsep, cudaMemcpyDeviceToHost));
+    const float score = f.scale * (float)D * 0.5f;
+    for (int b = 0; b < B; ++b)
+        for (int i = 0; i < kLq[b]; ++i) {
+            const int t = hcuq[b] + i, pos = kLen[b] - kLq[b] + i;
+            for (int h = 0; h < HQ; ++h) {
+                for (int c = 0; c < D; ++c) {
+                    const float got = from_bf16(houtp[((size_t)t * HQ + h) * D + c]);
+                    if (!(fabsf(got - 0.5f * (float)pos) <= 1e-2f)) {
+                        if (bad < 5) fprintf(stderr, "prefill: out[%d,%d,%d] = %g, want %g\n", t, h, c, got, 0.5f * pos);
+                        ++bad;
+                    }
+                }
+                const float l = hlsep[h * TQ + t], want = score + logf((float)(pos + 1));
+                if (!(fabsf(l - want) <= 2e-3f)) {
+                    if (bad < 5) fprintf(stderr, "prefill: lse[%d,%d] = %g, want %g\n", h, t, l, want);
+                    ++bad;
+                }
+            }
+        }
     if (bad) {
         fprintf(stderr, "%d mismatches\n", bad);
         return 1;
     }
-    printf("ok: store + decode (split 16) + decode_noalloc through the C ABI\n");
+    printf("ok: store + decode (split 16) + decode_noalloc + prefill through the C ABI\n");
     free(hk);
     free(hv);
     return 0;

@@ -1,8 +1,8 @@
 """The C ABI from plain C: tests/c_abi/decode_closed_form.c includes only
 include/pa.h, links libpa.so and the CUDA runtime, stores tokens and runs split
-decode (pa_decode and pa_decode_noalloc) on a case with a closed-form answer
-(equal keys: the output is the mean of the V rows), and exits 0 when every
-element matches."""
+decode (pa_decode and pa_decode_noalloc) and causal extend (pa_prefill) on
+cases with closed-form answers (equal keys: the output is the mean of the
+visible V rows), and exits 0 when every element matches."""
 import glob
 import os
 import shutil
