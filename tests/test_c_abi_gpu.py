@@ -1,4 +1,4 @@
-"""The C ABI from plain C: tests/c_abi/decode_closed_form.c includes only
+"""The C ABI from plain C: tests/c_abi/abi_closed_form.c includes only
 include/pa.h, links libpa.so and the CUDA runtime, stores tokens and runs split
 decode (pa_decode and pa_decode_noalloc) and causal extend (pa_prefill) on
 cases with closed-form answers (equal keys: the output is the mean of the
@@ -22,7 +22,7 @@ def _cuda_home():
     return os.environ.get("CUDA_HOME", "/usr/local/cuda")
 
 
-def test_c_program_decode_closed_form(cuda_device, tmp_path):
+def test_c_program_abi_closed_form(cuda_device, tmp_path):
     import paged_kv_flashattention_gb300 as pa     # the in-tree libpa.so is built
     assert pa.abi_version() == 1
     gcc = shutil.which("gcc") or shutil.which("cc")
@@ -33,10 +33,10 @@ def test_c_program_decode_closed_form(cuda_device, tmp_path):
                if os.path.exists(os.path.join(d, "libcudart.so"))]
     assert libdirs, f"libcudart.so not found under {cuda}"
     pkg = os.path.join(ROOT, "paged_kv_flashattention_gb300")
-    exe = str(tmp_path / "decode_closed_form")
+    exe = str(tmp_path / "abi_closed_form")
     cmd = [gcc, "-std=c99", "-O2", "-Wall", "-Wextra", "-Werror",
            "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include"),
-           os.path.join(ROOT, "tests", "c_abi", "decode_closed_form.c"),
+           os.path.join(ROOT, "tests", "c_abi", "abi_closed_form.c"),
            "-L", pkg, "-lpa", "-L", libdirs[0], "-lcudart", "-lm",
            f"-Wl,-rpath,{pkg}", f"-Wl,-rpath,{libdirs[0]}", "-o", exe]
     r = subprocess.run(cmd, capture_output=True, text=True)
