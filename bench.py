@@ -143,6 +143,9 @@ class MixedBatch:
         self.v_cache = torch.empty(shape, dtype=torch.bfloat16, device=dev)
         W.fill_normal_device(self.k_cache, W.SEED_BASE + 50 + seed_offset)
         W.fill_normal_device(self.v_cache, W.SEED_BASE + 51 + seed_offset)
+        # never-written slots past each sequence's end in its last page: NaN
+        W.poison_tails_device(d, self.k_cache, self.v_cache)
+        W.poison_tails_device(p, self.k_cache, self.v_cache)
         g = torch.Generator(device=dev)
         g.manual_seed(W.SEED_BASE + 52 + seed_offset)
         Tn = d.num_new_tokens + p.num_new_tokens
@@ -217,6 +220,51 @@ class MixedBatch:
         return ev
 
 
+def _pct(sorted_vals, q):
+    """q-th percentile (nearest rank) of an ascending list."""
+    if not sorted_vals:
+        return float("nan")
+    i = min(len(sorted_vals) - 1, max(0, int(math.ceil(q / 100.0 * len(sorted_vals))) - 1))
+    return float(sorted_vals[i])
+
+
+# The other workloads of the path, each timed on its own in the default run
+# (config name -> microbenchmark cases): tiny decode, Llama-3.2-1B-shaped
+# decode, varlen causal prefill 16 x 512, extend with a partial prefix hit at
+# page size 16 and 1, the store of the 16 x 512 batch, and the FP8 variants.
+CONFIG_CASES = {
+    "tiny_decode": ["tiny_decode"],
+    "llama32_1b_decode": ["llama32_1b_decode", "llama32_1b_decode_fp8"],
+    "varlen_prefill_16x512": ["varlen_prefill_16x512", "varlen_prefill_16x512_fp8", "store_16x512",
+                              "rope_store_16x512"],
+    "extend_partial_hit": ["extend_partial_hit_p16", "extend_partial_hit_p1", "extend_partial_hit_p16_fp8",
+                           "extend_partial_hit_p1_fp8"],
+    "decode_64seq_logu": ["decode_64seq_logu", "decode_64seq_logu_fp8"],
+}
+
+
+def config_block(dev, peaks, args):
+    """Median / p95 time, rate and fraction of the measured peak of every
+    case in CONFIG_CASES (prefill also against its attainable roofline
+    max(FLOP / peak, bytes / HBM))."""
+    import torch
+    out = {}
+    for cfg, cases in CONFIG_CASES.items():
+        out[cfg] = {}
+        for name in cases:
+            r = time_case(name, dev, args.config_steps, 5)
+            if r["unit"] == "TFLOP/s":
+                r["frac_bf16"] = round(r["rate"] / peaks["bf16_tflops"], 4)
+                t_att = max(r["work"] / (peaks["bf16_tflops"] * 1e12), r["bytes"] / (peaks["hbm_gbs"] * 1e9))
+                r["attainable_us"] = round(t_att * 1e6, 2)
+                r["frac_attainable"] = round(t_att * 1e6 / r["us_median"], 4)
+            else:
+                r["frac_hbm"] = round(r["rate"] / peaks["hbm_gbs"], 4)
+            out[cfg][name] = r
+            torch.cuda.empty_cache()
+    return out
+
+
 def max_over_ranks(value: float, world: int, device=None) -> float:
     """The slowest rank's time: every rank contributes its own measurement and
     all receive the maximum (a plain all-reduce; nothing of the attention
@@ -264,6 +312,26 @@ def run_gpu(args):
         torch.cuda.synchronize()
     barrier()
     total_ms = start.elapsed_time(end)
+    # ---- per-step times: events around every step, back to back (median,
+    # p95), then the same with L2 flushed before every step (a 512 MiB
+    # write, outside the events)
+    def per_step(flush=None):
+        pairs = []
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            mb.step()
+            b.record()
+            pairs.append((a, b))
+        torch.cuda.synchronize()
+        return sorted(a.elapsed_time(b) for a, b in pairs)
+    step_ms = per_step()
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    step_ms_flushed = per_step(flush_buf)
+    del flush_buf
+    barrier()
     # ---- the same steps with the phases in sequence, for the per-kernel
     # numbers (events recorded between the launches on the same stream)
     phase = {"store_meta": [], "prefill": [], "decode": []}
@@ -390,10 +458,19 @@ def run_gpu(args):
         "e2e": {"value": round(world * mb.step_bytes / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
+        "step_ms": {"median": round(_pct(step_ms, 50), 4), "p95": round(_pct(step_ms, 95), 4),
+                    "note": "events around every step, back to back"},
+        "l2_flushed": {"ms_median": round(_pct(step_ms_flushed, 50), 4),
+                       "ms_p95": round(_pct(step_ms_flushed, 95), 4),
+                       "value": round(world * mb.step_bytes / (_pct(step_ms_flushed, 50) * 1e-3) / 1e9, 1),
+                       "unit": "GB/s", "flush": "512 MiB device write before every step, outside the events"},
         "gpu_launches": mb.launches_per_step * args.steps,
         "clocks": clk.summary(),
         "device_error": dev_err,
     }
+    if rank == 0 and not args.no_configs:
+        line["configs"] = config_block(dev, peaks, args)
+        line["device_error"] |= device_error()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(mb, args.cpu_seconds)
     if rank == 0:
@@ -426,6 +503,22 @@ def oracle_decode_sample(dec: W.Problem, seqs, fetch_pages, q_rows):
     return dt, int(L.sum()) * dec.num_kv_heads * dec.head_dim * 2 * 2
 
 
+def decode_sample(dec: W.Problem, cap_bytes: float = 2e9):
+    """The fixed sample of the mixed batch's decode sequences that both CPU
+    timings use (the cpu_baseline leg and the reference arm): a seeded
+    permutation of the 256 sequences, taken in order until about cap_bytes
+    of K/V."""
+    order = np.random.default_rng(5).permutation(dec.num_seqs)
+    seqs, acc = [], 0
+    for b in order:
+        nb = int(dec.device_len[b]) * dec.num_kv_heads * dec.head_dim * 4
+        if seqs and acc + nb > cap_bytes:
+            break
+        seqs.append(int(b))
+        acc += nb
+    return seqs
+
+
 def cpu_baseline(mb: MixedBatch, target_s: float):
     """The fp64 oracle on the host cores, on a bounded sample of the decode
     batch (the step's dominant work), in the same unit (GB/s of K/V)."""
@@ -439,17 +532,10 @@ def cpu_baseline(mb: MixedBatch, target_s: float):
         v = mb.v_cache.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
         return k, v
 
-    order = np.random.default_rng(5).permutation(dec.num_seqs)
     qh = mb.q_dec.view(torch.int16).cpu().numpy().view(np.uint16)
-    # a fixed sample of the decode batch (~2 GB of K/V), run repeatedly until
-    # about target_s seconds of oracle time have been spent
-    seqs, acc = [], 0
-    for b in order:
-        nb = int(dec.device_len[b]) * dec.num_kv_heads * dec.head_dim * 4
-        if seqs and acc + nb > 2e9:
-            break
-        seqs.append(int(b))
-        acc += nb
+    # the sample (~2 GB of K/V), run repeatedly until about target_s seconds
+    # of oracle time have been spent
+    seqs = decode_sample(dec)
     total_t, total_b, reps = 0.0, 0, 0
     while total_t < target_s and reps < 100:
         dt, by = oracle_decode_sample(dec, seqs, fetch, qh[seqs])
@@ -463,8 +549,8 @@ def cpu_baseline(mb: MixedBatch, target_s: float):
 
 
 def run_reference(args):
-    """Reference arm: the fp64 CPU oracle, each step a bounded sample of the
-    workload's decode batch (rank 0 only)."""
+    """Reference arm: the fp64 CPU oracle, each step the same decode sample
+    as the cpu_baseline leg (rank 0 only)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
@@ -473,7 +559,7 @@ def run_reference(args):
     dec = cfg["decode"]
     rng = np.random.default_rng(W.SEED_BASE + 60)
     # host pool holding only the sampled sequences' pages (seeded N(0,1) values)
-    seqs = [int(b) for b in np.argsort(dec.device_len)[:args.ref_seqs]]
+    seqs = decode_sample(dec, args.ref_cap_gb * 1e9)
     pages = sorted(set(p for b in seqs for p in dec.meta["page_lists"][b]))
     shape = (len(pages), dec.page_size, dec.num_kv_heads, dec.head_dim)
     kc, vc = W.normal_bf16(rng, shape), W.normal_bf16(rng, shape)
@@ -490,7 +576,7 @@ def run_reference(args):
         times.append(dt)
     ms = 1e3 * sum(times) / len(times)
     value = nbytes / (ms * 1e-3) / 1e9
-    sample = (f"fp64 oracle decode of the {len(seqs)} shortest of the 256 decode sequences "
+    sample = (f"fp64 oracle decode of {len(seqs)} of the 256 decode sequences, the cpu_baseline sample "
               f"({nbytes / 1e9:.3f} GB of K/V per step)")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
@@ -537,15 +623,15 @@ def micro_problem(name):
     return p, kernel
 
 
-def run_micro(args):
-    """One kernel on one workload, as in a microbenchmark manifest: warm-up,
-    then `steps` launches timed one by one with CUDA events (median, p95)."""
+def prepare_case(name, dev):
+    """Device inputs of one microbenchmark case.  Returns (fn, work, unit,
+    extra): fn() launches the kernel(s) once, work is the algorithmic bytes
+    or FLOPs of one launch, extra holds derived facts of the case."""
     import torch
     import paged_kv_flashattention_gb300 as pa
     from paged_kv_flashattention_gb300 import metadata
-    dev = torch.device("cuda", 0)
-    p, kernel = micro_problem(args.micro)
-    fp8 = args.micro.endswith("_fp8")
+    p, kernel = micro_problem(name)
+    fp8 = name.endswith("_fp8")
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
     q = to(p.q)
     kn, vn = to(p.k_new), to(p.v_new)
@@ -563,6 +649,7 @@ def run_micro(args):
                          torch.from_numpy(p.table_idx).to(dev), p.page_size)
     Hkv, D, Hq = p.num_kv_heads, p.head_dim, p.num_q_heads
     out = torch.empty_like(q)
+    extra = {"kernel": kernel, "page_size": p.page_size, "kv": "fp8_e4m3" if fp8 else "bf16"}
     if kernel == "decode":
         ws = torch.empty(max(16, pa.decode_workspace_size(q.shape, kc, m.max_seqlen_k)),
                          dtype=torch.uint8, device=dev)
@@ -570,14 +657,19 @@ def run_micro(args):
                                scale=p.scale, out=out, workspace=ws, **scales)
         work = int(p.device_len.astype(np.int64).sum()) * Hkv * D * 2 * kc.element_size() + 2 * q.numel() * 2
         unit = "GB/s"
+        extra["seqs"] = p.num_seqs
     elif kernel == "prefill":
+        sched = torch.zeros(2, dtype=torch.int32, device=dev)
         fn = lambda: pa.prefill(q, kc, vc, m.page_table, m.cu_seqlens_q, m.cu_seqlens_k,
                                 m.max_seqlen_q, m.max_seqlen_k, causal=p.causal, scale=p.scale, out=out,
-                                **scales)
+                                scheduler=sched, **scales)
         off = p.cached_len.astype(np.int64)
         E = p.extend_len.astype(np.int64)
         work = 4 * D * Hq * int(np.sum(E * off + E * (E + 1) // 2))
         unit = "TFLOP/s"
+        # bytes a perfect kernel moves: Q read, O written, each request's K/V read once
+        extra["bytes"] = 2 * q.numel() * 2 + int(p.device_len.astype(np.int64).sum()) * Hkv * D * 2 * kc.element_size()
+        extra["tokens"] = int(E.sum())
     elif kernel == "rope":
         table = pa.rope_cos_sin_table(int(p.device_len.max()) + 1, D, 10000.0).to(dev)
         pos = torch.from_numpy(np.concatenate([np.arange(c, c + e) for c, e in zip(p.cached_len, p.extend_len)])
@@ -590,11 +682,19 @@ def run_micro(args):
         fn = lambda: pa.store_kv(kn, vn, sm, kc, vc)
         work = 2 * 2 * kn.numel() * 2
         unit = "GB/s"
-    for _ in range(args.warmup):
+    return fn, work, unit, extra
+
+
+def time_case(name, dev, steps, warmup):
+    """One kernel on one workload, as in a microbenchmark manifest: warm-up,
+    then replays of a captured CUDA graph of the call (so host launch gaps do
+    not sit between the events), timed in groups of 10 back-to-back replays;
+    median and p95 over the groups."""
+    import torch
+    fn, work, unit, extra = prepare_case(name, dev)
+    for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
-    # Replay the call from a captured CUDA graph so host launch overhead does
-    # not sit between the events; each replay is timed on its own.
     graph = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -607,9 +707,7 @@ def run_micro(args):
     for _ in range(3):
         graph.replay()
     torch.cuda.synchronize()
-    # back-to-back replays between two events (mean), in groups of 10 so a
-    # median and p95 over groups can be reported as well
-    groups = max(1, args.steps // 10)
+    groups = max(1, steps // 10)
     ts = []
     for _ in range(groups):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -623,9 +721,21 @@ def run_micro(args):
     med = us[len(us) // 2]
     p95 = us[min(len(us) - 1, int(0.95 * len(us)))]
     rate = work / (med * 1e-6) / (1e12 if unit == "TFLOP/s" else 1e9)
-    print(json.dumps({"micro": args.micro, "kernel": kernel, "us_median": round(med, 2),
-                      "us_p95": round(p95, 2), "rate": round(rate, 1), "unit": unit,
-                      "work": work, "iters": args.steps, "warmup": args.warmup}), flush=True)
+    res = {"kernel": extra["kernel"], "us_median": round(med, 2), "us_p95": round(p95, 2), "rate": round(rate, 1),
+           "unit": unit, "work": work, "iters": groups * 10}
+    for k in ("page_size", "kv", "seqs", "tokens", "bytes"):
+        if k in extra:
+            res[k] = extra[k]
+    del graph
+    torch.cuda.synchronize()
+    return res
+
+
+def run_micro(args):
+    import torch
+    dev = torch.device("cuda", 0)
+    r = time_case(args.micro, dev, args.steps, args.warmup)
+    print(json.dumps({"micro": args.micro, **r, "warmup": args.warmup}), flush=True)
 
 
 def main(argv=None):
@@ -639,7 +749,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-sms", type=int, default=12,
                     help="SMs the prefill gets while decode runs beside it (0 = one after the other)")
-    ap.add_argument("--ref-seqs", type=int, default=24, help="decode sequences per reference step")
+    ap.add_argument("--ref-cap-gb", type=float, default=2.0,
+                    help="K/V bytes of the decode sample the reference arm times per step (the "
+                         "cpu_baseline leg's sample at the default)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config block (configs 1-4 and FP8 variants timed one by one)")
+    ap.add_argument("--config-steps", type=int, default=100, help="timed launches per config case")
     ap.add_argument("--micro", choices=sorted(MICRO_CASES), default=None,
                     help="time one kernel on one workload instead of the full step")
     args = ap.parse_args(argv)

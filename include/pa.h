@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 
 typedef enum {
     PA_OK = 0,
@@ -221,12 +221,17 @@ pa_status pa_build_page_table(const int32_t *token_table, int64_t token_table_st
  *   lse[h * lse_stride + t] = ln sum_j exp(scale * q . K_j)   (optional)
  * The score matrix never leaves the chip (tiled, online softmax; [T] s.11-12).
  * max_seqlen_q / max_seqlen_k must bound every request's Lq / Lk.
- * Work is handed to persistent CTAs by a pair of device counters that the
- * library owns (1024 pairs per device, taken in turn by successive calls and
- * left at zero by every launch).  Calls whose kernels may run at the same
- * time on one device (different streams) must therefore be fewer than 1024
- * pa_prefill calls apart; calls on one stream never conflict.
+ * Work is handed to persistent CTAs by two device counters in the caller's
+ * `scheduler` array (PA_PREFILL_SCHEDULER_INTS int32, zero before its first
+ * use; every launch that completes leaves them at zero again, so one array
+ * serves any number of calls that run one after the other, e.g. on one
+ * stream or in one captured graph).  Launches that may run at the same time
+ * (calls on different streams, graph replays beside other prefill work) each
+ * need their own array: two launches sharing one would skip or repeat work
+ * items.  After a launch that raised PA_DEVERR_TIMEOUT the counters may be
+ * left non-zero: clear the array before using it again.
  */
+#define PA_PREFILL_SCHEDULER_INTS 2
 typedef struct {
     const void *q;               /* bf16 [total_q, Hq, d] */
     const void *k_cache;         /* bf16 [num_pages, page_size, Hkv, d] */
@@ -257,6 +262,9 @@ typedef struct {
     int32_t max_ctas;            /* 0 = one persistent CTA per SM; n > 0: at most n CTAs
                                     (each holds a whole SM), leaving the other SMs to a
                                     concurrent launch, e.g. pa_decode on another stream */
+    int32_t *scheduler;          /* device int32 [PA_PREFILL_SCHEDULER_INTS], owned by the
+                                    caller: zero before its first use, left zero by every
+                                    completed launch; required (NULL = PA_ERR_INVALID) */
 } pa_prefill_params;
 
 pa_status pa_prefill(const pa_prefill_params *p, void *stream);
@@ -363,16 +371,6 @@ pa_status pa_decode_noalloc(const pa_decode_params *p, void *stream);
 pa_status pa_lse_combine(const float *o_partial, const float *lse_partial,
                          const int32_t *splits_per_row, int32_t num_rows, int32_t max_splits,
                          int32_t head_dim, void *out, float *lse_out, void *stream);
-
-/*
- * pa_selftest_exp2 - evaluate, on the device, the 2^x approximation the
- * prefill softmax uses for a quarter of its exponentials (2^round(x) times a
- * cubic fitted to 2^f on [-1/2, 1/2], relative error < 8e-5 for x >= -125),
- * so tests can compare it with CUDA's exp2f.  ([T] s.12 defines the
- * exponentials; the approximation is this library's.)
- * x, y: device fp32 [n]; y[i] = approximation of 2^x[i].
- */
-pa_status pa_selftest_exp2(const float *x, float *y, int64_t n, void *stream);
 
 #ifdef __cplusplus
 }

@@ -33,7 +33,7 @@ class PrefillParams(ctypes.Structure):
         ("page_size", c_i32), ("num_pages", c_i64), ("causal", c_i32), ("scale", c_f32),
         ("out", c_p), ("lse", c_p), ("lse_stride", c_i64),
         ("kv_dtype", c_i32), ("k_scale", c_p), ("v_scale", c_p), ("sliding_window", c_i32),
-        ("max_ctas", c_i32),
+        ("max_ctas", c_i32), ("scheduler", c_p),
     ]
 
 
@@ -78,7 +78,6 @@ SIGNATURES = {
     "pa_decode": (ctypes.c_int, [ctypes.POINTER(DecodeParams), c_p]),
     "pa_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(DecodeParams), c_p]),
     "pa_lse_combine": (ctypes.c_int, [c_p, c_p, c_p, c_i32, c_i32, c_i32, c_p, c_p, c_p]),
-    "pa_selftest_exp2": (ctypes.c_int, [c_p, c_p, c_i64, c_p]),
 }
 
 

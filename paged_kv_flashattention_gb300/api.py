@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import ctypes
 import math
+import threading
 
 import numpy as np
 import torch
@@ -244,17 +245,43 @@ def _pool_geometry(k_cache: torch.Tensor, v_cache: torch.Tensor, page_size: int 
     return int(num_pages), int(P), int(Hkv), int(d)
 
 
+# Zeroed scheduler arrays of pa_prefill, one per (device, stream): launches on
+# one stream run one after the other, so they can share one array (each
+# launch leaves it at zero); launches on different streams get their own.
+_sched_lock = threading.Lock()
+_sched_arrays: dict = {}
+PA_PREFILL_SCHEDULER_INTS = 2
+
+
+def prefill_scheduler(device=None, stream=None) -> torch.Tensor:
+    """The cached zeroed int32 [2] scheduler array for (device, stream):
+    the default of ``prefill(scheduler=None)``.  Create it before capturing a
+    CUDA graph that calls prefill on that stream."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    key = (dev.index, int(stream.cuda_stream))
+    with _sched_lock:
+        t = _sched_arrays.get(key)
+        if t is None:
+            t = torch.zeros(PA_PREFILL_SCHEDULER_INTS, dtype=torch.int32, device=dev)
+            _sched_arrays[key] = t
+        return t
+
+
 def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
             cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int,
             max_seqlen_k: int, *, causal: bool = True, scale: float | None = None,
             page_size: int | None = None, out: torch.Tensor | None = None,
             lse: torch.Tensor | None = None, k_scale: torch.Tensor | None = None,
             v_scale: torch.Tensor | None = None, sliding_window: int = 0,
-            max_ctas: int = 0) -> torch.Tensor:
+            max_ctas: int = 0, scheduler: torch.Tensor | None = None) -> torch.Tensor:
     """Varlen prefill / extend attention.  q: bf16 [total_q, Hq, d];
     returns out bf16 [total_q, Hq, d]; lse (optional) fp32 [Hq, total_q].
     Pools are bf16, or E4M3 codes (uint8 / float8_e4m3fn) with fp32
-    per-KV-head ``k_scale`` and ``v_scale``."""
+    per-KV-head ``k_scale`` and ``v_scale``.  ``scheduler`` is the int32 [2]
+    work-counter array of the launch (zero between launches); by default the
+    array cached for the current stream (``prefill_scheduler``)."""
     dev = q.device
     num_pages, P, Hkv, d = _pool_geometry(k_cache, v_cache, page_size)
     _need(q, "q", torch.bfloat16, dev)
@@ -277,6 +304,11 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
         _need(lse, "lse", torch.float32, dev, contiguous=False)
         if lse.dim() != 2 or lse.shape[0] != Hq or lse.stride(1) != 1:
             raise ValueError("lse must be [Hq, >= total_q] with unit inner stride")
+    if scheduler is None:
+        scheduler = prefill_scheduler(dev)
+    _need(scheduler, "scheduler", torch.int32, dev)
+    if scheduler.numel() < PA_PREFILL_SCHEDULER_INTS:
+        raise ValueError("scheduler must hold 2 int32")
     p = _lib.PrefillParams(
         q=_ptr(q), k_cache=_ptr(k_cache), v_cache=_ptr(v_cache), page_table=_ptr(page_table),
         page_table_stride=page_table.stride(0), total_q=total_q, cu_seqlens_q=_ptr(cu_seqlens_q),
@@ -287,7 +319,7 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
         lse=_ptr(lse), lse_stride=(lse.stride(0) if lse is not None else 0), kv_dtype=kvd,
         k_scale=_ptr(k_scale) if kvd == PA_KV_FP8_E4M3 else None,
         v_scale=_ptr(v_scale) if kvd == PA_KV_FP8_E4M3 else None, sliding_window=int(sliding_window),
-        max_ctas=int(max_ctas))
+        max_ctas=int(max_ctas), scheduler=_ptr(scheduler))
     lib = _lib.load()
     _check(lib.pa_prefill(ctypes.byref(p), _stream(q)), lib)
     return out

@@ -270,6 +270,8 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
         return fail(PA_ERR_INVALID, "FP8 pools need k_scale and v_scale");
     if (p->sliding_window < 0) return fail(PA_ERR_INVALID, "sliding_window must be >= 0");
     if (p->max_ctas < 0) return fail(PA_ERR_INVALID, "max_ctas must be >= 0");
+    if (p->scheduler == nullptr) return fail(PA_ERR_INVALID, "scheduler (device int32[2], zero-initialised) is NULL");
+    if ((reinterpret_cast<uintptr_t>(p->scheduler) & 7u) != 0) return fail(PA_ERR_INVALID, "scheduler must be 8-byte aligned");
     cudaError_t e = launch_prefill(*p, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "prefill configuration not supported by this library");
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "prefill launch");
@@ -296,6 +298,16 @@ static pa_status check_decode(const pa_decode_params *p) {
     if (p->sliding_window < 0) return fail(PA_ERR_INVALID, "sliding_window must be >= 0");
     if (p->max_ctas < 0) return fail(PA_ERR_INVALID, "max_ctas must be >= 0");
     if (p->overlap_previous != 0 && p->overlap_previous != 1) return fail(PA_ERR_INVALID, "overlap_previous must be 0 or 1");
+    // The split layout adds up the sequences' (window-clipped) lengths over
+    // the KV-head groups in 32-bit integers on the device; sequences that
+    // share prefix pages can reach sums beyond that, so bound them here.
+    const int64_t eff = (p->sliding_window > 0 && p->sliding_window < p->max_seqlen_k) ? p->sliding_window
+                                                                                       : p->max_seqlen_k;
+    const int64_t groups = p->num_kv_heads / plan_decode(*p).heads_per_cta;
+    if ((int64_t)p->num_seqs * eff * groups > (int64_t)INT32_MAX)
+        return fail(PA_ERR_UNSUPPORTED,
+                    "num_seqs * max_seqlen_k * KV-head groups = %lld exceeds 2^31 - 1 keys in one decode call",
+                    (long long)((int64_t)p->num_seqs * eff * groups));
     return PA_OK;
 }
 
@@ -351,15 +363,6 @@ pa_status pa_decode_noalloc(const pa_decode_params *p, void *stream) {
     q.workspace = scratch;
     q.workspace_bytes = scratch ? kDecodeNoAllocScratchBytes : 0;
     return pa_decode(&q, stream);
-}
-
-pa_status pa_selftest_exp2(const float *x, float *y, int64_t n, void *stream) {
-    g_last_error[0] = 0;
-    if (n < 0) return fail(PA_ERR_INVALID, "n < 0");
-    if (n == 0) return PA_OK;
-    if (!x || !y) return fail(PA_ERR_INVALID, "NULL pointer");
-    cudaError_t e = launch_exp2_selftest(x, y, n, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? PA_OK : cuda_fail(e, "exp2 self-test launch");
 }
 
 pa_status pa_lse_combine(const float *o_partial, const float *lse_partial, const int32_t *splits_per_row,

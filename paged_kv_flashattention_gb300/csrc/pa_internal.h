@@ -46,7 +46,6 @@ cudaError_t launch_lse_combine(const float *o_partial, const float *lse_partial,
                                cudaStream_t stream);
 
 cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream);
-cudaError_t launch_exp2_selftest(const float *x, float *y, int64_t n, cudaStream_t stream);
 
 int num_sms();
 

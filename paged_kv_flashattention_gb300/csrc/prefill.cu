@@ -38,18 +38,19 @@
 //     with a tree of independent maxima, updates the running maximum lazily
 //     (only when the tile maximum exceeds it by more than 8 in log2 units;
 //     then O_k in TMEM is rescaled), computes p = 2^(s*scale*log2 e - m) with
-//     packed f32x2 FMAs and the MUFU unit (a cubic on the FMA pipe can take a
-//     share of the exponentials, kPolyEvery), writes P as bf16 over its S
-//     columns with tcgen05.st, and at the
-//     end normalises O and writes bf16 output and the natural-log LSE.
+//     packed f32x2 FMAs and the MUFU unit, writes P as bf16 over its S
+//     columns with tcgen05.st, and at the end normalises O and writes bf16
+//     output and the natural-log LSE.
 // TMEM (512 columns): S_k at [128k, 128k+128), O_k at [256 + 128k, +d).
 //
 // FP8 pools (E4M3 codes with a scale per KV head; the first page lists FP8 /
 // quantized KV as a dispatch axis, section 19): tcgen05 kind::f16 needs 16-bit
-// operands on both sides, so the E4M3 tiles land in a separate ring (one
-// byte per element, no swizzle) and the two otherwise idle warps of the
-// control warpgroup widen them exactly to f16 into the swizzled layout the
-// MMA reads, and turn each item's Q tiles in place into f16 q * k_scale.
+// operands on both sides, so the E4M3 tiles are loaded one byte per element
+// without swizzle (at d = 128 into the upper half of the f16 slot they are
+// widened into, in place; at d = 64 into a separate landing ring) and the two
+// otherwise idle warps of the control warpgroup widen them exactly to f16 in
+// the swizzled layout the MMA reads, and turn each item's Q tiles in place
+// into f16 q * k_scale.
 // The MMAs then run with f16 operands (P is written to TMEM as f16) and the
 // epilogue multiplies by v_scale.
 #include <cuda.h>
@@ -70,10 +71,6 @@ namespace {
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per step
 constexpr float kLazy = 8.0f;
-// Every kPolyEvery-th pair of exponentials is computed by the FMA-pipe cubic
-// instead of the MUFU unit (0 = never).  Measured on the extend workload,
-// all-MUFU was faster while the K/V loads still limit the kernel.
-constexpr int kPolyEvery = 0;
 
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     uint64_t ai = *reinterpret_cast<uint64_t *>(&a), bi = *reinterpret_cast<uint64_t *>(&b), r;
@@ -85,24 +82,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
-}
-
-// 2^x on the FMA pipe for two values: 2^x = 2^n * p(x - n), n = round(x).
-// round() adds 1.5 * 2^23 in fp32 (the sum's low mantissa bits hold n) and
-// 2^n is applied by adding n << 23 to p's bits.  p is a cubic fitted to 2^f
-// on [-1/2, 1/2] (relative error < 8e-5; exp2_poly_fit.py).  x is clamped at
-// -125 so the result stays a normal float (2^-125 is zero for bf16 P).
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 t = add2(x, make_float2(12582912.f, 12582912.f));
-    const float2 n = add2(t, make_float2(-12582912.f, -12582912.f));
-    const float2 f = add2(x, make_float2(-n.x, -n.y));
-    float2 p = ffma2(make_float2(0.0551705262f, 0.0551705262f), f, make_float2(0.24260831f, 0.24260831f));
-    p = ffma2(p, f, make_float2(0.69326092f, 0.69326092f));
-    p = ffma2(p, f, make_float2(0.999928252f, 0.999928252f));
-    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
 }
 
 struct PrefillArgs {
@@ -129,7 +108,7 @@ struct PrefillArgs {
     int32_t num_virtual;          // max_tiles * num_seqs * (Hq / T) work-item slots
     const float *k_scale;         // FP8 pools: per-KV-head scales
     const float *v_scale;
-    int32_t *sched;               // [0] next item, [1] CTAs finished; both 0 between launches
+    int32_t *sched;               // caller's [0] next item, [1] CTAs finished; 0 between launches
     int32_t window;               // sliding window W (0 = none): keys >= position - (W - 1)
 };
 
@@ -206,7 +185,8 @@ __device__ int prefill_fetch(const PrefillArgs &a) {
 }
 
 // Called once per CTA after its last fetch: the last CTA to finish resets the
-// counters for the next launch that uses them.
+// counters (in the caller's scheduler array) for the next launch that uses
+// them.
 __device__ void prefill_sched_done(const PrefillArgs &a) {
     __threadfence();
     if (atomicAdd(&a.sched[1], 1) == (int)gridDim.x - 1) {
@@ -331,7 +311,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     uint64_t *o_final = p_full + T;          // T: every MMA of O_k of an item (with keys) done
     constexpr int R = kItemRing;
     uint64_t *item_full = o_final + T;       // R: item index published
-    uint64_t *item_empty = item_full + R;    // R: read by the MMA thread, every softmax warp
+    uint64_t *item_empty = item_full + R;    // R: read by the MMA warp, every softmax warp
                                              //    and (page size 1) the other gather warps
     int *item_idx = reinterpret_cast<int *>(item_empty + R);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(item_idx + R);
@@ -652,6 +632,22 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                         *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (rr & 7)) * 16)) = hi;
                     }
                 }
+                // Rows of an item's last V tile at keys >= kv_end are slots
+                // the store never wrote (the last page is loaded whole): P is
+                // 0 there, but 0 * NaN is not, so they become zeros (this
+                // warp's rows of the page that holds key kv_end - 1; later
+                // pages are zero-filled by the TMA).
+                if (c == 2 * it.n_kv - 1 && (it.kv_end & 15)) {
+                    __syncwarp();
+                    const int kbase = (it.j0 + it.n_kv - 1) * kBN;
+                    const int r0 = max(it.kv_end - kbase, 64 * cw);
+                    const int r1 = min(((it.kv_end + 15) & ~15) - kbase, 64 * cw + 64);
+                    for (int i = lane; i < (r1 - r0) * (D / 8); i += 32) {
+                        const int row = r0 + i / (D / 8), ch = i % (D / 8);
+                        *reinterpret_cast<uint4 *>(dst + (ch / 8) * 16384 + row * 128 + (ch % 8) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -707,6 +703,27 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                 for (int j = 0; ok && j < n_kv; ++j) {
                     const int cv = gl + 2 * j + 1;
                     const uint64_t dv = dv0 + (uint64_t)(((cv % NC) * S::kTileBytes) >> 4);
+                    if (!F8 && paged16 && (it.kv_end & 15) && j + 1 == n_kv) {
+                        // The last page of a request is loaded whole (one
+                        // 16-token TMA box), so rows of the item's last V tile
+                        // at keys >= kv_end hold slots the store never wrote.
+                        // P is 0 there, but 0 * NaN is not: clear those rows
+                        // (at most 15, up to the end of the page; later pages
+                        // are zero-filled by the TMA) once the tile has landed,
+                        // while the softmax of this step still runs.  (FP8
+                        // tiles are cleared by the widening warps.)
+                        if (!wait_full(cv)) { ok = false; break; }
+                        const int kbase = (it.j0 + j) * kBN;
+                        const int r0 = it.kv_end - kbase;                  // first row past the keys
+                        const int r1 = ((it.kv_end + 15) & ~15) - kbase;   // end of its page
+                        uint8_t *vt = land(cv % NS);
+                        for (int row = r0; row < r1; ++row)
+#pragma unroll
+                            for (int ch = 0; ch < D / 8; ++ch)
+                                *reinterpret_cast<uint4 *>(vt + (ch / 8) * 16384 + row * 128 + (ch % 8) * 16) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                        fence_proxy_async_smem();                          // generic writes -> the MMA's reads
+                    }
                     for (int k = 0; k < T; ++k) {
                         if (!mbar_wait(&p_full[k], (gs + j) & 1)) { ok = false; break; }
                         if (k == 0 && !wait_full(cv)) { ok = false; break; }
@@ -831,12 +848,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
 #pragma unroll
             for (int c = 0; c < kBN / 2; ++c) {
                 const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), c2, nm2);
-                float2 p;
-                if (kPolyEvery > 0 && (c % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
-                    p = exp2_poly2(x);
-                } else {
-                    p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                }
+                const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                 acc[c & 3] = add2(acc[c & 3], p);
                 pk[c] = F8 ? pack_f16x2(p.x, p.y) : pack_bf16x2(p.x, p.y);
             }
@@ -913,17 +925,6 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     }
 }
 
-__global__ void exp2_selftest_kernel(const float *__restrict__ x, float *__restrict__ y, int64_t n) {
-    const int64_t i = 2 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
-    if (i + 1 < n) {
-        const float2 r = exp2_poly2(make_float2(x[i], x[i + 1]));
-        y[i] = r.x;
-        y[i + 1] = r.y;
-    } else if (i < n) {
-        y[i] = exp2_poly2(make_float2(x[i], x[i])).x;
-    }
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -974,33 +975,6 @@ cudaError_t launch_t(const PrefillArgs &a, dim3 grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     kern<<<grid, 128 * (T + 1), smem, stream>>>(a);
     return cudaGetLastError();
-}
-
-// Work counters of the prefill scheduler: kSchedSlots pairs per device, zero
-// at module load and reset to zero by the last CTA of every launch.  Launches
-// take pairs in turn, so launches that may run at the same time (different
-// streams) use different pairs as long as fewer than kSchedSlots prefill
-// launches are issued on the device between them.
-constexpr int kSchedSlots = 1024;
-static __device__ int32_t g_prefill_sched[2 * kSchedSlots];
-
-cudaError_t prefill_sched(int32_t **ptr) {
-    static std::mutex lock;
-    static int32_t *base[kMaxDevices] = {nullptr};
-    static uint32_t next[kMaxDevices] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(lock);
-    if (base[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_prefill_sched);
-        if (e != cudaSuccess) return e;
-        base[dev] = static_cast<int32_t *>(p);
-    }
-    *ptr = base[dev] + 2 * (next[dev]++ % kSchedSlots);
-    return cudaSuccess;
 }
 
 }  // namespace
@@ -1055,21 +1029,13 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     if (virt > INT32_MAX) return cudaErrorNotSupported;
     a.num_virtual = (int32_t)virt;
     if (virt == 0) return cudaSuccess;
-    cudaError_t e = prefill_sched(&a.sched);
-    if (e != cudaSuccess) return e;
+    a.sched = p.scheduler;
     // persistent: one CTA per SM (each holds all 512 TMEM columns)
     int64_t ctas = num_sms();
     if (p.max_ctas > 0 && p.max_ctas < ctas) ctas = p.max_ctas;   // leave SMs to a concurrent launch
     dim3 grid((unsigned)(virt < ctas ? virt : ctas));
     return a.window > 0 ? dispatch_f8<true>(a, f8, p.head_dim, T, grid, stream)
                         : dispatch_f8<false>(a, f8, p.head_dim, T, grid, stream);
-}
-
-cudaError_t launch_exp2_selftest(const float *x, float *y, int64_t n, cudaStream_t stream) {
-    if (n <= 0) return cudaSuccess;
-    const int64_t threads = (n + 1) / 2;
-    exp2_selftest_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(x, y, n);
-    return cudaGetLastError();
 }
 
 }  // namespace pa

@@ -11,9 +11,10 @@
  * score = scale * q . k.  Prefill of the last Lq keys of each sequence: the
  * query at position p sees keys 0 .. p, so its output is p / 2 and its lse
  * score + ln(p + 1).  Unused page-table entries point at a page full of NaN,
- * so any read through a wrong entry shows up in the output (slots past a
- * sequence's end inside its last page hold zeros: the prefill reads whole
- * pages).  Splits of 16 keys force decode's split-and-merge path.
+ * so any read through a wrong entry shows up in the output, and so do the
+ * slots past a sequence's end inside its last page (never written: a kernel
+ * that lets one of them reach an output fails).  Splits of 16 keys force
+ * decode's split-and-merge path.
  *
  * Exit status 0 = every check passed.
  */
@@ -106,13 +107,8 @@ int main(void) {
     const size_t pool_elems = (size_t)PAGES * P * row;
     uint16_t *hk = malloc(pool_elems * 2), *hv = malloc(pool_elems * 2);
     for (size_t i = 0; i < pool_elems; ++i) hk[i] = hv[i] = 0x7FC0;   /* NaN */
-    /* the pages of each sequence: K = 1, V = key index, zeros past the end;
+    /* the pages of each sequence: K = 1, V = key index, NaN past the end;
        the last key is left NaN here and written by pa_store_kv below */
-    for (int b = 0; b < B; ++b)
-        for (int j = kLen[b]; j < (kLen[b] + P - 1) / P * P; ++j) {
-            const size_t slot = (size_t)kPages[b][j / P] * P + j % P;
-            for (size_t e = 0; e < row; ++e) hk[slot * row + e] = hv[slot * row + e] = 0;
-        }
     for (int b = 0; b < B; ++b)
         for (int j = 0; j + 1 < kLen[b]; ++j) {
             const size_t slot = (size_t)kPages[b][j / P] * P + j % P;
@@ -214,8 +210,10 @@ int main(void) {
     float hlsep[HQ * TQ];
     for (int i = 0; i < TQ * HQ * D; ++i) hqp[i] = bf16(0.5f);
     void *qp, *outp;
-    int32_t *cuq, *cuk;
+    int32_t *cuq, *cuk, *sched;
     float *lsep;
+    CK(cudaMalloc((void **)&sched, PA_PREFILL_SCHEDULER_INTS * sizeof(int32_t)));
+    CK(cudaMemset(sched, 0, PA_PREFILL_SCHEDULER_INTS * sizeof(int32_t)));
     CK(cudaMalloc(&qp, sizeof hqp));
     CK(cudaMalloc(&outp, sizeof houtp));
     CK(cudaMalloc((void **)&lsep, sizeof hlsep));
@@ -250,6 +248,7 @@ int main(void) {
     f.lse = lsep;
     f.lse_stride = TQ;
     f.kv_dtype = PA_KV_BF16;
+    f.scheduler = sched;
     PK(pa_prefill(&f, NULL));
     int32_t bits = 0;
     PK(pa_device_error(&bits, NULL));

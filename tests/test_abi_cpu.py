@@ -8,6 +8,7 @@ import re
 import numpy as np
 import pytest
 
+import abi_reject_cases
 import oracle
 import workloads as W
 
@@ -39,7 +40,7 @@ def test_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libpa.so does not export {name}"
         assert name in _lib.SIGNATURES, f"binding has no signature for {name}"
-    assert lib.pa_abi_version() == 1
+    assert lib.pa_abi_version() == 2
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
@@ -67,82 +68,29 @@ def test_build_seqlens_edges(lib):
         pa.build_seqlens([2**30, 2**30], [2**30, 0])    # total keys overflow int32
 
 
-def _prefill(lib, **kw):
-    from paged_kv_flashattention_gb300 import _lib
-    base = dict(q=0x1000, k_cache=0x2000, v_cache=0x3000, page_table=0x4000, page_table_stride=64,
-                total_q=64, cu_seqlens_q=0x5000, cu_seqlens_k=0x6000, num_seqs=2, max_seqlen_q=16,
-                max_seqlen_k=32, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
-                num_pages=100, causal=1, scale=0.1, out=0x7000, lse=None, lse_stride=0)
-    base.update(kw)
-    p = _lib.PrefillParams(**base)
-    return lib.pa_prefill(ctypes.byref(p), None)
+@pytest.fixture(scope="module")
+def rejections(lib):
+    """Every malformed call of tests/abi_reject_cases.py, run in a child
+    process that sees no GPU (CUDA_VISIBLE_DEVICES=''): the calls carry
+    made-up device addresses, so a check that failed to reject one would only
+    meet a CUDA error there, never a real GPU."""
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "abi_reject_cases.py")],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def _decode(lib, **kw):
-    from paged_kv_flashattention_gb300 import _lib
-    base = dict(q=0x1000, k_cache=0x2000, v_cache=0x3000, page_table=0x4000, page_table_stride=64,
-                cache_seqlens=0x5000, num_seqs=2, max_seqlen_k=4096, num_q_heads=8,
-                num_kv_heads=2, head_dim=128, page_size=16, num_pages=1000, scale=0.1,
-                out=0x7000, lse=None, workspace=0x8000, workspace_bytes=16, kv_chunk=0)
-    base.update(kw)
-    p = _lib.DecodeParams(**base)
-    return lib.pa_decode(ctypes.byref(p), None)
-
-
-INVALID, UNSUPPORTED = 1, 2
-
-
-@pytest.mark.parametrize("kw,status", [
-    (dict(head_dim=96), UNSUPPORTED),
-    (dict(page_size=8), UNSUPPORTED),
-    (dict(num_q_heads=6, num_kv_heads=4), INVALID),
-    (dict(num_q_heads=32, num_kv_heads=2), UNSUPPORTED),     # group 16
-    (dict(q=0x1001), INVALID),                               # misaligned
-    (dict(out=0), INVALID),
-    (dict(max_seqlen_q=64, max_seqlen_k=32), INVALID),
-    (dict(causal=2), INVALID),
-    (dict(page_table_stride=1), INVALID),
-    (dict(scale=float("nan")), INVALID),
-    (dict(scale=0.0), INVALID),
-    (dict(scale=-0.1), INVALID),
-    (dict(scale=float("inf")), INVALID),
-    (dict(sliding_window=-3), INVALID),
-])
-def test_prefill_rejects_before_launch(lib, kw, status):
-    assert _prefill(lib, **kw) == status
-    assert lib.pa_last_error()
-
-
-@pytest.mark.parametrize("kw,status", [
-    (dict(head_dim=80), UNSUPPORTED),
-    (dict(kv_chunk=24), INVALID),
-    (dict(kv_chunk=-16), INVALID),
-    (dict(workspace=0), INVALID),
-    (dict(workspace_bytes=16), INVALID),                      # far too small for 4096 keys
-    (dict(k_cache=0x2008), INVALID),
-    (dict(page_table_stride=8), INVALID),
-    (dict(num_seqs=20000), UNSUPPORTED),
-    (dict(kv_dtype=2), INVALID),
-    (dict(kv_dtype=1), INVALID),                              # FP8 without scales
-    (dict(sliding_window=-1), INVALID),
-    (dict(scale=-0.125), INVALID),
-    (dict(scale=float("inf")), INVALID),
-])
-def test_decode_rejects_before_launch(lib, kw, status):
-    assert _decode(lib, **kw) == status
-
-
-def test_store_rejects_before_launch(lib):
-    assert lib.pa_store_kv(0x1001, 0x2000, 0x3000, 4, 0x4000, 0x5000, 64, 2, 64, None) == INVALID
-    assert lib.pa_store_kv(0x1000, 0x2000, 0x3000, -1, 0x4000, 0x5000, 64, 2, 64, None) == INVALID
-    assert lib.pa_store_kv(0x1000, 0x2000, 0x3000, 4, 0x4000, 0x5000, 64, 1, 4, None) == UNSUPPORTED
-    # zero tokens: nothing to do, nothing launched
-    assert lib.pa_store_kv(0, 0, 0, 0, 0, 0, 0, 2, 64, None) == 0
-    # FP8 store: scales required, head_dim a multiple of 16
-    assert lib.pa_store_kv_fp8(0x1000, 0x2000, 0x3000, 4, 0x4000, 0x5000, 64, 2, 64, None, 0x6000, None) == INVALID
-    assert lib.pa_store_kv_fp8(0x1000, 0x2000, 0x3000, 4, 0x4000, 0x5000, 64, 2, 72, 0x6000, 0x7000, None) == UNSUPPORTED
-    assert lib.pa_store_kv_fp8(0x1008, 0x2000, 0x3000, 4, 0x4000, 0x5000, 64, 2, 64, 0x6000, 0x7000, None) == INVALID
-    assert lib.pa_store_kv_fp8(0, 0, 0, 0, 0, 0, 0, 2, 64, None, None, None) == 0
+@pytest.mark.parametrize("case", abi_reject_cases.all_case_ids())
+def test_rejects_before_launch(rejections, case):
+    status, message = rejections[case]
+    want = abi_reject_cases.expected()[case]
+    assert status == want, f"{case}: status {status} ({message}), expected {want}"
+    if want != 0:
+        assert message, f"{case}: no error message"
 
 
 def test_decode_workspace_size_host_only(lib):
@@ -181,18 +129,6 @@ def test_rope_table_host(lib):
         assert np.abs(t[:, :r // 2] - c).max() <= 2.0 ** -25 and np.abs(t[:, r // 2:] - s).max() <= 2.0 ** -25
     with pytest.raises(pa.PagedAttentionError):
         pa.rope_cos_sin_table(16, 7, 10000.0)
-
-
-def test_rope_store_rejects_before_launch(lib):
-    from paged_kv_flashattention_gb300 import _lib
-    base = dict(q=0x1000, q_out=0x1000, k=0x2000, v=0x3000, positions=0x4000, cos_sin=0x5000, max_pos=64,
-                rot_dim=128, interleaved=0, slot_mapping=0x6000, num_tokens=4, num_q_heads=8,
-                num_kv_heads=2, head_dim=128, k_cache=0x7000, v_cache=0x8000, num_slots=64, kv_dtype=0)
-    for kw, status in ((dict(rot_dim=72), UNSUPPORTED), (dict(rot_dim=256), UNSUPPORTED),
-                       (dict(interleaved=2), INVALID), (dict(kv_dtype=1), INVALID),
-                       (dict(q=0x1008), INVALID), (dict(head_dim=72), UNSUPPORTED)):
-        p = _lib.RopeStoreParams(**{**base, **kw})
-        assert lib.pa_rope_store_kv(ctypes.byref(p), None) == status, kw
 
 
 def test_graph_bucket_selection():

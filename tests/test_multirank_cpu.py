@@ -52,12 +52,12 @@ def test_max_over_ranks_single():
 def test_reference_arm_prints_on_rank0_only():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--steps", "1", "--warmup", "3", "--ref-seqs", "2"],
+                        "--steps", "1", "--warmup", "3", "--ref-cap-gb", "0.01"],
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
     env = dict(os.environ, RANK="0", WORLD_SIZE="2")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--steps", "1", "--warmup", "3", "--ref-seqs", "2"],
+                        "--steps", "1", "--warmup", "3", "--ref-cap-gb", "0.01"],
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0
     import json

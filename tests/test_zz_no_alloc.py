@@ -1,16 +1,14 @@
 """pa_decode_noalloc: decode for callers that may not allocate device memory
 (graph capture, host-owned memory arenas, hard memory budgets).  It must agree
 with pa_decode within the parity tolerance on two calls in a row (the shared
-scratch keeps the previous call's contents), and reject sizes beyond its fixed
-32 MiB scratch without launching.  This file is collected last on purpose."""
-import ctypes
-
-import numpy as np
+scratch keeps the previous call's contents), and with the fp64 oracle.  Its
+rejection of sizes beyond the fixed 32 MiB scratch is checked without a GPU
+(tests/abi_reject_cases.py).  This file is collected last on purpose."""
 import pytest
 import torch
 
 import workloads as W
-from pa_harness import DeviceProblem, TOL_MAX_ABS, TOL_MEAN_ABS
+from pa_harness import DeviceProblem, TOL_MAX_ABS, TOL_MEAN_ABS, compare, oracle_ref
 
 pytestmark = pytest.mark.gpu
 
@@ -33,6 +31,7 @@ def _close(a, b, what):
 def test_noalloc_matches_decode_twice(cuda_device):
     import paged_kv_flashattention_gb300 as pa
     cases = [(W.config(2), 0), (W.config(1), 16)]   # a split batch, then a smaller one
+    refs = {p.name: oracle_ref(p) for p, _ in cases}
     for rep in range(2):                             # two calls in a row per case
         for p, chunk in cases:
             d, m = _inputs(p, cuda_device)
@@ -47,18 +46,7 @@ def test_noalloc_matches_decode_twice(cuda_device):
             torch.cuda.synchronize()
             _close(out, ref, f"{p.name} call {rep}")
             assert (lse - lse_ref).abs().max().item() <= 2e-3
+            # and against the oracle itself, not only the other entry point
+            o_ref, l_ref = refs[p.name]
+            compare(out, o_ref, f"{p.name} no-alloc vs oracle, call {rep}", lse_gpu=lse, lse_ref=l_ref)
             assert pa.device_error() == 0
-
-
-def test_noalloc_rejects_oversized_scratch(cuda_device):
-    import paged_kv_flashattention_gb300 as pa
-    from paged_kv_flashattention_gb300 import _lib
-    lib = _lib.load()
-    # 4096 sequences of 32768 keys with 128-key splits need far more than 32 MiB
-    p = _lib.DecodeParams(q=0x1000, k_cache=0x2000, v_cache=0x3000, page_table=0x4000,
-                          page_table_stride=2048, cache_seqlens=0x5000, num_seqs=4096,
-                          max_seqlen_k=32768, num_q_heads=32, num_kv_heads=8, head_dim=128,
-                          page_size=16, num_pages=1 << 20, scale=0.1, out=0x6000, kv_chunk=128)
-    assert lib.pa_decode_workspace_size(ctypes.byref(p)) > (32 << 20)
-    assert lib.pa_decode_noalloc(ctypes.byref(p), None) == 2
-    assert b"32" in lib.pa_last_error()

@@ -21,6 +21,10 @@ Conventions
   page-table entry and the padding of the token table point at it, so a
   kernel that reads an entry it should not shows NaN in its output instead of
   touching memory outside the pool.
+* Slots past a request's last key inside its last page were never written by
+  the store (a serving engine's pool holds whatever was there before): they
+  are filled with NaN too (``tail_slots``), so a kernel that lets any value
+  of an unwritten slot reach an output fails the parity tests.
 * ``token_table`` is the allocator's record at token granularity (one slot per
   position, slot = page * page_size + offset), one row per request
   (``table_idx = arange(B)``).  ``slot_mapping`` lists the slots of the new
@@ -91,9 +95,32 @@ def fp8_pools(p: "Problem", seed: int, scale_lo: float = 0.1, scale_hi: float = 
     vc = e4m3_codes(rng, p.v_cache.shape)
     kc[p.num_pages - 1] = E4M3_NAN
     vc[p.num_pages - 1] = E4M3_NAN
+    poison_tails(p, kc, vc, E4M3_NAN)
     ks = rng.uniform(scale_lo, scale_hi, size=p.num_kv_heads).astype(np.float32)
     vs = rng.uniform(scale_lo, scale_hi, size=p.num_kv_heads).astype(np.float32)
     return kc, vc, ks, vs
+
+
+def tail_slots(page_lists, device_len, token_table, page_size: int) -> np.ndarray:
+    """Flat slot indices (page * page_size + offset) of the slots of used
+    pages that no request reads: the unwritten tail of each request's last
+    page.  A slot that some request reads (shared prefix pages) is excluded."""
+    used = sorted(set(int(p) for pl in page_lists for p in pl))
+    if not used or page_size == 1:
+        return np.zeros(0, np.int64)
+    every = (np.asarray(used, np.int64)[:, None] * page_size + np.arange(page_size)).ravel()
+    read = [token_table[b, :int(L)].astype(np.int64) for b, L in enumerate(device_len) if int(L) > 0]
+    read = np.concatenate(read) if read else np.zeros(0, np.int64)
+    return np.setdiff1d(every, read)
+
+
+def poison_tails(p: "Problem", k_pool: np.ndarray, v_pool: np.ndarray, value) -> None:
+    """Write `value` (NaN bits) into every unwritten tail slot of p's pools
+    (shape [num_pages, page_size, Hkv, d], modified in place)."""
+    s = tail_slots(p.meta["page_lists"], p.device_len, p.token_table, p.page_size)
+    if s.size:
+        k_pool.reshape(p.num_pages * p.page_size, -1)[s] = value
+        v_pool.reshape(p.num_pages * p.page_size, -1)[s] = value
 
 
 @dataclass
@@ -223,6 +250,7 @@ def build(name: str, *, cached_len, extend_len, num_q_heads: int, num_kv_heads: 
         p.v_cache = normal_bf16(rng, shape)
         p.k_cache[num_pages - 1] = BF16_NAN
         p.v_cache[num_pages - 1] = BF16_NAN
+        poison_tails(p, p.k_cache, p.v_cache, BF16_NAN)
     return p
 
 
@@ -293,7 +321,21 @@ def add_host_data(p: Problem, rng_seed: int | None = None) -> Problem:
     p.v_cache = normal_bf16(rng, shape)
     p.k_cache[-1] = BF16_NAN
     p.v_cache[-1] = BF16_NAN
+    poison_tails(p, p.k_cache, p.v_cache, BF16_NAN)
     return p
+
+
+def poison_tails_device(p: Problem, k_pool, v_pool) -> int:
+    """Device-pool version of ``poison_tails``: write bf16 NaN into p's
+    unwritten tail slots of two torch CUDA pools [num_pages, P, Hkv, d].
+    Returns the number of slots poisoned."""
+    import torch
+    s = tail_slots(p.meta["page_lists"], p.device_len, p.token_table, p.page_size)
+    if s.size:
+        idx = torch.from_numpy(s).to(k_pool.device)
+        for t in (k_pool, v_pool):
+            t.view(-1, t.shape[-2] * t.shape[-1]).index_fill_(0, idx, float("nan"))
+    return int(s.size)
 
 
 def fill_normal_device(t, seed: int) -> None:
