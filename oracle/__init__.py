@@ -60,6 +60,12 @@ def _bind(lib):
     lib.oracle_attention_fp8.argtypes = [P, P, P, P, P, P, i64, P, P, i32, i32, i32, i32, i32,
                                          i64, ctypes.c_int, i32, dbl, P, i64, P, P]
     lib.oracle_attention_fp8.restype = ctypes.c_int
+    lib.oracle_attention_bm.argtypes = [P, P, P, P, i64, P, P, i32, i32, i32, i32, i32,
+                                        i64, ctypes.c_int, i32, P, i32, i32, dbl, P, i64, P, P]
+    lib.oracle_attention_bm.restype = ctypes.c_int
+    lib.oracle_attention_fp8_bm.argtypes = [P, P, P, P, P, P, i64, P, P, i32, i32, i32, i32, i32,
+                                            i64, ctypes.c_int, i32, P, i32, i32, dbl, P, i64, P, P]
+    lib.oracle_attention_fp8_bm.restype = ctypes.c_int
     lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_value.restype = dbl
     lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
@@ -236,12 +242,14 @@ def seqlens(cached_len, extend_len, *, lib=None):
 def attention(q, k_cache, v_cache, page_table, cu_seqlens_q, cu_seqlens_k, *,
               num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
               causal: bool, scale: float, rows=None, k_scale=None, v_scale=None, window_left: int = -1,
-              lib=None):
+              block_mask=None, lib=None):
     """fp64 attention over paged K/V.
 
     q: uint16 [Tq, Hq, d]; caches: uint16 [num_pages*page_size, Hkv, d] (any
     shape with that element order), or uint8 E4M3 codes with float32
     ``k_scale``/``v_scale`` [Hkv]; page_table int32 [B, stride].
+    block_mask: optional uint8 [B, nq, nk]; entry [b, i // 128, j // 128] == 0
+    hides key j from query row i of request b.
     Returns (out, lse): float64 [Tq, Hq, d] and [Tq, Hq], or, when ``rows`` (an
     int64 [n, 2] array of (token, head)) is given, [n, d] and [n].
     """
@@ -268,6 +276,22 @@ def attention(q, k_cache, v_cache, page_table, cu_seqlens_q, cu_seqlens_k, *,
         out = np.zeros((rws.shape[0], d), dtype=np.float64)
         lse = np.zeros((rws.shape[0],), dtype=np.float64)
         rp, nr = _ptr(rws), rws.shape[0]
+    if block_mask is not None:
+        bm = _c(block_mask, np.uint8)
+        assert bm.ndim == 3 and bm.shape[0] == B
+        if fp8:
+            ks = _c(k_scale, np.float32)
+            vs = _c(v_scale, np.float32)
+            _check(_load(lib).oracle_attention_fp8_bm(
+                _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(pt), pt.shape[1], _ptr(cq), _ptr(ck),
+                B, Hq, Hkv, d, P, num_pages, int(bool(causal)), int(window_left), _ptr(bm), bm.shape[1],
+                bm.shape[2], float(scale), rp, nr, _ptr(out), _ptr(lse)), "oracle_attention_fp8_bm")
+        else:
+            _check(_load(lib).oracle_attention_bm(
+                _ptr(q), _ptr(kc), _ptr(vc), _ptr(pt), pt.shape[1], _ptr(cq), _ptr(ck), B,
+                Hq, Hkv, d, P, num_pages, int(bool(causal)), int(window_left), _ptr(bm), bm.shape[1],
+                bm.shape[2], float(scale), rp, nr, _ptr(out), _ptr(lse)), "oracle_attention_bm")
+        return out, lse
     if fp8:
         ks = _c(k_scale, np.float32)
         vs = _c(v_scale, np.float32)

@@ -36,9 +36,11 @@ def gather_request(cache_rows, page_row, length: int, page_size: int, kv_head: i
 
 
 def attention(q, k_cache, v_cache, page_table, cu_q, cu_k, *, num_q_heads, num_kv_heads,
-              head_dim, page_size, causal, scale, window_left=-1):
+              head_dim, page_size, causal, scale, window_left=-1, block_mask=None):
     """q: nested [Tq][Hq][d] bf16 bits (or a numpy array); caches indexable as
-    cache[slot][kv_head] -> d bits.  Returns nested lists O[Tq][Hq][d]."""
+    cache[slot][kv_head] -> d bits; block_mask: optional [B][nq][nk] bytes over
+    blocks of 128 query rows x 128 keys (0 = the keys of that block are not
+    attended to).  Returns nested lists O[Tq][Hq][d]."""
     group = num_q_heads // num_kv_heads
     Tq = int(cu_q[-1])
     out = [[[0.0] * head_dim for _ in range(num_q_heads)] for _ in range(Tq)]
@@ -54,7 +56,8 @@ def attention(q, k_cache, v_cache, page_table, cu_q, cu_k, *, num_q_heads, num_k
                     # absolute position of this query among the request's keys
                     pos = (Lk - Lq) + i
                     keys = [j for j in range(Lk) if ((not causal) or j <= pos)
-                            and (window_left < 0 or pos - j <= window_left)]
+                            and (window_left < 0 or pos - j <= window_left)
+                            and (block_mask is None or block_mask[b][i // 128][j // 128] != 0)]
                     if not keys:
                         continue            # empty: output stays 0
                     e = [math.exp(scale * math.fsum(a * c for a, c in zip(qv, K[j]))) for j in keys]

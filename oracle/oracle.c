@@ -34,7 +34,15 @@
  *    section 19) bounds the visible keys from below: with window_left >= 0
  *    a query at absolute position p sees only keys j >= p - window_left
  *    (so window_left + 1 keys at most when causal); window_left < 0 means
- *    no window.
+ *    no window.  A block-sparse mask (the "custom sparse" entry of the same
+ *    list; the pages give no format, the reading here is the plainest one
+ *    that a tiled kernel can honour): per request a grid of bytes over
+ *    blocks of 128 queries x 128 keys, mask[b][i / 128][j / 128] for query
+ *    index i within the request's rows (0 .. Lq - 1) and key j; a zero byte
+ *    hides every key of that block from every query of that block.  It is
+ *    additive in the sense of section 10: a hidden key's score is -inf, on
+ *    top of the causal and window limits.  A row left with no visible key
+ *    returns O = 0 and lse = -inf.
  *
  *  - oracle_page_table_from_token_table: the metadata step of the
  *    mini-sglang page, "from ledger to tensors": the global table is token
@@ -269,6 +277,15 @@ typedef struct {
     const float *k_scale, *v_scale;
 } kv_pools;
 
+/* Optional block-sparse mask: bytes [num_seqs][nq][nk] over 128 x 128 blocks
+ * (m == NULL: none). */
+typedef struct {
+    const uint8_t *m;
+    int32_t nq, nk;
+} block_mask;
+
+#define ORACLE_MASK_BLOCK 128
+
 static double kv_value(const void *cache, int fp8, const float *scale, int64_t idx, int32_t kvh)
 {
     if (!fp8) return widen_bf16(((const uint16_t *)cache)[idx]);
@@ -279,8 +296,8 @@ static int attention_row(const uint16_t *q, const kv_pools *kv,
                          const int32_t *page_table, int64_t pt_stride,
                          const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
                          int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
-                         int causal, int32_t window_left, double scale, int64_t t, int32_t h,
-                         double *o, double *lse, double *s_row)
+                         int causal, int32_t window_left, const block_mask *bm, double scale,
+                         int64_t t, int32_t h, double *o, double *lse, double *s_row)
 {
     /* request b owning query token t */
     int32_t b = -1;
@@ -309,9 +326,17 @@ static int attention_row(const uint16_t *q, const kv_pools *kv,
 
     for (int c = 0; c < d; ++c) o[c] = 0.0;
     if (n_vis <= j_lo) { *lse = -INFINITY; return ORACLE_OK; }
+    /* the block-mask row of this query (NULL: every block visible) */
+    const uint8_t *mrow = NULL;
+    if (bm && bm->m) {
+        if (i / ORACLE_MASK_BLOCK >= bm->nq || (n_vis - 1) / ORACLE_MASK_BLOCK >= bm->nk) return ORACLE_EINVAL;
+        mrow = bm->m + ((int64_t)b * bm->nq + i / ORACLE_MASK_BLOCK) * (int64_t)bm->nk;
+    }
 
-    /* pass 0: materialise the score row S[j] = scale * q . K_j */
+    /* pass 0: materialise the score row S[j] = scale * q . K_j (-inf where
+     * the block mask hides the key) */
     for (int64_t j = j_lo; j < n_vis; ++j) {
+        if (mrow && mrow[j / ORACLE_MASK_BLOCK] == 0) { s_row[j] = -INFINITY; continue; }
         int64_t page = page_table[b * pt_stride + j / P];
         if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
         int64_t row = page * P + j % P;
@@ -324,6 +349,7 @@ static int attention_row(const uint16_t *q, const kv_pools *kv,
     /* pass 1: row maximum */
     double m = -INFINITY;
     for (int64_t j = j_lo; j < n_vis; ++j) if (s_row[j] > m) m = s_row[j];
+    if (m == -INFINITY) { *lse = -INFINITY; return ORACLE_OK; }   /* every key hidden */
     /* pass 2: exponentials, their sum, and P.V */
     double l = 0.0;
     for (int64_t j = j_lo; j < n_vis; ++j) {
@@ -348,8 +374,8 @@ static int attention_all(const uint16_t *q, const kv_pools *kv,
                          const int32_t *page_table, int64_t pt_stride,
                          const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
                          int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
-                         int causal, int32_t window_left, double scale, const int64_t *rows,
-                         int64_t nrows, double *out, double *lse)
+                         int causal, int32_t window_left, const block_mask *bm, double scale,
+                         const int64_t *rows, int64_t nrows, double *out, double *lse)
 {
     if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || P <= 0 || Hq % Hkv) return ORACLE_EINVAL;
     int64_t Tq = num_seqs > 0 ? cu_q[num_seqs] : 0;
@@ -380,8 +406,8 @@ static int attention_all(const uint16_t *q, const kv_pools *kv,
                     continue;
                 }
                 int st = attention_row(q, kv, page_table, pt_stride, cu_q, cu_k,
-                                       num_seqs, Hq, Hkv, d, P, num_pages, causal, window_left, scale, t, h,
-                                       out + r * (int64_t)d, lse + r, s_row);
+                                       num_seqs, Hq, Hkv, d, P, num_pages, causal, window_left, bm, scale,
+                                       t, h, out + r * (int64_t)d, lse + r, s_row);
                 if (st != ORACLE_OK) {
 #pragma omp atomic write
                     status = st;
@@ -402,7 +428,24 @@ int oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t 
 {
     kv_pools kv = {k_cache, v_cache, 0, NULL, NULL};
     return attention_all(q, &kv, page_table, pt_stride, cu_q, cu_k, num_seqs, Hq, Hkv, d, P,
-                         num_pages, causal, window_left, scale, rows, nrows, out, lse);
+                         num_pages, causal, window_left, NULL, scale, rows, nrows, out, lse);
+}
+
+/* The same with a block-sparse mask bmask [num_seqs][bm_q][bm_k] (bytes;
+ * zero = the 128 x 128 block is hidden). */
+int oracle_attention_bm(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *page_table, int64_t pt_stride,
+                        const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
+                        int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
+                        int causal, int32_t window_left, const uint8_t *bmask, int32_t bm_q,
+                        int32_t bm_k, double scale, const int64_t *rows, int64_t nrows, double *out,
+                        double *lse)
+{
+    if (bmask && (bm_q <= 0 || bm_k <= 0)) return ORACLE_EINVAL;
+    kv_pools kv = {k_cache, v_cache, 0, NULL, NULL};
+    block_mask bm = {bmask, bm_q, bm_k};
+    return attention_all(q, &kv, page_table, pt_stride, cu_q, cu_k, num_seqs, Hq, Hkv, d, P,
+                         num_pages, causal, window_left, &bm, scale, rows, nrows, out, lse);
 }
 
 /* The same over E4M3 pools (codes [num_pages*P, Hkv, d]) with per-KV-head
@@ -417,7 +460,23 @@ int oracle_attention_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_
 {
     kv_pools kv = {k_cache, v_cache, 1, k_scale, v_scale};
     return attention_all(q, &kv, page_table, pt_stride, cu_q, cu_k, num_seqs, Hq, Hkv, d, P,
-                         num_pages, causal, window_left, scale, rows, nrows, out, lse);
+                         num_pages, causal, window_left, NULL, scale, rows, nrows, out, lse);
+}
+
+int oracle_attention_fp8_bm(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *page_table, int64_t pt_stride,
+                            const int32_t *cu_q, const int32_t *cu_k, int32_t num_seqs,
+                            int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int64_t num_pages,
+                            int causal, int32_t window_left, const uint8_t *bmask, int32_t bm_q,
+                            int32_t bm_k, double scale, const int64_t *rows, int64_t nrows,
+                            double *out, double *lse)
+{
+    if (bmask && (bm_q <= 0 || bm_k <= 0)) return ORACLE_EINVAL;
+    kv_pools kv = {k_cache, v_cache, 1, k_scale, v_scale};
+    block_mask bm = {bmask, bm_q, bm_k};
+    return attention_all(q, &kv, page_table, pt_stride, cu_q, cu_k, num_seqs, Hq, Hkv, d, P,
+                         num_pages, causal, window_left, &bm, scale, rows, nrows, out, lse);
 }
 
 /* ---------------------------------------------------------------- RoPE */

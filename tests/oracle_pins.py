@@ -32,6 +32,12 @@ angle)) for the rotation, by its defining property (q(m) . k(n) depends only
 on m - n) and by position 0 being the identity; the bf16 rounding by the
 input generator's float32 -> bf16 rounding on float32 values and exact ties.
 
+The block-sparse mask (128 x 128 blocks of a request's query rows and keys)
+is pinned by the brute force filtering keys by the mask byte, by the all-ones
+and all-zero masks, by a block-diagonal mask equalling independent 128-token
+requests, and by a hidden first key block equalling a page table shifted by
+128 keys.
+
 The hand-worked golden cases live in tests/golden/.
 """
 from __future__ import annotations
@@ -673,7 +679,110 @@ def check_window_is_truncated_cache(lib=None):
         assert np.array_equal(o[b], ob[0]) and np.array_equal(l[b], lb[0]), "window != truncated cache"
 
 
-ALL_CHECKS = [check_window_brute_force, check_window_closed_forms, check_window_is_truncated_cache,
+# ------------------------------------------------------- block-sparse mask
+def _mask_problems():
+    """Requests longer than one 128-row / 128-key block: a long prompt, a
+    cached prefix with an extend crossing a block edge, a short extend over a
+    long prefix, and an empty request."""
+    return [W.small_problem(71, [0, 40, 200, 0], [300, 130, 64, 0], num_q_heads=4, num_kv_heads=2,
+                            head_dim=8, page_size=4),
+            W.small_problem(72, [0, 129], [257, 128], num_q_heads=2, num_kv_heads=1, head_dim=8,
+                            page_size=16)]
+
+
+def _oracle_mask(p, kc, vc, mask, causal=None, lib=None, window_left=-1):
+    cu_q, cu_k, _, pt = _meta(p, lib)
+    return oracle.attention(p.q, kc, vc, pt, cu_q, cu_k, num_q_heads=p.num_q_heads,
+                            num_kv_heads=p.num_kv_heads, head_dim=p.head_dim, page_size=p.page_size,
+                            causal=p.causal if causal is None else causal, scale=p.scale,
+                            window_left=window_left, block_mask=mask, lib=lib)
+
+
+def check_block_mask_brute_force(lib=None):
+    """Random 128 x 128 block masks, causal and not, with and without a
+    window, against the brute force (which filters keys by the mask byte of
+    the query's and the key's blocks)."""
+    rng = np.random.default_rng(7)
+    for p in _mask_problems():
+        kc, vc = stored_caches(p, lib)
+        cu_q, cu_k, _, pt = _meta(p, lib)
+        kcr = kc.reshape(-1, p.num_kv_heads, p.head_dim)
+        vcr = vc.reshape(-1, p.num_kv_heads, p.head_dim)
+        for causal, w in ((True, -1), (False, -1), (True, 150)):
+            m = W.block_mask(rng, p.extend_len, p.device_len, density=0.5, keep_diagonal=False)
+            o, _ = _oracle_mask(p, kc, vc, m, causal, lib, window_left=w)
+            ob = np.array(brute.attention(p.q, kcr, vcr, pt, cu_q, cu_k, num_q_heads=p.num_q_heads,
+                                          num_kv_heads=p.num_kv_heads, head_dim=p.head_dim,
+                                          page_size=p.page_size, causal=causal, scale=p.scale,
+                                          window_left=w, block_mask=m),
+                          dtype=np.float64).reshape(o.shape)
+            _assert_close(o, ob, 1e-12, f"block mask causal={causal} window={w}")
+
+
+def check_block_mask_closed_forms(lib=None):
+    """An all-ones mask changes nothing; an all-zero mask leaves every row
+    empty (O = 0, lse = -inf)."""
+    for p in _mask_problems():
+        kc, vc = stored_caches(p, lib)
+        o, l = run_oracle(p, lib, caches=(kc, vc))
+        nq = max(1, -(-int(p.extend_len.max()) // 128))
+        nk = max(1, -(-int(p.device_len.max()) // 128))
+        ones = np.ones((p.num_seqs, nq, nk), np.uint8)
+        o1, l1 = _oracle_mask(p, kc, vc, ones, lib=lib)
+        assert np.array_equal(o, o1) and np.array_equal(l, l1), "all-ones mask must change nothing"
+        o0, l0 = _oracle_mask(p, kc, vc, np.zeros_like(ones), lib=lib)
+        assert np.all(o0 == 0.0) and np.all(l0 == -np.inf), "all-zero mask must hide every key"
+
+
+def check_block_mask_diagonal_is_split(lib=None):
+    """Causal attention of a prompt with no cached prefix under a
+    block-diagonal mask equals the same prompt cut into independent requests
+    of 128 tokens (each block attends only within itself)."""
+    L = 300
+    p = W.small_problem(73, [0], [L], num_q_heads=4, num_kv_heads=2, head_dim=8, page_size=4)
+    kc, vc = stored_caches(p, lib)
+    nb = -(-L // 128)
+    diag = np.zeros((1, nb, nb), np.uint8)
+    for k in range(nb):
+        diag[0, k, k] = 1
+    o, l = _oracle_mask(p, kc, vc, diag, causal=True, lib=lib)
+    _, _, _, pt = _meta(p, lib)
+    lens = [min(128, L - 128 * k) for k in range(nb)]
+    per = 128 // p.page_size
+    pts = np.full((nb, per), pt[0, 0], np.int32)
+    for k in range(nb):
+        row = pt[0, k * per:k * per + -(-lens[k] // p.page_size)]
+        pts[k, :row.shape[0]] = row
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    os_, ls_ = oracle.attention(p.q, kc, vc, pts, cu, cu, num_q_heads=4, num_kv_heads=2, head_dim=8,
+                                page_size=p.page_size, causal=True, scale=p.scale, lib=lib)
+    assert np.array_equal(o, os_) and np.array_equal(l, ls_), "block-diagonal mask != split requests"
+
+
+def check_block_mask_hidden_prefix(lib=None):
+    """Non-causal attention with key block 0 hidden for every query equals
+    attention over the keys from 128 on (the page table shifted by 128
+    keys)."""
+    p = W.small_problem(74, [200, 140], [30, 9], num_q_heads=4, num_kv_heads=2, head_dim=8, page_size=4,
+                        causal=False)
+    kc, vc = stored_caches(p, lib)
+    nk = -(-int(p.device_len.max()) // 128)
+    m = np.ones((p.num_seqs, 1, nk), np.uint8)
+    m[:, :, 0] = 0
+    o, l = _oracle_mask(p, kc, vc, m, causal=False, lib=lib)
+    cu_q, cu_k, _, pt = _meta(p, lib)
+    shift = 128 // p.page_size
+    Lk2 = (p.device_len - 128).astype(np.int64)
+    cu_k2 = np.concatenate([[0], np.cumsum(Lk2)]).astype(np.int32)
+    o2, l2 = oracle.attention(p.q, kc, vc, np.ascontiguousarray(pt[:, shift:]), cu_q, cu_k2,
+                              num_q_heads=4, num_kv_heads=2, head_dim=8, page_size=p.page_size,
+                              causal=False, scale=p.scale, lib=lib)
+    assert np.array_equal(o, o2) and np.array_equal(l, l2), "hidden first key block != shifted table"
+
+
+ALL_CHECKS = [check_block_mask_brute_force, check_block_mask_closed_forms,
+              check_block_mask_diagonal_is_split, check_block_mask_hidden_prefix,
+              check_window_brute_force, check_window_closed_forms, check_window_is_truncated_cache,
               check_rope_table, check_rope_complex, check_rope_relative_position, check_round_bf16,
               check_e4m3_codec, check_store_fp8, check_attention_fp8_exact_values, check_store, check_metadata, check_golden, check_brute_force, check_equal_scores,
               check_single_key, check_dominant_key, check_empty, check_sdpa_library,

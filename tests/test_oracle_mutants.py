@@ -42,6 +42,10 @@ MUTANTS = [
     ("window_off_by_one", "j_lo = off + i - window_left;", "j_lo = off + i - window_left + 1;", 1),
     ("window_from_query_index", "j_lo = off + i - window_left;", "j_lo = i - window_left;", 1),
     ("window_ignored", "if (window_left >= 0) {\n        j_lo", "if (0) {\n        j_lo", 1),
+    ("block_mask_ignored", "if (mrow && mrow[j / ORACLE_MASK_BLOCK] == 0) { s_row[j] = -INFINITY; continue; }", "", 1),
+    ("block_mask_key_blocks_of_64", "mrow[j / ORACLE_MASK_BLOCK] == 0", "mrow[j / 64] == 0", 1),
+    ("block_mask_query_by_position", "+ i / ORACLE_MASK_BLOCK) * (int64_t)bm->nk;", "+ (off + i) / ORACLE_MASK_BLOCK) * (int64_t)bm->nk;", 1),
+    ("block_mask_empty_row_nan", "if (m == -INFINITY) { *lse = -INFINITY; return ORACLE_OK; }   /* every key hidden */", "", 1),
 ]
 
 

@@ -325,6 +325,33 @@ def add_host_data(p: Problem, rng_seed: int | None = None) -> Problem:
     return p
 
 
+MASK_BLOCK = 128
+
+
+def block_mask(rng: np.random.Generator, extend_len, device_len, density: float = 0.6,
+               keep_diagonal: bool = True) -> np.ndarray:
+    """A random block-sparse mask for a batch: uint8 [B, nq, nk] over blocks of
+    128 query rows (of each request's own rows) x 128 keys, each block kept
+    with probability ``density``; with ``keep_diagonal`` the block holding a
+    query block's own positions at the end of its keys is always kept (the
+    usual shape of a sparse causal pattern).  Blocks outside a request's
+    lengths are set too (never read)."""
+    ext = np.asarray(extend_len, np.int64)
+    dev = np.asarray(device_len, np.int64)
+    B = ext.shape[0]
+    nq = max(1, int(-(-ext.max() // MASK_BLOCK)) if B else 1)
+    nk = max(1, int(-(-dev.max() // MASK_BLOCK)) if B else 1)
+    m = (rng.random((B, nq, nk)) < density).astype(np.uint8)
+    if keep_diagonal:
+        for b in range(B):
+            off = int(dev[b] - ext[b])
+            for qb in range(nq):
+                last = off + min(int(ext[b]), (qb + 1) * MASK_BLOCK) - 1    # last row's position
+                if last >= 0:
+                    m[b, qb, last // MASK_BLOCK] = 1
+    return m
+
+
 def poison_tails_device(p: Problem, k_pool, v_pool) -> int:
     """Device-pool version of ``poison_tails``: write bf16 NaN into p's
     unwritten tail slots of two torch CUDA pools [num_pages, P, Hkv, d].
