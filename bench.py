@@ -238,7 +238,7 @@ CONFIG_CASES = {
     "varlen_prefill_16x512": ["varlen_prefill_16x512", "varlen_prefill_16x512_fp8", "store_16x512",
                               "rope_store_16x512"],
     "extend_partial_hit": ["extend_partial_hit_p16", "extend_partial_hit_p1", "extend_partial_hit_p16_fp8",
-                           "extend_partial_hit_p1_fp8"],
+                           "extend_partial_hit_p1_fp8", "extend_partial_hit_p16_mask50"],
     "decode_64seq_logu": ["decode_64seq_logu", "decode_64seq_logu_fp8"],
 }
 
@@ -609,7 +609,28 @@ MICRO_CASES = {
     "varlen_prefill_16x512_fp8": (3, None, "prefill"),
     "extend_partial_hit_p16_fp8": (4, None, "prefill"),
     "extend_partial_hit_p1_fp8": (4, "p1", "prefill"),
+    # the extend batch under a block-sparse mask keeping half of the 128 x
+    # 128 blocks (and every diagonal block): the skipped blocks cost nothing
+    "extend_partial_hit_p16_mask50": (4, None, "prefill"),
 }
+
+
+def masked_causal_pairs(p, mask) -> int:
+    """(query, key) pairs a causal prefill attends to under a 128 x 128
+    block mask: per request and query row, the visible keys of the kept key
+    blocks (work accounting for the bench only)."""
+    total = 0
+    kb = np.arange(mask.shape[2], dtype=np.int64)
+    for b in range(p.num_seqs):
+        Lq, Lk = int(p.extend_len[b]), int(p.device_len[b])
+        if Lq == 0:
+            continue
+        i = np.arange(Lq, dtype=np.int64)
+        last = (Lk - Lq) + i                                   # last visible key of row i
+        per_block = np.clip(last[:, None] + 1 - 128 * kb[None, :], 0, 128)
+        per_block = np.minimum(per_block, np.clip(Lk - 128 * kb[None, :], 0, 128))
+        total += int((per_block * mask[b][i // 128]).sum())
+    return total
 
 
 def micro_problem(name):
@@ -660,12 +681,17 @@ def prepare_case(name, dev):
         extra["seqs"] = p.num_seqs
     elif kernel == "prefill":
         sched = torch.zeros(2, dtype=torch.int32, device=dev)
-        fn = lambda: pa.prefill(q, kc, vc, m.page_table, m.cu_seqlens_q, m.cu_seqlens_k,
-                                m.max_seqlen_q, m.max_seqlen_k, causal=p.causal, scale=p.scale, out=out,
-                                scheduler=sched, **scales)
         off = p.cached_len.astype(np.int64)
         E = p.extend_len.astype(np.int64)
         work = 4 * D * Hq * int(np.sum(E * off + E * (E + 1) // 2))
+        if "_mask" in name:
+            mask = W.block_mask(np.random.default_rng(W.SEED_BASE + 73), p.extend_len, p.device_len, 0.5)
+            scales["block_mask"] = torch.from_numpy(mask).to(dev)
+            work = 4 * D * Hq * masked_causal_pairs(p, mask)
+            extra["kept_blocks"] = round(float(mask.mean()), 3)
+        fn = lambda: pa.prefill(q, kc, vc, m.page_table, m.cu_seqlens_q, m.cu_seqlens_k,
+                                m.max_seqlen_q, m.max_seqlen_k, causal=p.causal, scale=p.scale, out=out,
+                                scheduler=sched, **scales)
         unit = "TFLOP/s"
         # bytes a perfect kernel moves: Q read, O written, each request's K/V read once
         extra["bytes"] = 2 * q.numel() * 2 + int(p.device_len.astype(np.int64).sum()) * Hkv * D * 2 * kc.element_size()
@@ -723,7 +749,7 @@ def time_case(name, dev, steps, warmup):
     rate = work / (med * 1e-6) / (1e12 if unit == "TFLOP/s" else 1e9)
     res = {"kernel": extra["kernel"], "us_median": round(med, 2), "us_p95": round(p95, 2), "rate": round(rate, 1),
            "unit": unit, "work": work, "iters": groups * 10}
-    for k in ("page_size", "kv", "seqs", "tokens", "bytes"):
+    for k in ("page_size", "kv", "seqs", "tokens", "bytes", "kept_blocks"):
         if k in extra:
             res[k] = extra[k]
     del graph

@@ -265,7 +265,20 @@ typedef struct {
     int32_t *scheduler;          /* device int32 [PA_PREFILL_SCHEDULER_INTS], owned by the
                                     caller: zero before its first use, left zero by every
                                     completed launch; required (NULL = PA_ERR_INVALID) */
+    const uint8_t *block_mask;   /* optional block-sparse mask ([T] s.19 "custom sparse";
+                                    the pages give no format, this library's reading):
+                                    device bytes [num_seqs, block_mask_q_blocks,
+                                    block_mask_k_blocks] over blocks of
+                                    PA_MASK_BLOCK = 128 query rows x 128 keys; query row i
+                                    of request b (i counted from the request's first row,
+                                    0 .. Lq - 1) sees key j only if
+                                    block_mask[b][i / 128][j / 128] != 0, on top of the
+                                    causal and window limits.  Blocks that are zero are
+                                    skipped (no load, no MMA).  NULL = no mask. */
+    int32_t block_mask_q_blocks; /* >= ceil(max_seqlen_q / 128) when block_mask is set */
+    int32_t block_mask_k_blocks; /* >= ceil(max_seqlen_k / 128) when block_mask is set */
 } pa_prefill_params;
+#define PA_MASK_BLOCK 128
 
 pa_status pa_prefill(const pa_prefill_params *p, void *stream);
 

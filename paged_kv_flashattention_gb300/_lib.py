@@ -33,7 +33,8 @@ class PrefillParams(ctypes.Structure):
         ("page_size", c_i32), ("num_pages", c_i64), ("causal", c_i32), ("scale", c_f32),
         ("out", c_p), ("lse", c_p), ("lse_stride", c_i64),
         ("kv_dtype", c_i32), ("k_scale", c_p), ("v_scale", c_p), ("sliding_window", c_i32),
-        ("max_ctas", c_i32), ("scheduler", c_p),
+        ("max_ctas", c_i32), ("scheduler", c_p), ("block_mask", c_p), ("block_mask_q_blocks", c_i32),
+        ("block_mask_k_blocks", c_i32),
     ]
 
 

@@ -275,13 +275,17 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
             page_size: int | None = None, out: torch.Tensor | None = None,
             lse: torch.Tensor | None = None, k_scale: torch.Tensor | None = None,
             v_scale: torch.Tensor | None = None, sliding_window: int = 0,
-            max_ctas: int = 0, scheduler: torch.Tensor | None = None) -> torch.Tensor:
+            max_ctas: int = 0, scheduler: torch.Tensor | None = None,
+            block_mask: torch.Tensor | None = None) -> torch.Tensor:
     """Varlen prefill / extend attention.  q: bf16 [total_q, Hq, d];
     returns out bf16 [total_q, Hq, d]; lse (optional) fp32 [Hq, total_q].
     Pools are bf16, or E4M3 codes (uint8 / float8_e4m3fn) with fp32
     per-KV-head ``k_scale`` and ``v_scale``.  ``scheduler`` is the int32 [2]
     work-counter array of the launch (zero between launches); by default the
-    array cached for the current stream (``prefill_scheduler``)."""
+    array cached for the current stream (``prefill_scheduler``).
+    ``block_mask``: optional uint8 [B, nq, nk] on the device; entry
+    [b, i // 128, j // 128] == 0 hides key j from request b's query row i
+    (rows counted from the request's first row)."""
     dev = q.device
     num_pages, P, Hkv, d = _pool_geometry(k_cache, v_cache, page_size)
     _need(q, "q", torch.bfloat16, dev)
@@ -304,6 +308,10 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
         _need(lse, "lse", torch.float32, dev, contiguous=False)
         if lse.dim() != 2 or lse.shape[0] != Hq or lse.stride(1) != 1:
             raise ValueError("lse must be [Hq, >= total_q] with unit inner stride")
+    if block_mask is not None:
+        _need(block_mask, "block_mask", torch.uint8, dev)
+        if block_mask.dim() != 3 or block_mask.shape[0] != cu_seqlens_q.numel() - 1:
+            raise ValueError("block_mask must be [num_seqs, q_blocks, k_blocks]")
     if scheduler is None:
         scheduler = prefill_scheduler(dev)
     _need(scheduler, "scheduler", torch.int32, dev)
@@ -319,7 +327,9 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
         lse=_ptr(lse), lse_stride=(lse.stride(0) if lse is not None else 0), kv_dtype=kvd,
         k_scale=_ptr(k_scale) if kvd == PA_KV_FP8_E4M3 else None,
         v_scale=_ptr(v_scale) if kvd == PA_KV_FP8_E4M3 else None, sliding_window=int(sliding_window),
-        max_ctas=int(max_ctas), scheduler=_ptr(scheduler))
+        max_ctas=int(max_ctas), scheduler=_ptr(scheduler), block_mask=_ptr(block_mask),
+        block_mask_q_blocks=int(block_mask.shape[1]) if block_mask is not None else 0,
+        block_mask_k_blocks=int(block_mask.shape[2]) if block_mask is not None else 0)
     lib = _lib.load()
     _check(lib.pa_prefill(ctypes.byref(p), _stream(q)), lib)
     return out

@@ -271,6 +271,15 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
     if (p->sliding_window < 0) return fail(PA_ERR_INVALID, "sliding_window must be >= 0");
     if (p->max_ctas < 0) return fail(PA_ERR_INVALID, "max_ctas must be >= 0");
     if (p->scheduler == nullptr) return fail(PA_ERR_INVALID, "scheduler (device int32[2], zero-initialised) is NULL");
+    if (p->block_mask != nullptr) {
+        const int64_t need_q = ((int64_t)p->max_seqlen_q + PA_MASK_BLOCK - 1) / PA_MASK_BLOCK;
+        const int64_t need_k = ((int64_t)p->max_seqlen_k + PA_MASK_BLOCK - 1) / PA_MASK_BLOCK;
+        if (p->block_mask_q_blocks < need_q || p->block_mask_k_blocks < need_k || p->block_mask_q_blocks <= 0 ||
+            p->block_mask_k_blocks <= 0)
+            return fail(PA_ERR_INVALID, "block_mask of %d x %d blocks per request; %lld x %lld needed for max_seqlen_q %d, max_seqlen_k %d",
+                        p->block_mask_q_blocks, p->block_mask_k_blocks, (long long)need_q, (long long)need_k,
+                        p->max_seqlen_q, p->max_seqlen_k);
+    }
     if ((reinterpret_cast<uintptr_t>(p->scheduler) & 7u) != 0) return fail(PA_ERR_INVALID, "scheduler must be 8-byte aligned");
     cudaError_t e = launch_prefill(*p, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "prefill configuration not supported by this library");

@@ -110,20 +110,45 @@ struct PrefillArgs {
     const float *v_scale;
     int32_t *sched;               // caller's [0] next item, [1] CTAs finished; 0 between launches
     int32_t window;               // sliding window W (0 = none): keys >= position - (W - 1)
+    const uint8_t *bmask;         // block-sparse mask [num_seqs][bm_q][bm_k] over 128 x 128 blocks, or null
+    int32_t bm_q, bm_k;
 };
 
 // One work item: a 128-row query tile of T query heads of one request.
 struct PrefillItem {
-    int b, tile, h0, kvh, q0, Lk, off, rows_here, kv_end, n_kv, min_vis;
+    int b, tile, h0, kvh, q0, Lk, off, rows_here, kv_end, min_vis;
+    int n_all;    // 128-key steps from j0 up to the last key the tile sees
+    int n_kv;     // of those, the steps the block mask keeps (all of them without one)
     int j0;       // first 128-key step (a sliding window skips the ones before)
     int lo_max;   // keys below this are outside some row's window: mask there
+};
+
+// With a block-sparse mask an item's steps are the kept ones only: every
+// role walks them by ordinal 0 .. n_kv - 1 (barrier phases, first and last
+// step, load counts) and maps an ordinal to its step with a cursor, which
+// advances through the mask row of the item's query block.  Ordinals are
+// visited in increasing order.  Without a mask the map is the identity.
+struct StepCursor {
+    int idx = -1, step = -1;      // the idx-th kept step is `step` (relative to j0)
+    template <bool EXT>
+    __device__ __forceinline__ int at(const PrefillArgs &a, const PrefillItem &it, int i) {
+        if (!EXT || a.bmask == nullptr) return i;
+        if (i < idx) idx = step = -1;
+        const uint8_t *row = a.bmask + ((int64_t)it.b * a.bm_q + it.tile) * a.bm_k + it.j0;
+        while (idx < i) {
+            ++step;
+            while (row[step] == 0) ++step;   // the i-th kept step exists: i < n_kv
+            ++idx;
+        }
+        return step;
+    }
 };
 
 // Item v of the virtual list (k-th tile from the end of request b, head group
 // hp), k-major: every request's later, longer tiles come before its earlier
 // ones, so persistent CTAs taking items round robin start with the longest
 // work.  Returns false for a hole (request b has fewer than k + 1 tiles).
-template <int T, bool WIN = false>
+template <int T, bool EXT = false>
 __device__ __forceinline__ bool prefill_item(const PrefillArgs &a, int v, PrefillItem &it) {
     const int groups = a.num_q_heads / T;
     const int hp = v % groups;
@@ -153,12 +178,19 @@ __device__ __forceinline__ bool prefill_item(const PrefillArgs &a, int v, Prefil
     // bound fixes the first step, the last row's where masking stops
     it.j0 = 0;
     it.lo_max = 0;
-    if (WIN && a.window > 0) {
+    if (EXT && a.window > 0) {
         const int lo_first = it.off + it.tile * kBM - (a.window - 1);
         it.j0 = lo_first > 0 ? lo_first / kBN : 0;
         it.lo_max = lo_first + it.rows_here - 1;
         it.n_kv -= it.j0;
         if (it.n_kv < 0) it.n_kv = 0;
+    }
+    it.n_all = it.n_kv;
+    if (EXT && a.bmask != nullptr) {        // count the steps the block mask keeps
+        const uint8_t *row = a.bmask + ((int64_t)b * a.bm_q + it.tile) * a.bm_k + it.j0;
+        int kept = 0;
+        for (int j = 0; j < it.n_all; ++j) kept += row[j] != 0;
+        it.n_kv = kept;
     }
     return true;
 }
@@ -273,9 +305,9 @@ constexpr int kSoftmaxRegs = 184;
 constexpr int kItemRing = 4;      // items published ahead of the consumers
 constexpr int kControlRegs = 128;
 
-// WIN: the sliding-window instantiation (windowless launches keep the window
-// arithmetic out of their registers).
-template <int D, int T, bool F8, bool WIN>
+// EXT: the instantiation for sliding windows and block-sparse masks (plain
+// launches keep that arithmetic out of their registers).
+template <int D, int T, bool F8, bool EXT>
 __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
     using S = PrefillSmem<D, T, F8>;
     // A kernel launched after this one as a programmatic dependent (decode
@@ -360,23 +392,23 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
     // swizzled layout TMA would produce (rows past the visible keys are
     // zero), two key rows per instruction (16 lanes x 16 bytes per 256-byte
     // row at d = 128), as one copy group.
-    auto gather_rows = [&](const PrefillItem &it, int c, int (&rows)[kBN / 32]) {
+    auto gather_rows = [&](const PrefillItem &it, int st, int (&rows)[kBN / 32]) {
         const int32_t *pt = a.page_table + (int64_t)it.b * a.pt_stride;
-        const int key0 = (it.j0 + (c >> 1)) * kBN;
+        const int key0 = (it.j0 + st) * kBN;
 #pragma unroll
         for (int rr = 0; rr < kBN / 32; ++rr) {
             const int key = key0 + rr * 32 + lane;
             rows[rr] = key < it.kv_end ? pt[key] : -1;
         }
     };
-    auto gather_copy = [&](const PrefillItem &it, int c, int gl, const int (&rows)[kBN / 32]) {
+    auto gather_copy = [&](const PrefillItem &it, int c, int st, int gl, const int (&rows)[kBN / 32]) {
         if constexpr (F8) {
             // E4M3 rows of D bytes, copied as they are (row-major, no swizzle)
             constexpr int kChunks = D / 16;
             constexpr int kRowsPerIssue = 32 / kChunks;
             uint8_t *dst = land(gl % NS);
             const uint8_t *src = (c & 1) ? a.v_cache : a.k_cache;
-            const int key0 = (it.j0 + (c >> 1)) * kBN;
+            const int key0 = (it.j0 + st) * kBN;
             const int q = lane % kChunks, sub = lane / kChunks;
 #pragma unroll 1
             for (int rr = 0; rr < kBN / 32; ++rr) {
@@ -403,7 +435,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         constexpr int kRowsPerIssue = 32 / kChunks;   // 2 (d = 128) or 4 (d = 64)
         uint8_t *dst = smem + S::kRing + (gl % NS) * S::kTileBytes;
         const uint8_t *src = (c & 1) ? a.v_cache : a.k_cache;
-        const int key0 = (it.j0 + (c >> 1)) * kBN;
+        const int key0 = (it.j0 + st) * kBN;
         const int q = lane % kChunks;                 // this lane's chunk of a row
         const int hh = q / 8;
         const int sub = lane / kChunks;
@@ -440,13 +472,18 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         const int n = 2 * it.n_kv;
         int c = ((g - gl0) % kGatherWarps + kGatherWarps) % kGatherWarps;
         if (c >= n) return true;
+        StepCursor cur;
         int rows[kBN / 32];
-        gather_rows(it, c, rows);
+        int st = cur.at<EXT>(a, it, c >> 1);
+        gather_rows(it, st, rows);
         for (; c < n; c += kGatherWarps) {
             const int gl = gl0 + c;
             if (gl >= NS && !mbar_wait(&empty[gl % NS], ((gl / NS) - 1) & 1)) return false;
-            gather_copy(it, c, gl, rows);
-            if (c + kGatherWarps < n) gather_rows(it, c + kGatherWarps, rows);
+            gather_copy(it, c, st, gl, rows);
+            if (c + kGatherWarps < n) {
+                st = cur.at<EXT>(a, it, (c + kGatherWarps) >> 1);
+                gather_rows(it, st, rows);
+            }
             cp_async_wait_all();
             fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA
             mbar_arrive(&full[gl % NS]);
@@ -484,7 +521,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         // first slot of the page, num_slots (zero fill) when there is none or
         // the id is outside the pool.  Split so that the read is in flight
         // while the producer waits for a ring slot.
-        auto page_id = [&](const PrefillItem &it, int j) {
+        auto page_id = [&](const PrefillItem &it, int j) {      // j: the step (relative to j0)
             const int kk = (it.j0 + j) * kBN + lane * 16;
             return (lane < kBN / 16 && kk < it.kv_end) ? a.page_table[(int64_t)it.b * a.pt_stride + kk / 16] : -1;
         };
@@ -501,7 +538,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         // earlier: a CTA that holds an item it has not started keeps it from
         // CTAs that are idle at the end).
         for (int v; (v = take(local)) >= 0;) {
-            prefill_item<T, WIN>(a, v, it);
+            prefill_item<T, EXT>(a, v, it);
             // load 2j is K_j, 2j + 1 is V_j; gl counts loads over the CTA's
             // life.  The Q tiles are loaded once the previous item's last S
             // MMA is done.
@@ -518,11 +555,13 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                 return true;
             };
             if (paged16) {
-                int page = page_id(it, 0);              // pages of the current step
+                StepCursor cur;                         // load c belongs to kept step c >> 1
+                int st = cur.at<EXT>(a, it, 0);
+                int page = page_id(it, st);             // pages of the current step
                 int slot0 = a.num_slots;
                 ok = load_q();
                 for (int c = 0; ok && c < 2 * it.n_kv; ++c, ++gl) {
-                    if (!(c & 1)) slot0 = page_slot0(it, c >> 1, page);
+                    if (!(c & 1)) slot0 = page_slot0(it, st, page);
                     const int slot = gl % NS, round = gl / NS;
                     if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) { ok = false; break; }
                     uint8_t *dst = land(slot);
@@ -540,7 +579,10 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                         }
                     }
                     // K_j and V_j share pages; after K_j start reading the next step's
-                    if (!(c & 1) && c + 2 < 2 * it.n_kv) page = page_id(it, (c >> 1) + 1);
+                    if (!(c & 1) && c + 2 < 2 * it.n_kv) {
+                        st = cur.at<EXT>(a, it, (c >> 1) + 1);
+                        page = page_id(it, st);
+                    }
                 }
             } else {
                 ok = load_q() && gather_item(it, gl, 0);
@@ -563,7 +605,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             if (lane == 0) mbar_arrive(&item_empty[slot]);
             ++local;
             if (v < 0) break;
-            prefill_item<T, WIN>(a, v, it);
+            prefill_item<T, EXT>(a, v, it);
             if (!gather_item(it, gl, g)) break;
             gl += 2 * it.n_kv;
         }
@@ -580,7 +622,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
             __syncwarp();
             if (lane == 0) mbar_arrive(&item_empty[slot]);
             if (v < 0) break;
-            prefill_item<T, WIN>(a, v, it);
+            prefill_item<T, EXT>(a, v, it);
             // Q tiles: bf16 -> f16 of q * k_scale, in place
             if (!__all_sync(0xffffffffu, mbar_wait(q_full, local & 1))) break;
             ++local;
@@ -637,9 +679,9 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                 // 0 there, but 0 * NaN is not, so they become zeros (this
                 // warp's rows of the page that holds key kv_end - 1; later
                 // pages are zero-filled by the TMA).
-                if (c == 2 * it.n_kv - 1 && (it.kv_end & 15)) {
+                if (c == 2 * it.n_kv - 1 && (it.kv_end & 15) && StepCursor().at<EXT>(a, it, it.n_kv - 1) == it.n_all - 1) {
                     __syncwarp();
-                    const int kbase = (it.j0 + it.n_kv - 1) * kBN;
+                    const int kbase = (it.j0 + it.n_all - 1) * kBN;
                     const int r0 = max(it.kv_end - kbase, 64 * cw);
                     const int r1 = min(((it.kv_end + 15) & ~15) - kbase, 64 * cw + 64);
                     for (int i = lane; i < (r1 - r0) * (D / 8); i += 32) {
@@ -690,7 +732,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                 const int v = item_idx[slot];
                 mbar_arrive(&item_empty[slot]);
                 if (v < 0) break;
-                prefill_item<T, WIN>(a, v, it);
+                prefill_item<T, EXT>(a, v, it);
                 const int n_kv = it.n_kv;
                 if (!mbar_wait(F8 ? q_conv : q_full, local & 1)) break;
                 if (n_kv > 0) {
@@ -703,7 +745,8 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                 for (int j = 0; ok && j < n_kv; ++j) {
                     const int cv = gl + 2 * j + 1;
                     const uint64_t dv = dv0 + (uint64_t)(((cv % NC) * S::kTileBytes) >> 4);
-                    if (!F8 && paged16 && (it.kv_end & 15) && j + 1 == n_kv) {
+                    if (!F8 && paged16 && (it.kv_end & 15) && j + 1 == n_kv &&
+                        StepCursor().at<EXT>(a, it, j) == it.n_all - 1) {
                         // The last page of a request is loaded whole (one
                         // 16-token TMA box), so rows of the item's last V tile
                         // at keys >= kv_end hold slots the store never wrote.
@@ -713,7 +756,7 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
                         // while the softmax of this step still runs.  (FP8
                         // tiles are cleared by the widening warps.)
                         if (!wait_full(cv)) { ok = false; break; }
-                        const int kbase = (it.j0 + j) * kBN;
+                        const int kbase = (it.j0 + it.n_all - 1) * kBN;      // the item's last step
                         const int r0 = it.kv_end - kbase;                  // first row past the keys
                         const int r1 = ((it.kv_end + 15) & ~15) - kbase;   // end of its page
                         uint8_t *vt = land(cv % NS);
@@ -776,13 +819,14 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
         if (lane == 0) mbar_arrive(&item_empty[slot]);
         ++local;
         if (v < 0) break;
-        prefill_item<T, WIN>(a, v, it);
+        prefill_item<T, EXT>(a, v, it);
         const int n_kv = it.n_kv, Lk = it.Lk, off = it.off, min_vis = it.min_vis;
         const int qi = it.tile * kBM + r;             // query index within the request
         const bool row_valid = r < it.rows_here;
         const int vis_end = a.causal ? min(Lk, off + qi + 1) : Lk;   // keys [0, vis_end)
         float m_run = -INFINITY;
         float l_run = 0.f;
+        StepCursor cur;                               // ordinal j -> kept step
         // tcgen05.ld / st are warp-collective (.sync.aligned): every branch
         // that encloses one is warp-uniform, and the warp reconverges after
         // each (per-lane) barrier wait.
@@ -794,10 +838,10 @@ __global__ void __launch_bounds__(128 * (T + 1), 1) prefill_kernel(const __grid_
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) tmem_ld32(s_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
             tmem_wait_ld();
-            const int kbase = (it.j0 + j) * kBN;
-            if (kbase + kBN > min_vis || (WIN && kbase < it.lo_max)) {   // diagonal / end / window edge: mask
+            const int kbase = (it.j0 + cur.at<EXT>(a, it, j)) * kBN;
+            if (kbase + kBN > min_vis || (EXT && kbase < it.lo_max)) {   // diagonal / end / window edge: mask
                 const int lim = row_valid ? vis_end - kbase : kBN;
-                const int lo = (WIN && row_valid && a.window > 0) ? off + qi - (a.window - 1) - kbase : 0;
+                const int lo = (EXT && row_valid && a.window > 0) ? off + qi - (a.window - 1) - kbase : 0;
 #pragma unroll
                 for (int c = 0; c < kBN; ++c)
                     if (c >= lim || c < lo) sr[c] = __float_as_uint(-INFINITY);
@@ -964,13 +1008,13 @@ bool make_map_fp8(CUtensorMap *m, const void *base, int d, int heads, int64_t ro
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int T, bool F8, bool WIN>
+template <int D, int T, bool F8, bool EXT>
 cudaError_t launch_t(const PrefillArgs &a, dim3 grid, cudaStream_t stream) {
     using S = PrefillSmem<D, T, F8>;
     static_assert(S::kSlots >= 2 && (!F8 || S::kCSlots >= 2), "ring too small");
     // One CTA per SM (it allocates all 512 TMEM columns).
     const int smem = (S::kTotal + 1024) > 120 * 1024 ? (S::kTotal + 1024) : 120 * 1024;
-    auto kern = prefill_kernel<D, T, F8, WIN>;
+    auto kern = prefill_kernel<D, T, F8, EXT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, 128 * (T + 1), smem, stream>>>(a);
@@ -979,16 +1023,16 @@ cudaError_t launch_t(const PrefillArgs &a, dim3 grid, cudaStream_t stream) {
 
 }  // namespace
 
-template <bool WIN>
+template <bool EXT>
 cudaError_t dispatch_f8(const PrefillArgs &a, bool f8, int d, int T, dim3 grid, cudaStream_t stream) {
     if (f8) {
         if (d == 128)
-            return T == 2 ? launch_t<128, 2, true, WIN>(a, grid, stream) : launch_t<128, 1, true, WIN>(a, grid, stream);
-        return T == 2 ? launch_t<64, 2, true, WIN>(a, grid, stream) : launch_t<64, 1, true, WIN>(a, grid, stream);
+            return T == 2 ? launch_t<128, 2, true, EXT>(a, grid, stream) : launch_t<128, 1, true, EXT>(a, grid, stream);
+        return T == 2 ? launch_t<64, 2, true, EXT>(a, grid, stream) : launch_t<64, 1, true, EXT>(a, grid, stream);
     }
     if (d == 128)
-        return T == 2 ? launch_t<128, 2, false, WIN>(a, grid, stream) : launch_t<128, 1, false, WIN>(a, grid, stream);
-    return T == 2 ? launch_t<64, 2, false, WIN>(a, grid, stream) : launch_t<64, 1, false, WIN>(a, grid, stream);
+        return T == 2 ? launch_t<128, 2, false, EXT>(a, grid, stream) : launch_t<128, 1, false, EXT>(a, grid, stream);
+    return T == 2 ? launch_t<64, 2, false, EXT>(a, grid, stream) : launch_t<64, 1, false, EXT>(a, grid, stream);
 }
 
 cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
@@ -1004,6 +1048,9 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     a.k_scale = p.k_scale;
     a.v_scale = p.v_scale;
     a.window = p.sliding_window;
+    a.bmask = p.block_mask;
+    a.bm_q = p.block_mask_q_blocks;
+    a.bm_k = p.block_mask_k_blocks;
     a.k_cache = static_cast<const uint8_t *>(p.k_cache);
     a.v_cache = static_cast<const uint8_t *>(p.v_cache);
     a.page_table = p.page_table;
@@ -1034,8 +1081,8 @@ cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream) {
     int64_t ctas = num_sms();
     if (p.max_ctas > 0 && p.max_ctas < ctas) ctas = p.max_ctas;   // leave SMs to a concurrent launch
     dim3 grid((unsigned)(virt < ctas ? virt : ctas));
-    return a.window > 0 ? dispatch_f8<true>(a, f8, p.head_dim, T, grid, stream)
-                        : dispatch_f8<false>(a, f8, p.head_dim, T, grid, stream);
+    return (a.window > 0 || a.bmask != nullptr) ? dispatch_f8<true>(a, f8, p.head_dim, T, grid, stream)
+                                                : dispatch_f8<false>(a, f8, p.head_dim, T, grid, stream);
 }
 
 }  // namespace pa
