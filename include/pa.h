@@ -38,6 +38,8 @@
  *    a request with Lq queries and Lk keys sees keys 0 .. Lk - Lq + i
  *    (cached prefix, then the extend tokens; [M]).
  *  - A query row that sees no key yields O = 0 and lse = -inf.
+ *  - Masks: causal (end-aligned), sliding window, and for pa_prefill a
+ *    block-sparse mask over 128 x 128 blocks (pa_prefill_params.block_mask).
  *  - Supported: head_dim 64 or 128; page_size 1 or 16; Hq % Hkv == 0 with
  *    group size Hq / Hkv in {1, 2, 4, 8}; Hkv * head_dim <= 4096.
  *  - Every device pointer must be 16-byte aligned.  The library allocates
