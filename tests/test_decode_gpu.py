@@ -160,3 +160,43 @@ def test_lse_combine(cuda_device, d):
     mask = np.arange(S)[None, :] < n[:, None]
     ref_o, ref_l = online.merge_partials(np.where(mask[..., None], o, 0.0), np.where(mask, l, -np.inf))
     compare(out, ref_o, f"lse_combine d{d}", lse_gpu=lse, lse_ref=ref_l)
+
+
+def _shared_prefix_problem(seed, decode, page, d=128):
+    """Requests 1 and 3 start with request 0's pages (a cached prefix shared
+    through the page table, PagedAttention's block sharing), request 2 with
+    request 1's; each then continues on pages of its own."""
+    cached = [300, 310, 350, 20] if not decode else [300, 333, 400, 40]
+    ext = [1, 1, 1, 1] if decode else [40, 130, 64, 17]
+    n = 256 // page                                      # shared pages: the first 256 keys
+    return W.small_problem(seed, cached, ext, num_q_heads=8, num_kv_heads=2, head_dim=d, page_size=page,
+                           shared_prefix_pages={1: (0, n), 2: (1, n), 3: (0, 1)})
+
+
+@pytest.mark.parametrize("page", [1, 16])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_shared_prefix_pages(cuda_device, page, fp8):
+    """Several requests whose page tables point at the same physical pages,
+    through pa_decode and pa_prefill, against the oracle (which reads them
+    through the same tables)."""
+    for decode in (True, False):
+        p = _shared_prefix_problem(900 + page + 2 * fp8 + 4 * decode, decode, page)
+        pl = p.meta["page_lists"]
+        assert pl[1][:256 // page] == pl[0][:256 // page] and pl[2][:256 // page] == pl[1][:256 // page]
+        what = f"shared prefix {'decode' if decode else 'prefill'} P{page}{' fp8' if fp8 else ''}"
+        if fp8:
+            from test_fp8_gpu import FP8Problem
+            f = FP8Problem(p, cuda_device, 950 + page)
+            out, lse = f.decode() if decode else f.prefill()
+            torch.cuda.synchronize()
+            ref, ref_lse = f.oracle()
+        else:
+            dp = DeviceProblem(p, cuda_device)
+            dp.store()
+            out, lse = dp.decode() if decode else dp.prefill()
+            torch.cuda.synchronize()
+            ref, ref_lse = oracle_ref(p)
+        if decode:
+            compare(out, ref.reshape(out.shape), what, lse_gpu=lse, lse_ref=ref_lse.reshape(lse.shape))
+        else:
+            compare(out, ref, what, lse_gpu=lse[:, :ref.shape[0]].T.contiguous(), lse_ref=ref_lse)
