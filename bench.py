@@ -60,17 +60,30 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def ncu_traffic(kernel_file: str, summary: str):
+def source_sha256(kernel_files) -> str:
+    """sha256 of the kernel's source files (csrc/, in the order given)."""
+    h = hashlib.sha256()
+    for f in kernel_files:
+        h.update(open(os.path.join(ROOT, "paged_kv_flashattention_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel_files, summary: str):
     """DRAM bytes per launch from a committed ncu summary, or None when the
-    kernel source changed since the capture (the summary records its hash)."""
+    kernel's sources changed since the capture (the summary records their
+    hash, source_sha256(kernel_files))."""
     try:
         text = open(os.path.join(ROOT, "profiles", summary)).read()
         want = re.search(r"source_sha256:\s*([0-9a-f]{64})", text).group(1)
         bytes_ = float(re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", text).group(1))
-        src = open(os.path.join(ROOT, "paged_kv_flashattention_gb300", "csrc", kernel_file), "rb").read()
-        return bytes_ if hashlib.sha256(src).hexdigest() == want else None
+        return bytes_ if source_sha256(kernel_files) == want else None
     except Exception:
         return None
+
+
+# the sources of the two attention passes the roofline names
+MIXED_SOURCES = ("mixed.cu", "prefill_impl.cuh", "decode_impl.cuh", "pa_device.cuh", "decode.cu")
+DECODE_SOURCES = ("decode.cu", "decode_impl.cuh", "pa_device.cuh")
 
 
 # --------------------------------------------------------------------------
@@ -165,7 +178,7 @@ class MixedBatch:
         self.max_dec = int(d.device_len.max())
         self.out_dec = torch.empty_like(self.q_dec)
         self.out_pre = torch.empty_like(self.q_pre)
-        ws = pa.decode_workspace_size(self.q_dec.shape, self.k_cache, self.max_dec)
+        ws = pa.decode_workspace_size(self.q_dec.shape, self.k_cache, self.max_dec, kv_chunk=256)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         self.pt_dec = torch.empty((d.num_seqs, -(-self.max_dec // self.P)), dtype=torch.int32, device=dev)
         self.pt_pre = torch.empty((p.num_seqs, -(-int(p.device_len.max()) // self.P)), dtype=torch.int32,
@@ -181,6 +194,13 @@ class MixedBatch:
         self.launches_per_step = 6   # store, 2 page tables, prefill, decode split + combine
         self.num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
         self.prefill_sms = 12        # overlapped schedule (0: phases in sequence)
+        # "overlap": prefill on prefill_sms SMs, decode as its programmatic
+        # dependent on the rest; "fused": both halves in one persistent launch
+        # (pa_mixed_batch); "sequential": one phase after the other
+        self.schedule = "fused"
+        self.mixed_sched = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.fused_prefill_ctas = 12   # fused schedule: CTAs that take prefill tiles first (0 = automatic)
+        self.fused_kv_chunk = 256      # fused schedule: the decode split layout's unit
         from paged_kv_flashattention_gb300.metadata import MetadataBuilder
         self.meta_dec = MetadataBuilder(dev, d.num_seqs)
         self.meta_pre = MetadataBuilder(dev, p.num_seqs)
@@ -193,7 +213,8 @@ class MixedBatch:
         other, with events between them."""
         torch, pa = self.torch, self.pa
         if concurrent is None:
-            concurrent = not timing and self.prefill_sms > 0
+            concurrent = not timing and self.prefill_sms > 0 and self.schedule == "overlap"
+        fused = not timing and self.schedule == "fused"
         ev = None
         if timing:
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
@@ -205,6 +226,10 @@ class MixedBatch:
                                    self.idx_pre, self.P, page_table_out=self.pt_pre)
         if timing:
             ev[1].record()
+        if fused:
+            self._keep = (md, mp)
+            self.fused_pass()
+            return ev
         pa.prefill(self.q_pre, self.k_cache, self.v_cache, mp.page_table, mp.cu_seqlens_q, mp.cu_seqlens_k,
                    mp.max_seqlen_q, mp.max_seqlen_k, causal=True, out=self.out_pre,
                    max_ctas=self.prefill_sms if concurrent else 0)
@@ -218,6 +243,81 @@ class MixedBatch:
             ev[3].record()
         self._keep = (md, mp)
         return ev
+
+
+def _fused_pass(self):
+    """The attention of one step in one launch (pa_mixed_batch: prefill and
+    split-KV decode, then the combine) on the last step's metadata."""
+    md, mp = self._keep
+    self.pa.mixed_batch(self.q_pre, self.q_dec, self.k_cache, self.v_cache, mp.page_table, mp.cu_seqlens_q,
+                        mp.cu_seqlens_k, mp.max_seqlen_q, mp.max_seqlen_k, md.page_table, md.cache_seqlens,
+                        md.max_seqlen_k, causal=True, out_prefill=self.out_pre, out_decode=self.out_dec,
+                        workspace=self.workspace, scheduler=self.mixed_sched,
+                        prefill_ctas=self.fused_prefill_ctas, kv_chunk=self.fused_kv_chunk)
+
+
+MixedBatch.fused_pass = _fused_pass
+
+
+def schedule_text(mb) -> str:
+    if mb.schedule == "fused":
+        n = mb.fused_prefill_ctas or "automatically chosen"
+        return (f"prefill and decode in one persistent launch: {n} CTAs take the prefill tiles first, the "
+                f"others start on decode key ranges at once (T-ranges of {mb.fused_kv_chunk} keys), then "
+                f"the LSE combine")
+    if mb.schedule == "overlap" and mb.prefill_sms > 0:
+        return f"prefill on {mb.prefill_sms} SMs overlapped with decode on the other {mb.num_sms - mb.prefill_sms}"
+    return "phases in sequence"
+
+
+def schedule_compare(mb, steps: int) -> dict:
+    """Median step time of every schedule of the same step (events around
+    every step, back to back), the chosen one restored afterwards."""
+    import torch
+    keep = mb.schedule, mb.prefill_sms, mb.fused_prefill_ctas, mb.fused_kv_chunk
+    out = {}
+    runs = [("overlap", "overlap", keep[1] or 12, 0, 0), ("sequential", "sequential", 0, 0, 0),
+            ("fused", "fused", 0, keep[2], keep[3]), ("fused_prefill_share_automatic", "fused", 0, 0, keep[3]),
+            ("fused_prefill_on_all_ctas", "fused", 0, mb.num_sms, keep[3]),
+            ("fused_ranges_1024", "fused", 0, keep[2], 1024)]
+    for name, sched, sms, fpc, kc in runs:
+        mb.schedule, mb.prefill_sms, mb.fused_prefill_ctas, mb.fused_kv_chunk = sched, sms, fpc, kc
+        for _ in range(3):
+            mb.step()
+        pairs = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            mb.step()
+            b.record()
+            pairs.append((a, b))
+        torch.cuda.synchronize()
+        t = sorted(a.elapsed_time(b) for a, b in pairs)
+        out[name] = {"ms_median": round(_pct(t, 50), 4), "ms_p95": round(_pct(t, 95), 4),
+                     "gbs": round(mb.step_bytes / (_pct(t, 50) * 1e-3) / 1e9, 1)}
+    mb.schedule, mb.prefill_sms, mb.fused_prefill_ctas, mb.fused_kv_chunk = keep
+    return out
+
+
+
+def roofline_block(mb, fused_ms, dec_gbs, peaks, peak_src) -> dict:
+    """The dominant kernel of the timed step against the measured HBM copy
+    peak: the mixed-batch launch (with its combine) under the fused schedule,
+    else the decode pass (split kernel + combine)."""
+    if fused_ms:
+        ms = _pct(fused_ms, 50)
+        nbytes = mb.decode_bytes + mb.prefill_bytes
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": "mixed-batch launch (prefill tiles and split-KV decode in one "
+                "persistent kernel) + LSE combine", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": peak_src,
+                "bytes_per_launch": nbytes, "ms_median": round(ms, 4), "ms_p95": round(_pct(fused_ms, 95), 4),
+                "traffic": ncu_traffic(MIXED_SOURCES, "mixed_batch_launch.md")}
+    return {"bound": "hbm", "kernel": "decode pass (split-KV kernel + LSE combine)",
+            "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "peak_source": peak_src,
+            "bytes_per_launch": mb.decode_bytes,
+            "traffic": ncu_traffic(DECODE_SOURCES, "decode_mixed_batch.md")}
 
 
 def _pct(sorted_vals, q):
@@ -292,6 +392,13 @@ def run_gpu(args):
 
     mb = MixedBatch(dev)
     mb.prefill_sms = args.prefill_sms
+    mb.schedule = args.schedule
+    mb.fused_prefill_ctas = args.fused_prefill_ctas
+    mb.fused_kv_chunk = args.fused_kv_chunk
+    if mb.schedule == "fused":
+        mb.launches_per_step = 5     # store, 2 page tables, mixed prefill+decode, combine
+    elif mb.schedule == "sequential":
+        mb.prefill_sms = 0
     torch.cuda.synchronize()
 
     def barrier():
@@ -344,6 +451,20 @@ def run_gpu(args):
         phase["store_meta"].append(e[0].elapsed_time(e[1]))
         phase["prefill"].append(e[1].elapsed_time(e[2]))
         phase["decode"].append(e[2].elapsed_time(e[3]))
+    # ---- the attention of the timed step on its own (fused schedule): one
+    # pa_mixed_batch per iteration (mixed kernel + combine), events around each
+    fused_ms = []
+    if mb.schedule == "fused":
+        pairs = []
+        for _ in range(args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            mb.fused_pass()
+            b.record()
+            pairs.append((a, b))
+        torch.cuda.synchronize()
+        fused_ms = sorted(a.elapsed_time(b) for a, b in pairs)
+    barrier()
     ms_step = max_over_ranks(total_ms, world, dev) / args.steps
     from paged_kv_flashattention_gb300 import device_error
     dev_err = device_error()
@@ -437,14 +558,9 @@ def run_gpu(args):
                    f"{mb.decode_bytes / 1e9:.2f} GB per step; no flush)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "step": "store_kv + metadata (2 batches) + prefill + decode(split+combine)",
-                   "schedule": (f"prefill on {mb.prefill_sms} SMs overlapped with decode on the other "
-                                f"{mb.num_sms - mb.prefill_sms}" if mb.prefill_sms > 0 else "phases in sequence"),
+                   "schedule": schedule_text(mb),
                    "step_bytes": mb.step_bytes},
-        "roofline": {"bound": "hbm", "kernel": "decode pass (split-KV kernel + LSE combine)",
-                     "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "peak_source": peak_src,
-                     "bytes_per_launch": mb.decode_bytes,
-                     "traffic": ncu_traffic("decode.cu", "decode_mixed_batch.md")},
+        "roofline": roofline_block(mb, fused_ms, dec_gbs, peaks, peak_src),
         "decode": {"ms": round(dec_ms, 4), "gbs": round(dec_gbs, 1),
                    "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4),
                    "frac_hbm_spec_8tbs": round(dec_gbs / 8000.0, 4),
@@ -468,6 +584,9 @@ def run_gpu(args):
         "clocks": clk.summary(),
         "device_error": dev_err,
     }
+    if rank == 0:
+        line["schedules"] = schedule_compare(mb, args.steps)
+        line["device_error"] |= device_error()
     if rank == 0 and not args.no_configs:
         line["configs"] = config_block(dev, peaks, args)
         line["device_error"] |= device_error()
@@ -612,6 +731,9 @@ MICRO_CASES = {
     # the extend batch under a block-sparse mask keeping half of the 128 x
     # 128 blocks (and every diagonal block): the skipped blocks cost nothing
     "extend_partial_hit_p16_mask50": (4, None, "prefill"),
+    # decode_64seq_logu's sequences and two 2048-token prefill chunks over one
+    # pool, in one mixed-batch launch (automatic prefill share, 256-key T-ranges)
+    "mixed_64seq_logu": (None, None, "mixed"),
 }
 
 
@@ -639,7 +761,11 @@ def micro_problem(name):
         return W.config(cfg, variant), kernel
     rng = np.random.default_rng(W.SEED_BASE + 70)
     Lk = np.exp(rng.uniform(math.log(512), math.log(32768), size=64)).astype(np.int32)
-    p = W.build(name.replace("_fp8", ""), cached_len=Lk - 1, extend_len=np.ones(64, np.int32), num_q_heads=32,
+    cached, ext = Lk - 1, np.ones(64, np.int32)
+    if kernel == "mixed":          # then the two prefill chunks, no cached prefix
+        cached = np.concatenate([cached, [0, 0]]).astype(np.int32)
+        ext = np.concatenate([ext, [2048, 2048]]).astype(np.int32)
+    p = W.build(name.replace("_fp8", ""), cached_len=cached, extend_len=ext, num_q_heads=32,
                 num_kv_heads=8, head_dim=128, page_size=16, seed=W.SEED_BASE + 71, pool_factor=1.1)
     return p, kernel
 
@@ -696,6 +822,26 @@ def prepare_case(name, dev):
         # bytes a perfect kernel moves: Q read, O written, each request's K/V read once
         extra["bytes"] = 2 * q.numel() * 2 + int(p.device_len.astype(np.int64).sum()) * Hkv * D * 2 * kc.element_size()
         extra["tokens"] = int(E.sum())
+    elif kernel == "mixed":
+        nd = p.num_seqs - 2
+        tt, idx = torch.from_numpy(p.token_table).to(dev), torch.from_numpy(p.table_idx).to(dev)
+        md = metadata.prepare(p.cached_len[:nd], p.extend_len[:nd], tt, idx[:nd], p.page_size)
+        mp = metadata.prepare(p.cached_len[nd:], p.extend_len[nd:], tt, idx[nd:], p.page_size)
+        qd, qp = q[:nd], q[nd:]
+        od, op = torch.empty_like(qd), torch.empty_like(qp)
+        ws = torch.empty(pa.decode_workspace_size(qd.shape, kc, md.max_seqlen_k, kv_chunk=256),
+                         dtype=torch.uint8, device=dev)
+        sched = torch.zeros(4, dtype=torch.int32, device=dev)
+        fn = lambda: pa.mixed_batch(qp, qd, kc, vc, mp.page_table, mp.cu_seqlens_q, mp.cu_seqlens_k,
+                                    mp.max_seqlen_q, mp.max_seqlen_k, md.page_table, md.cache_seqlens,
+                                    md.max_seqlen_k, scale=p.scale, out_prefill=op, out_decode=od, workspace=ws,
+                                    scheduler=sched, kv_chunk=256)
+        kv_row = Hkv * D * 2 * kc.element_size()
+        work = (int(p.device_len[:nd].astype(np.int64).sum()) * kv_row + 2 * qd.numel() * 2 +
+                int(p.device_len[nd:].astype(np.int64).sum()) * kv_row + 2 * qp.numel() * 2)
+        unit = "GB/s"
+        extra["seqs"] = nd
+        extra["tokens"] = int(p.extend_len[nd:].sum())
     elif kernel == "rope":
         table = pa.rope_cos_sin_table(int(p.device_len.max()) + 1, D, 10000.0).to(dev)
         pos = torch.from_numpy(np.concatenate([np.arange(c, c + e) for c, e in zip(p.cached_len, p.extend_len)])
@@ -775,6 +921,13 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-sms", type=int, default=12,
                     help="SMs the prefill gets while decode runs beside it (0 = one after the other)")
+    ap.add_argument("--schedule", choices=["overlap", "fused", "sequential"], default="fused",
+                    help="how one step runs its prefill and decode halves")
+    ap.add_argument("--fused-prefill-ctas", type=int, default=12,
+                    help="fused schedule: CTAs that take prefill tiles before decode ranges "
+                         "(0 = chosen by the kernel from the work)")
+    ap.add_argument("--fused-kv-chunk", type=int, default=256,
+                    help="fused schedule: keys per T-range of the decode split layout")
     ap.add_argument("--ref-cap-gb", type=float, default=2.0,
                     help="K/V bytes of the decode sample the reference arm times per step (the "
                          "cpu_baseline leg's sample at the default)")

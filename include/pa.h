@@ -11,6 +11,7 @@
  *   pa_prefill           varlen causal prefill / extend attention
  *   pa_decode            one-query-per-sequence split-KV decode attention
  *   pa_decode_noalloc    the same, with fixed library-owned split scratch
+ *   pa_mixed_batch       a continuous batch (prefill + decode) in one launch
  *   pa_lse_combine       merge of split partial results by log-sum-exp
  *
  * Sources (web pages; section names as printed on them):
@@ -344,6 +345,36 @@ size_t pa_decode_workspace_size(const pa_decode_params *p);
 int32_t pa_decode_kv_chunk(const pa_decode_params *p);
 
 pa_status pa_decode(const pa_decode_params *p, void *stream);
+
+/*
+ * pa_mixed_batch - one continuous batch of a serving engine ([T] s.13: the
+ * prefill and decode phases; [M] runs them as one batch): the prefill /
+ * extend requests of `pre` and the decode sequences of `dec`, over the SAME
+ * pools, in one persistent launch (plus the decode combine as a dependent
+ * second launch).  The first n CTAs (one CTA per SM) take prefill work
+ * items first; every CTA takes decode key ranges once it has no prefill
+ * work, so CTAs without prefill work start on decode at once and the
+ * tensor-bound prefill runs under the HBM-bound decode read.  n =
+ * pre->max_ctas when > 0 (at most the SM count); 0 = chosen in the kernel
+ * from the work of both halves (the prefill's attended (query, key) pairs
+ * and the decode's K/V bytes, at rates measured for these kernels).  A
+ * smaller dec->kv_chunk (the split layout's unit; the workspace grows as it
+ * shrinks) balances the end of the decode more finely.  Results are those of pa_prefill(pre) and
+ * pa_decode(dec) (decode may split its key ranges differently; the combine
+ * is exact up to rounding).
+ *  - pre->scheduler must hold PA_MIXED_SCHEDULER_INTS int32 (zero before its
+ *    first use, left zero by every completed launch: [0..1] the prefill
+ *    counters, [2..3] the decode ones); dec->workspace as for pa_decode.
+ *  - Both halves: bf16 pools, the same k_cache / v_cache / num_pages /
+ *    page_size / head counts / head_dim; an even GQA group and
+ *    num_kv_heads % 4 == 0; no window or block mask on the prefill half (a
+ *    decode window is fine); dec->overlap_previous = 0, max_ctas ignored.
+ *    Otherwise PA_ERR_UNSUPPORTED / PA_ERR_INVALID, nothing launched.
+ *  - A batch with no prefill rows is pa_decode(dec); one with no decode
+ *    sequences pa_prefill(pre).
+ */
+#define PA_MIXED_SCHEDULER_INTS 4
+pa_status pa_mixed_batch(const pa_prefill_params *pre, const pa_decode_params *dec, void *stream);
 
 /*
  * pa_decode_noalloc - pa_decode for callers that cannot allocate device

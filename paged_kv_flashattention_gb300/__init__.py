@@ -9,15 +9,16 @@ memory and streams only.
 """
 from .api import (PA_KV_BF16, PA_KV_FP8_E4M3, PagedAttentionError, abi_version, build_page_table,
                   build_seqlens, decode, decode_noalloc, decode_kv_chunk, decode_workspace_size,
-                  device_error, lse_combine, prefill, rope_cos_sin_table, rope_store_kv, store_kv,
-                  store_kv_fp8)
+                  device_error, lse_combine, mixed_batch, prefill, prefill_scheduler, rope_cos_sin_table,
+                  rope_store_kv, store_kv, store_kv_fp8)
 
 from .graphs import DecodeGraphRunner, bucket_for
 
 __all__ = [
     "PagedAttentionError", "abi_version", "build_page_table", "build_seqlens", "decode",
     "decode_noalloc",
-    "decode_kv_chunk", "decode_workspace_size", "device_error", "lse_combine", "prefill",
+    "decode_kv_chunk", "decode_workspace_size", "device_error", "lse_combine", "mixed_batch", "prefill",
+    "prefill_scheduler",
     "DecodeGraphRunner", "bucket_for",
     "store_kv", "store_kv_fp8", "PA_KV_BF16", "PA_KV_FP8_E4M3", "rope_cos_sin_table", "rope_store_kv",
 ]

@@ -78,6 +78,7 @@ SIGNATURES = {
     "pa_decode_kv_chunk": (c_i32, [ctypes.POINTER(DecodeParams)]),
     "pa_decode": (ctypes.c_int, [ctypes.POINTER(DecodeParams), c_p]),
     "pa_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(DecodeParams), c_p]),
+    "pa_mixed_batch": (ctypes.c_int, [ctypes.POINTER(PrefillParams), ctypes.POINTER(DecodeParams), c_p]),
     "pa_lse_combine": (ctypes.c_int, [c_p, c_p, c_p, c_i32, c_i32, c_i32, c_p, c_p, c_p]),
 }
 

@@ -251,12 +251,13 @@ def _pool_geometry(k_cache: torch.Tensor, v_cache: torch.Tensor, page_size: int 
 _sched_lock = threading.Lock()
 _sched_arrays: dict = {}
 PA_PREFILL_SCHEDULER_INTS = 2
+PA_MIXED_SCHEDULER_INTS = 4
 
 
 def prefill_scheduler(device=None, stream=None) -> torch.Tensor:
-    """The cached zeroed int32 [2] scheduler array for (device, stream):
-    the default of ``prefill(scheduler=None)``.  Create it before capturing a
-    CUDA graph that calls prefill on that stream."""
+    """The cached zeroed int32 [4] scheduler array for (device, stream):
+    the default of ``prefill(scheduler=None)`` and ``mixed_batch``.  Create
+    it before capturing a CUDA graph that calls either on that stream."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
@@ -264,7 +265,7 @@ def prefill_scheduler(device=None, stream=None) -> torch.Tensor:
     with _sched_lock:
         t = _sched_arrays.get(key)
         if t is None:
-            t = torch.zeros(PA_PREFILL_SCHEDULER_INTS, dtype=torch.int32, device=dev)
+            t = torch.zeros(PA_MIXED_SCHEDULER_INTS, dtype=torch.int32, device=dev)
             _sched_arrays[key] = t
         return t
 
@@ -286,6 +287,17 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
     ``block_mask``: optional uint8 [B, nq, nk] on the device; entry
     [b, i // 128, j // 128] == 0 hides key j from request b's query row i
     (rows counted from the request's first row)."""
+    p, out = _prefill_params(q, k_cache, v_cache, page_table, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                             max_seqlen_k, causal, scale, page_size, out, lse, k_scale, v_scale, sliding_window,
+                             max_ctas, scheduler, block_mask, PA_PREFILL_SCHEDULER_INTS)
+    lib = _lib.load()
+    _check(lib.pa_prefill(ctypes.byref(p), _stream(q)), lib)
+    return out
+
+
+def _prefill_params(q, k_cache, v_cache, page_table, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                    causal, scale, page_size, out, lse, k_scale, v_scale, sliding_window, max_ctas, scheduler,
+                    block_mask, sched_ints):
     dev = q.device
     num_pages, P, Hkv, d = _pool_geometry(k_cache, v_cache, page_size)
     _need(q, "q", torch.bfloat16, dev)
@@ -315,8 +327,8 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
     if scheduler is None:
         scheduler = prefill_scheduler(dev)
     _need(scheduler, "scheduler", torch.int32, dev)
-    if scheduler.numel() < PA_PREFILL_SCHEDULER_INTS:
-        raise ValueError("scheduler must hold 2 int32")
+    if scheduler.numel() < sched_ints:
+        raise ValueError(f"scheduler must hold {sched_ints} int32")
     p = _lib.PrefillParams(
         q=_ptr(q), k_cache=_ptr(k_cache), v_cache=_ptr(v_cache), page_table=_ptr(page_table),
         page_table_stride=page_table.stride(0), total_q=total_q, cu_seqlens_q=_ptr(cu_seqlens_q),
@@ -330,9 +342,7 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_
         max_ctas=int(max_ctas), scheduler=_ptr(scheduler), block_mask=_ptr(block_mask),
         block_mask_q_blocks=int(block_mask.shape[1]) if block_mask is not None else 0,
         block_mask_k_blocks=int(block_mask.shape[2]) if block_mask is not None else 0)
-    lib = _lib.load()
-    _check(lib.pa_prefill(ctypes.byref(p), _stream(q)), lib)
-    return out
+    return p, out
 
 
 def _decode_params(q, k_cache, v_cache, page_table, cache_seqlens, max_seqlen_k, scale, page_size,
@@ -414,6 +424,41 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_t
     lib = _lib.load()
     _check(lib.pa_decode(ctypes.byref(p), _stream(q)), lib)
     return out
+
+
+def mixed_batch(q_prefill: torch.Tensor, q_decode: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                page_table_prefill: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                max_seqlen_q: int, max_seqlen_k_prefill: int, page_table_decode: torch.Tensor,
+                cache_seqlens: torch.Tensor, max_seqlen_k_decode: int, *, causal: bool = True,
+                scale: float | None = None, out_prefill: torch.Tensor | None = None,
+                out_decode: torch.Tensor | None = None, lse_prefill: torch.Tensor | None = None,
+                lse_decode: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                kv_chunk: int = 0, scheduler: torch.Tensor | None = None, prefill_ctas: int = 0):
+    """One continuous batch in one launch (``pa_mixed_batch``): prefill /
+    extend of ``q_prefill`` [total_q, Hq, d] (cu_seqlens_q/k, its page table)
+    and decode of ``q_decode`` [B, Hq, d] (cache_seqlens, its page table)
+    over the same bf16 pools.  ``prefill_ctas`` > 0: that many CTAs take
+    prefill tiles before decode key ranges (the others start on decode at
+    once); 0: the kernel chooses the count from the work of both halves.
+    Returns (out_prefill, out_decode)."""
+    dev = q_prefill.device
+    p, out_prefill = _prefill_params(q_prefill, k_cache, v_cache, page_table_prefill, cu_seqlens_q, cu_seqlens_k,
+                                     max_seqlen_q, max_seqlen_k_prefill, causal, scale, None, out_prefill,
+                                     lse_prefill, None, None, 0, int(prefill_ctas), scheduler, None,
+                                     PA_MIXED_SCHEDULER_INTS)
+    _need(q_decode, "q_decode", torch.bfloat16, dev)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, dev)
+    _need(page_table_decode, "page_table_decode", torch.int32, dev, contiguous=False)
+    if out_decode is None:
+        out_decode = torch.empty_like(q_decode)
+    need = decode_workspace_size(q_decode.shape, k_cache, max_seqlen_k_decode, kv_chunk=kv_chunk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    dp = _decode_params(q_decode, k_cache, v_cache, page_table_decode, cache_seqlens, max_seqlen_k_decode, scale,
+                        None, out_decode, lse_decode, workspace, kv_chunk)
+    lib = _lib.load()
+    _check(lib.pa_mixed_batch(ctypes.byref(p), ctypes.byref(dp), _stream(q_prefill)), lib)
+    return out_prefill, out_decode
 
 
 def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

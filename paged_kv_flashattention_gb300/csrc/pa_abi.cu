@@ -86,7 +86,7 @@ const char *pa_last_error(void) { return pa::g_last_error; }
 pa_status pa_device_error(int32_t *bits, void *stream) {
     if (bits == nullptr) return fail(PA_ERR_INVALID, "bits is NULL");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t (*getters[])(int **) = {error_word_store, error_word_decode, error_word_prefill};
+    cudaError_t (*getters[])(int **) = {error_word_store, error_word_decode, error_word_prefill, error_word_mixed};
     int32_t acc = 0;
     for (auto get : getters) {
         int *addr = nullptr;
@@ -237,8 +237,10 @@ pa_status pa_build_page_table(const int32_t *token_table, int64_t token_table_st
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "build_page_table launch");
 }
 
-pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
-    g_last_error[0] = 0;
+// Validation of a pa_prefill call; *nothing = the call has no query rows
+// (then the remaining checks are skipped and nothing is launched).
+static pa_status check_prefill(const pa_prefill_params *p, bool *nothing) {
+    *nothing = false;
     if (p == nullptr) return fail(PA_ERR_INVALID, "params is NULL");
     pa_status st = check_heads(p->num_q_heads, p->num_kv_heads, p->head_dim, p->page_size);
     if (st != PA_OK) return st;
@@ -253,7 +255,10 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
     // masked key would be NaN); decode keeps the same rule.
     if (!(p->scale > 0.f) || p->scale == INFINITY) return fail(PA_ERR_INVALID, "scale must be finite and > 0");
     if (p->total_q < 0) return fail(PA_ERR_INVALID, "total_q < 0");
-    if (p->num_seqs == 0 || p->max_seqlen_q == 0 || p->total_q == 0) return PA_OK;
+    if (p->num_seqs == 0 || p->max_seqlen_q == 0 || p->total_q == 0) {
+        *nothing = true;
+        return PA_OK;
+    }
     const int64_t ncols = ((int64_t)p->max_seqlen_k + p->page_size - 1) / p->page_size;
     if (p->page_table_stride < ncols) return fail(PA_ERR_INVALID, "page_table_stride too small for max_seqlen_k");
     if (p->lse != nullptr && p->lse_stride < p->total_q) return fail(PA_ERR_INVALID, "lse_stride < total_q");
@@ -281,6 +286,14 @@ pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
                         p->max_seqlen_q, p->max_seqlen_k);
     }
     if ((reinterpret_cast<uintptr_t>(p->scheduler) & 7u) != 0) return fail(PA_ERR_INVALID, "scheduler must be 8-byte aligned");
+    return PA_OK;
+}
+
+pa_status pa_prefill(const pa_prefill_params *p, void *stream) {
+    g_last_error[0] = 0;
+    bool nothing = false;
+    pa_status st = check_prefill(p, &nothing);
+    if (st != PA_OK || nothing) return st;
     cudaError_t e = launch_prefill(*p, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "prefill configuration not supported by this library");
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "prefill launch");
@@ -330,11 +343,8 @@ int32_t pa_decode_kv_chunk(const pa_decode_params *p) {
     return plan_decode(*p).kv_chunk;
 }
 
-pa_status pa_decode(const pa_decode_params *p, void *stream) {
-    g_last_error[0] = 0;
-    pa_status st = check_decode(p);
-    if (st != PA_OK) return st;
-    if (p->num_seqs == 0) return PA_OK;
+// The checks pa_decode makes after check_decode for a non-empty batch.
+static pa_status check_decode_buffers(const pa_decode_params *p) {
     const int64_t ncols = ((int64_t)p->max_seqlen_k + p->page_size - 1) / p->page_size;
     if (p->page_table_stride < ncols) return fail(PA_ERR_INVALID, "page_table_stride too small for max_seqlen_k");
     if (!p->q || !p->k_cache || !p->v_cache || !p->page_table || !p->cache_seqlens || !p->out)
@@ -347,8 +357,49 @@ pa_status pa_decode(const pa_decode_params *p, void *stream) {
             return fail(PA_ERR_INVALID, "workspace of %zu bytes needed, %zu given", plan.workspace_bytes, p->workspace_bytes);
         if (!aligned16(p->workspace)) return fail(PA_ERR_INVALID, "workspace must be 16-byte aligned");
     }
+    return PA_OK;
+}
+
+pa_status pa_decode(const pa_decode_params *p, void *stream) {
+    g_last_error[0] = 0;
+    pa_status st = check_decode(p);
+    if (st != PA_OK) return st;
+    if (p->num_seqs == 0) return PA_OK;
+    st = check_decode_buffers(p);
+    if (st != PA_OK) return st;
+    const DecodePlan plan = plan_decode(*p);
     cudaError_t e = launch_decode(*p, plan, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "decode launch");
+}
+
+pa_status pa_mixed_batch(const pa_prefill_params *pre, const pa_decode_params *dec, void *stream) {
+    g_last_error[0] = 0;
+    bool no_prefill = false;
+    pa_status st = check_prefill(pre, &no_prefill);
+    if (st != PA_OK) return st;
+    st = check_decode(dec);
+    if (st != PA_OK) return st;
+    const bool no_decode = dec->num_seqs == 0;
+    // a batch of one kind only is that kind's own launch
+    if (no_prefill && no_decode) return PA_OK;
+    if (no_prefill) return pa_decode(dec, stream);
+    if (no_decode) return pa_prefill(pre, stream);
+    st = check_decode_buffers(dec);
+    if (st != PA_OK) return st;
+    if (pre->k_cache != dec->k_cache || pre->v_cache != dec->v_cache || pre->num_pages != dec->num_pages ||
+        pre->page_size != dec->page_size || pre->num_q_heads != dec->num_q_heads ||
+        pre->num_kv_heads != dec->num_kv_heads || pre->head_dim != dec->head_dim)
+        return fail(PA_ERR_INVALID, "prefill and decode halves must share the pools and the head geometry");
+    if (pre->kv_dtype != PA_KV_BF16 || dec->kv_dtype != PA_KV_BF16)
+        return fail(PA_ERR_UNSUPPORTED, "the mixed-batch launch takes bf16 pools; call pa_prefill and pa_decode");
+    if (pre->sliding_window != 0 || pre->block_mask != nullptr)
+        return fail(PA_ERR_UNSUPPORTED, "the mixed-batch launch's prefill half takes no window or block mask");
+    if ((pre->num_q_heads / pre->num_kv_heads) % 2 != 0 || pre->num_kv_heads % 4 != 0)
+        return fail(PA_ERR_UNSUPPORTED, "the mixed-batch launch needs an even GQA group and num_kv_heads %% 4 == 0");
+    if (dec->overlap_previous != 0) return fail(PA_ERR_INVALID, "overlap_previous must be 0 in a mixed-batch launch");
+    cudaError_t e = launch_mixed(*pre, *dec, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "mixed-batch configuration not supported (too many decode sequences for one CTA's shared memory?)");
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "mixed-batch launch");
 }
 
 pa_status pa_decode_noalloc(const pa_decode_params *p, void *stream) {

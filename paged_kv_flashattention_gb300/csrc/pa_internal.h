@@ -46,6 +46,7 @@ cudaError_t launch_lse_combine(const float *o_partial, const float *lse_partial,
                                cudaStream_t stream);
 
 cudaError_t launch_prefill(const pa_prefill_params &p, cudaStream_t stream);
+cudaError_t launch_mixed(const pa_prefill_params &pre, const pa_decode_params &dec, cudaStream_t stream);
 
 int num_sms();
 
@@ -60,5 +61,6 @@ cudaError_t decode_noalloc_scratch(void **ptr);
 cudaError_t error_word_store(int **addr);
 cudaError_t error_word_decode(int **addr);
 cudaError_t error_word_prefill(int **addr);
+cudaError_t error_word_mixed(int **addr);
 
 }  // namespace pa

@@ -82,6 +82,22 @@ NOALLOC_CASES = [
                                workspace_bytes=0), UNSUPPORTED),
 ]
 
+# pa_mixed_batch: a prefill half and a decode half that cannot share one launch
+MIXED_PREFILL = dict(PREFILL_BASE, num_q_heads=32, num_kv_heads=8, max_seqlen_k=4096, page_table_stride=256,
+                     num_pages=1000)
+MIXED_DECODE = dict(DECODE_BASE, num_q_heads=32, num_kv_heads=8, page_table_stride=256, workspace_bytes=1 << 30)
+MIXED_CASES = [
+    ("other_pools", dict(k_cache=0x9100), {}, INVALID),
+    ("other_head_dim", {}, dict(head_dim=64), INVALID),
+    ("fp8_pools", dict(kv_dtype=1, k_scale=0xA000, v_scale=0xA100), dict(kv_dtype=1, k_scale=0xA000, v_scale=0xA100),
+     UNSUPPORTED),
+    ("prefill_window", dict(sliding_window=64), {}, UNSUPPORTED),
+    ("odd_group", dict(num_q_heads=8, num_kv_heads=8), dict(num_q_heads=8, num_kv_heads=8), UNSUPPORTED),
+    ("kv_heads_not_4", dict(num_q_heads=12, num_kv_heads=6), dict(num_q_heads=12, num_kv_heads=6), UNSUPPORTED),
+    ("overlap_previous", {}, dict(overlap_previous=1), INVALID),
+    ("no_scheduler", dict(scheduler=0), {}, INVALID),
+]
+
 ROPE_CASES = [
     ("rot72", dict(rot_dim=72), UNSUPPORTED),
     ("rot256", dict(rot_dim=256), UNSUPPORTED),
@@ -110,6 +126,7 @@ STORE_CASES = [
 def all_case_ids():
     ids = [f"prefill/{c[0]}" for c in PREFILL_CASES] + [f"decode/{c[0]}" for c in DECODE_CASES]
     ids += [f"noalloc/{c[0]}" for c in NOALLOC_CASES] + [f"rope/{c[0]}" for c in ROPE_CASES]
+    ids += [f"mixed/{c[0]}" for c in MIXED_CASES]
     return ids + [f"store/{c[0]}" for c in STORE_CASES]
 
 
@@ -119,6 +136,7 @@ def expected():
     out.update({f"noalloc/{i}": s for i, _, s in NOALLOC_CASES})
     out.update({f"rope/{i}": s for i, _, s in ROPE_CASES})
     out.update({f"store/{i}": s for i, _, _, s in STORE_CASES})
+    out.update({f"mixed/{i}": s for i, _, _, s in MIXED_CASES})
     return out
 
 
@@ -144,6 +162,10 @@ def run_all() -> dict:
         rec(f"rope/{i}", lib.pa_rope_store_kv(ctypes.byref(p), None))
     for i, fn, args, _ in STORE_CASES:
         rec(f"store/{i}", getattr(lib, fn)(*args))
+    for i, kp, kd, _ in MIXED_CASES:
+        p = _lib.PrefillParams(**{**MIXED_PREFILL, **kp})
+        d = _lib.DecodeParams(**{**MIXED_DECODE, **kd})
+        rec(f"mixed/{i}", lib.pa_mixed_batch(ctypes.byref(p), ctypes.byref(d), None))
     return res
 
 

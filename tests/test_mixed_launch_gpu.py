@@ -1,0 +1,111 @@
+"""One continuous batch in one launch (pa_mixed_batch): prefill / extend
+requests and decode sequences over the same paged pool.  Both halves must
+agree with the fp64 oracle within the contract; the prefill half is
+bit-identical to pa_prefill (the same work items, computed the same way) and
+the decode half agrees with pa_decode within the tolerance (its key ranges
+may be cut elsewhere).  Repeated launches reuse one scheduler array."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from pa_harness import bf16_dev, compare, oracle_ref
+
+pytestmark = pytest.mark.gpu
+
+
+class Mixed:
+    """A batch whose first n_pre requests are prefill / extend requests and the
+    rest decode sequences (one new token each), sharing one pool and one
+    token table; every new token is stored before attention."""
+
+    def __init__(self, seed, pre_cached, pre_ext, dec_len, *, hq=32, hkv=8, d=128, page=16):
+        import paged_kv_flashattention_gb300 as pa
+        from paged_kv_flashattention_gb300 import metadata
+        self.n_pre = len(pre_cached)
+        cached = list(pre_cached) + [int(L) - 1 for L in dec_len]
+        ext = list(pre_ext) + [1] * len(dec_len)
+        self.p = p = W.small_problem(seed, cached, ext, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                                     page_size=page)
+        dev = torch.device("cuda:0")
+        self.dev = dev
+        self.k_cache, self.v_cache = bf16_dev(p.k_cache, dev), bf16_dev(p.v_cache, dev)
+        pa.store_kv(bf16_dev(p.k_new, dev), bf16_dev(p.v_new, dev), torch.from_numpy(p.slot_mapping).to(dev),
+                    self.k_cache, self.v_cache)
+        q = bf16_dev(p.q, dev)
+        self.tp = int(p.extend_len[:self.n_pre].sum())
+        self.q_pre, self.q_dec = q[:self.tp], q[self.tp:]
+        tt = torch.from_numpy(p.token_table).to(dev)
+        idx = torch.from_numpy(p.table_idx).to(dev)
+        self.mp = metadata.prepare(p.cached_len[:self.n_pre], p.extend_len[:self.n_pre], tt, idx[:self.n_pre], page)
+        self.md = metadata.prepare(p.cached_len[self.n_pre:], p.extend_len[self.n_pre:], tt, idx[self.n_pre:], page)
+        torch.cuda.synchronize()
+
+    def mixed(self, scheduler=None, prefill_ctas=0):
+        import paged_kv_flashattention_gb300 as pa
+        mp, md = self.mp, self.md
+        lse_p = torch.empty((self.p.num_q_heads, self.tp), dtype=torch.float32, device=self.dev)
+        lse_d = torch.empty((self.q_dec.shape[0], self.p.num_q_heads), dtype=torch.float32, device=self.dev)
+        op, od = pa.mixed_batch(self.q_pre, self.q_dec, self.k_cache, self.v_cache, mp.page_table, mp.cu_seqlens_q,
+                                mp.cu_seqlens_k, mp.max_seqlen_q, mp.max_seqlen_k, md.page_table,
+                                md.cache_seqlens, md.max_seqlen_k, scale=self.p.scale, lse_prefill=lse_p,
+                                lse_decode=lse_d, scheduler=scheduler, prefill_ctas=prefill_ctas)
+        torch.cuda.synchronize()
+        return op, od, lse_p, lse_d
+
+    def separate(self):
+        import paged_kv_flashattention_gb300 as pa
+        mp, md = self.mp, self.md
+        op = pa.prefill(self.q_pre, self.k_cache, self.v_cache, mp.page_table, mp.cu_seqlens_q, mp.cu_seqlens_k,
+                        mp.max_seqlen_q, mp.max_seqlen_k, causal=True, scale=self.p.scale)
+        od = pa.decode(self.q_dec, self.k_cache, self.v_cache, md.page_table, md.cache_seqlens, md.max_seqlen_k,
+                       scale=self.p.scale)
+        torch.cuda.synchronize()
+        return op, od
+
+    def check(self, what, prefill_ctas=0):
+        import paged_kv_flashattention_gb300 as pa
+        op, od, lp, ld = self.mixed(prefill_ctas=prefill_ctas)
+        ref, ref_lse = oracle_ref(self.p)                  # every row of the whole batch
+        compare(op, ref[:self.tp], f"{what}: prefill half", lse_gpu=lp.T.contiguous(), lse_ref=ref_lse[:self.tp])
+        compare(od, ref[self.tp:], f"{what}: decode half", lse_gpu=ld, lse_ref=ref_lse[self.tp:])
+        sp, sd = self.separate()
+        assert torch.equal(op.view(torch.int16), sp.view(torch.int16)), f"{what}: prefill half != pa_prefill"
+        assert (od.float() - sd.float()).abs().max().item() <= 2e-2, f"{what}: decode half vs pa_decode"
+        assert pa.device_error() == 0
+
+
+@pytest.mark.parametrize("page", [16, 1])
+@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (64, 16, 4), (128, 8, 4), (64, 32, 4)])
+def test_mixed_batch_launch(cuda_device, page, d, hq, hkv):
+    rng = np.random.default_rng(600 + page + d + hq)
+    dec_len = rng.integers(1, 2000, size=24)
+    m = Mixed(610 + page + d + hq, [0, 300, 1000], [700, 130, 5], dec_len, hq=hq, hkv=hkv, d=d, page=page)
+    m.check(f"mixed P{page} d{d} g{hq // hkv}")
+    m.check(f"mixed P{page} d{d} g{hq // hkv}, prefill on 5 CTAs", prefill_ctas=5)
+
+
+def test_mixed_batch_repeated_and_edges(cuda_device):
+    """Repeated launches on one scheduler array (reset by every launch; the
+    prefill share chosen by the kernel, one CTA or three) give the same
+    results; decode sequences of one key and long ones."""
+    dec_len = np.array([1, 1, 40, 5000, 17, 3000], np.int64)
+    m = Mixed(650, [0, 64], [129, 64], dec_len, hq=32, hkv=8, d=128, page=16)
+    sched = torch.zeros(4, dtype=torch.int32, device=cuda_device)
+    bits = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+    firsts = {n: m.mixed(sched, prefill_ctas=n) for n in (0, 1, 3)}
+    for n in (0, 1, 3, 0, 1, 3):
+        again = m.mixed(sched, prefill_ctas=n)
+        # with one prefill share the work items and the decode key ranges are
+        # fixed by the batch, whatever CTA takes them: the same bits
+        for a, b in zip(firsts[n], again):
+            assert torch.equal(bits(a), bits(b))
+        # another share may cut the decode rows into other partials: the
+        # prefill half is the same, the decode half equal up to rounding
+        op, od, lp, ld = firsts[0]
+        assert torch.equal(bits(op), bits(again[0])) and torch.equal(bits(lp), bits(again[2]))
+        assert (od.float() - again[1].float()).abs().max().item() <= 2e-2
+        assert (ld - again[3]).abs().max().item() <= 2e-3
+        assert sched.tolist() == [0, 0, 0, 0]
+    m.check("edges")
+    m.check("edges, prefill on one CTA", prefill_ctas=1)
