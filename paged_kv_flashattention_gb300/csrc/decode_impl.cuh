@@ -23,8 +23,11 @@ constexpr int kStageTok = 16;     // tokens per pipeline stage
 // Ring depth.  FP8 keeps 3 stages of half-length rows: the smaller ring lets
 // 4 CTAs share an SM instead of 2, which measured faster than 6 stages at 2
 // CTAs (each CTA's consumers work through one stage at a time).
-template <int EB>
-constexpr int stages_for() { return EB == 1 ? 3 : 3; }
+// Three stages at every row length: at d = 64 (bf16 rows half as long), six
+// stages halve the CTAs per SM and measured 1.5x slower on a Llama-3.2-1B
+// shaped decode, and 1 KiB rows (8 KV heads per CTA) measured the same as 4.
+template <int D, int EB>
+constexpr int stages_for() { return 3; }
 constexpr int kFp8MaxHeadsPerCta = 4;
 constexpr float kLazyRescale = 8.0f;  // log2 units
 
@@ -59,12 +62,12 @@ struct DecodeArgs {
     int32_t evict_first;          // K/V row copies with an L2 evict-first policy (beside a prefill)
 };
 
-template <int D, int HPC, int EB>
+template <int D, int HPC, int EB, int STAGES = stages_for<D, EB>()>
 struct DecodeSmem {
     static constexpr int kRowBytes = HPC * D * EB;           // one token, CTA's KV heads (EB bytes each)
     static constexpr int kRowStride = kRowBytes + 16;        // +16 B: ldmatrix rows hit distinct banks
     static constexpr int kStageBytes = 2 * kStageTok * kRowStride;
-    static constexpr int kStages = stages_for<EB>();
+    static constexpr int kStages = STAGES;
     static constexpr int kRingBytes = kStages * kStageBytes;
 };
 
@@ -182,11 +185,11 @@ __device__ __forceinline__ void decode_prefix(const DecodeArgs &a, int32_t *pref
 // 16-token stages into the ring (per token one bulk copy of the K row and
 // one of the V row), continuing the stage count of earlier ranges.  False
 // on a timeout.
-template <int D, int HPC, int EB>
+template <int D, int HPC, int EB, int STAGES = stages_for<D, EB>()>
 __device__ bool decode_produce(const DecodeArgs &a, const int32_t *prefix, int64_t T, int64_t g0,
                                int64_t g1, uint8_t *ring, uint64_t *full, uint64_t *empty, int &stage_ctr,
                                int lane) {
-    using S = DecodeSmem<D, HPC, EB>;
+    using S = DecodeSmem<D, HPC, EB, STAGES>;
     constexpr int kStages = S::kStages;
     const int B = a.num_seqs, HG = a.head_groups;
     // every K/V row is read once: beside a prefill, evict-first keeps the
@@ -233,12 +236,12 @@ __device__ bool decode_produce(const DecodeArgs &a, const int32_t *prefix, int64
 
 // Consumer warp cw (KV head hg * HPC + cw of each segment) of the same range.
 // False on a timeout.
-template <int D, int G, int HPC, bool F8>
+template <int D, int G, int HPC, bool F8, int STAGES = stages_for<D, F8 ? 1 : 2>()>
 __device__ bool decode_consume(const DecodeArgs &a, const int32_t *prefix, int64_t T, int64_t g0,
                                int64_t g1, uint8_t *ring, uint64_t *full, uint64_t *empty, uint16_t *pbuf,
                                int &stage_ctr, int cw, int lane) {
     constexpr int EB = F8 ? 1 : 2;
-    using S = DecodeSmem<D, HPC, EB>;
+    using S = DecodeSmem<D, HPC, EB, STAGES>;
     constexpr int kStages = S::kStages;
     const int B = a.num_seqs, HG = a.head_groups;
     // ---------------------------------------------------- consumer warps ----

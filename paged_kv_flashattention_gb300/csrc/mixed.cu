@@ -105,7 +105,7 @@ __device__ int auto_prefill_ctas(const PrefillArgs &a, const DecodeArgs &da, flo
 // reused).
 template <int D>
 struct MixedSmem {
-    using DS = DecodeSmem<D, kMixedHpc, 2>;
+    using DS = DecodeSmem<D, kMixedHpc, 2, 3>;
     static constexpr int kStages = DS::kStages;
     static constexpr int kRing = (DS::kRingBytes + 1023) / 1024 * 1024;
     static constexpr int kBars = 2 * kRing;                           // per stream: full, empty, chunk ring
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (c0 < 0) break;
             const int64_t g0 = (int64_t)c0 * T, g1 = min((int64_t)c1 * T, total);
-            if (!decode_produce<D, HPC, 2>(da, prefix, T, g0, g1, ring, full, empty, stage_ctr, lane)) break;
+            if (!decode_produce<D, HPC, 2, kStages>(da, prefix, T, g0, g1, ring, full, empty, stage_ctr, lane)) break;
         }
         // the last stream to finish resets the counters for the next launch
         if (lane == 0) {
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0) mbar_arrive(&cempty[slot]);
             if (c0 < 0) break;
             const int64_t g0 = (int64_t)c0 * T, g1 = min((int64_t)c1 * T, total);
-            if (!decode_consume<D, G, HPC, false>(da, prefix, T, g0, g1, ring, full, empty, pbuf, stage_ctr, cw,
+            if (!decode_consume<D, G, HPC, false, kStages>(da, prefix, T, g0, g1, ring, full, empty, pbuf, stage_ctr, cw,
                                                  lane))
                 break;
         }
@@ -279,8 +279,9 @@ cudaError_t launch_mixed(const pa_prefill_params &pp, const pa_decode_params &dp
     if (e != cudaSuccess) return e;
     if (T != 2) return cudaErrorNotSupported;
     a.sched = pp.scheduler;
-    const DecodePlan plan = plan_decode(dp);
-    if (plan.heads_per_cta != kMixedHpc) return cudaErrorNotSupported;
+    DecodePlan plan = plan_decode(dp);
+    if (dp.num_kv_heads % kMixedHpc != 0) return cudaErrorNotSupported;
+    plan.heads_per_cta = kMixedHpc;       // the split layout's head groups of this launch
     DecodeArgs da = decode_setup(dp, plan);
     da.evict_first = 1;
     const int sms = num_sms();
