@@ -262,9 +262,11 @@ DecodePlan plan_decode(const pa_decode_params &p) {
     // KV heads per CTA: the largest power of two <= 4 dividing Hkv (token
     // rows of 512 B at d = 64, 1 KiB at d = 128; a 3-stage ring of 48 or
     // 96 KiB, so two or more CTAs fit on an SM).
-    // FP8 rows are half as long: up to 8 heads, so a copy still moves >= 1 KiB
-    // at d = 128.
-    const int max_hpc = p.kv_dtype == PA_KV_FP8_E4M3 ? kFp8MaxHeadsPerCta : 4;
+    // FP8 rows are half as long: 8 heads at d = 64 and 4 at d = 128, 512 B
+    // either way (fp8_max_heads_per_cta).
+    const int max_hpc = p.kv_dtype != PA_KV_FP8_E4M3 ? 4
+                      : p.head_dim == 64               ? fp8_max_heads_per_cta<64>()
+                                                       : fp8_max_heads_per_cta<128>();
     int hpc = 1;
     while (hpc * 2 <= max_hpc && p.num_kv_heads % (hpc * 2) == 0) hpc *= 2;
     plan.heads_per_cta = hpc;

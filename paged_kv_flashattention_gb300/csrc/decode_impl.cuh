@@ -26,9 +26,14 @@ constexpr int kStageTok = 16;     // tokens per pipeline stage
 // Three stages at every row length: at d = 64 (bf16 rows half as long), six
 // stages halve the CTAs per SM and measured 1.5x slower on a Llama-3.2-1B
 // shaped decode, and 1 KiB rows (8 KV heads per CTA) measured the same as 4.
-template <int D, int EB>
+// (FP8 with 8 KV heads per CTA: 2 or 4 stages measured slower than 3 too.)
+template <int D, int EB, int HPC>
 constexpr int stages_for() { return 3; }
-constexpr int kFp8MaxHeadsPerCta = 4;
+// FP8 KV heads per CTA at most: 512-byte token rows at either head size (8
+// heads at d = 64: Llama-3.2-1B shaped decode 45 us against 51 us with 4;
+// 4 heads at d = 128: 8 measured 201 us against 194 us on a log-uniform mix).
+template <int D>
+constexpr int fp8_max_heads_per_cta() { return D == 64 ? 8 : 4; }
 constexpr float kLazyRescale = 8.0f;  // log2 units
 
 struct DecodeArgs {
@@ -62,7 +67,7 @@ struct DecodeArgs {
     int32_t evict_first;          // K/V row copies with an L2 evict-first policy (beside a prefill)
 };
 
-template <int D, int HPC, int EB, int STAGES = stages_for<D, EB>()>
+template <int D, int HPC, int EB, int STAGES = stages_for<D, EB, HPC>()>
 struct DecodeSmem {
     static constexpr int kRowBytes = HPC * D * EB;           // one token, CTA's KV heads (EB bytes each)
     static constexpr int kRowStride = kRowBytes + 16;        // +16 B: ldmatrix rows hit distinct banks
@@ -185,7 +190,7 @@ __device__ __forceinline__ void decode_prefix(const DecodeArgs &a, int32_t *pref
 // 16-token stages into the ring (per token one bulk copy of the K row and
 // one of the V row), continuing the stage count of earlier ranges.  False
 // on a timeout.
-template <int D, int HPC, int EB, int STAGES = stages_for<D, EB>()>
+template <int D, int HPC, int EB, int STAGES = stages_for<D, EB, HPC>()>
 __device__ bool decode_produce(const DecodeArgs &a, const int32_t *prefix, int64_t T, int64_t g0,
                                int64_t g1, uint8_t *ring, uint64_t *full, uint64_t *empty, int &stage_ctr,
                                int lane) {
@@ -236,7 +241,7 @@ __device__ bool decode_produce(const DecodeArgs &a, const int32_t *prefix, int64
 
 // Consumer warp cw (KV head hg * HPC + cw of each segment) of the same range.
 // False on a timeout.
-template <int D, int G, int HPC, bool F8, int STAGES = stages_for<D, F8 ? 1 : 2>()>
+template <int D, int G, int HPC, bool F8, int STAGES = stages_for<D, F8 ? 1 : 2, HPC>()>
 __device__ bool decode_consume(const DecodeArgs &a, const int32_t *prefix, int64_t T, int64_t g0,
                                int64_t g1, uint8_t *ring, uint64_t *full, uint64_t *empty, uint16_t *pbuf,
                                int &stage_ctr, int cw, int lane) {
