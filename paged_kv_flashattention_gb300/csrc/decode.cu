@@ -129,38 +129,60 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(
     n = max(0, min(n, max_splits));
     const float *lrow = lse_part + (int64_t)row * max_splits;
     const float *obase = o_part + (int64_t)row * max_splits * D + lane * VPL;
+    // The slots are read 128 at a time (four independent loads per lane):
+    // first the maximum, then, per group of 128, the weights and a warp ballot
+    // of the slots that carry any.  Only their partials are loaded (an empty
+    // slot, lse -inf, may have no partial written), 16 independent loads at a
+    // time across the group's four 32-slot blocks.
     float M = -INFINITY;
-    for (int s = lane; s < n; s += 32) M = fmaxf(M, lrow[s]);
+    for (int s0 = 0; s0 < n; s0 += 128) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int s = s0 + 32 * b + lane;
+            if (s < n) M = fmaxf(M, lrow[s]);
+        }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float acc[VPL];
 #pragma unroll
     for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
-    float den = 0.f;                       // this lane's splits; summed over the warp below
+    float den = 0.f;                       // this lane's slots; summed over the warp below
     if (M != -INFINITY) {
-        // 32 splits at a time, one per lane: the weights, and a ballot of the
-        // splits that carry any (an empty split, lse -inf, may have no
-        // partial written and is not read); their partials are then loaded
-        // up to U at a time, the loads independent of one another
         constexpr int U = 16;
-        for (int s0 = 0; s0 < n; s0 += 32) {
-            const float l = s0 + lane < n ? lrow[s0 + lane] : -INFINITY;
-            const float w = l == -INFINITY ? 0.f : __expf(l - M);
-            den += w;
-            uint32_t live = __ballot_sync(0xffffffffu, w > 0.f);
-            while (live != 0u) {
+        for (int s0 = 0; s0 < n; s0 += 128) {
+            float w[4];
+            uint32_t live[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int s = s0 + 32 * b + lane;
+                const float l = s < n ? lrow[s] : -INFINITY;
+                w[b] = l == -INFINITY ? 0.f : __expf(l - M);
+                den += w[b];
+                live[b] = __ballot_sync(0xffffffffu, w[b] > 0.f);
+            }
+            while ((live[0] | live[1] | live[2] | live[3]) != 0u) {
                 int j[U];
+                float wu[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    j[u] = live != 0u ? __ffs(live) - 1 : -1;     // the same on every lane
-                    live &= live - 1u;
-                }
-                float v[U][VPL], wu[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    wu[u] = __shfl_sync(0xffffffffu, w, j[u] < 0 ? 0 : j[u]);
-                    if (j[u] < 0) {
+                    // the next live slot of the group (the same on every lane)
+                    const int b = live[0] ? 0 : live[1] ? 1 : live[2] ? 2 : live[3] ? 3 : -1;
+                    if (b < 0) {
+                        j[u] = -1;
                         wu[u] = 0.f;
+                        continue;
+                    }
+                    const int bit = __ffs(live[b]) - 1;
+                    live[b] &= live[b] - 1u;
+                    j[u] = 32 * b + bit;
+                    const float wb = b == 0 ? w[0] : b == 1 ? w[1] : b == 2 ? w[2] : w[3];
+                    wu[u] = __shfl_sync(0xffffffffu, wb, bit);
+                }
+                float v[U][VPL];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (j[u] < 0) {
 #pragma unroll
                         for (int e = 0; e < VPL; ++e) v[u][e] = 0.f;
                         continue;

@@ -12,8 +12,8 @@
 // consumer warps running the split-KV decode of decode_impl.cuh: the streams
 // take key ranges of the decode batch (equal numbers of (sequence, head
 // group, key) rows): each stream of the CTAs without prefill work first walks
-// one large static run, and the rest is handed out in shrinking runs from a
-// second device counter.  The CTAs without prefill work start on decode at
+// most of its own slice of the rows, and the slices' tails are handed out one
+// short range at a time from a second device counter.  The CTAs without prefill work start on decode at
 // once and the prefill CTAs join as they finish, so the tensor-bound prefill
 // runs under the HBM-bound decode read and the decode work still spreads
 // over every SM at the end.
@@ -170,17 +170,23 @@ __global__ void __launch_bounds__(384, 1)
     T = (T + 15) / 16 * 16;
     if (T < da.min_split) T = da.min_split;
     const int stream = (warp >= 4 && warp < 8) || warp == 10 ? 1 : 0;
-    // T-ranges [0, N) of the decode rows.  Every stream of the CTAs without
-    // prefill items (of all CTAs when all have some) first walks one run of
-    // K consecutive ranges: together 7/8 of the work, split equally as the
-    // decode kernel splits it.  The other ranges go, from a counter, to
-    // whichever stream is free (the prefill CTAs' streams included once their
-    // items are done) in runs that shrink with the work left.
+    // T-ranges [0, N) of the decode rows, cut into one slice of Q ranges per
+    // stream of the CTAs without prefill items (of all CTAs when all have
+    // some).  Each such stream first walks the first K = 7/8 of its slice:
+    // together 7/8 of the work, split equally as the decode kernel splits it.
+    // The slices' last R ranges (and the ranges past the last slice) are the
+    // pool, taken slice by slice from a counter by whichever stream is free
+    // (the prefill CTAs' streams included once their items are done) in runs
+    // that shrink with the work left, down to single ranges at the end.  A
+    // run that crosses into the next slice's tail is walked as two ranges.  A
+    // row thus gets partials only where it crosses a slice's tail.
     const int N = (int)((total + T - 1) / T);
     const int first_static = prefill_ctas < (int)gridDim.x ? prefill_ctas : 0;
     const int n_static = 2 * ((int)gridDim.x - first_static);
-    const int K = (int)((int64_t)N * kStaticSixteenths / 16 / n_static);
-    const int dyn0 = K * n_static;
+    const int Q = N / n_static;
+    const int K = Q * kStaticSixteenths / 16;
+    const int R = Q - K;
+    const int pool = n_static * R + (N - n_static * Q);
     const int my_run = (int)blockIdx.x >= first_static ? 2 * ((int)blockIdx.x - first_static) + stream : -1;
 
     uint8_t *ring = smem + stream * M::kRing;
@@ -195,24 +201,37 @@ __global__ void __launch_bounds__(384, 1)
             for (int b = lane; b <= B; b += 32) da.ws_prefix[b] = prefix[b];
             if (lane == 0) da.ws_header[0] = (int32_t)T;
         }
+        // pool index d -> T-range: the tails slice by slice, then the rest
+        auto pool_range = [&](int d) { return d < n_static * R ? (d / R) * Q + K + d % R : n_static * Q + (d - n_static * R); };
         int stage_ctr = 0;
-        int seen = dyn0;                                          // the counter as of the last grab
+        int seen = 0;                                             // the counter as of the last grab
+        int rest0 = -1, rest1 = -1;                               // the second part of a run
         for (int n = 0;; ++n) {
             int c0 = -1, c1 = -1;                                 // T-ranges [c0, c1)
             if (n == 0 && my_run >= 0 && K > 0) {
-                c0 = my_run * K;
+                c0 = my_run * Q;
                 c1 = c0 + K;
+            } else if (rest0 >= 0) {
+                c0 = rest0;
+                c1 = rest1;
+                rest0 = -1;
             } else {
-                // guided: a share of what was left at the last grab, shrinking
-                // to single ranges at the end
-                const int k = max(1, (N - seen) / (4 * (int)gridDim.x));
-                int c = 0;
-                if (lane == 0) c = dyn0 + atomicAdd(&m.dsched[0], k);
-                c = __shfl_sync(0xffffffffu, c, 0);
-                seen = c + k;
-                if (c < N) {
-                    c0 = c;
-                    c1 = min(c + k, N);
+                const int k = max(1, min(R > 0 ? R : 1, (pool - seen) / (4 * (int)gridDim.x)));
+                int d = 0;
+                if (lane == 0) d = atomicAdd(&m.dsched[0], k);
+                d = __shfl_sync(0xffffffffu, d, 0);
+                seen = d + k;
+                if (d < pool) {
+                    const int e = min(d + k, pool);               // pool indices [d, e)
+                    c0 = pool_range(d);
+                    // contiguous up to the end of d's tail (or of the pool)
+                    int split = e;
+                    if (d < n_static * R) split = min(e, (d / R + 1) * R);
+                    c1 = pool_range(split - 1) + 1;
+                    if (split < e) {
+                        rest0 = pool_range(split);
+                        rest1 = pool_range(e - 1) + 1;
+                    }
                 }
             }
             const int slot = n & 1;
