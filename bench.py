@@ -173,16 +173,15 @@ class MixedBatch:
         tt[:d.num_seqs, :d.token_table.shape[1]] = d.token_table
         tt[d.num_seqs:, :p.token_table.shape[1]] = p.token_table
         self.token_table = torch.from_numpy(tt).to(dev)
-        self.idx_dec = torch.arange(d.num_seqs, dtype=torch.int32, device=dev)
-        self.idx_pre = torch.arange(d.num_seqs, d.num_seqs + p.num_seqs, dtype=torch.int32, device=dev)
+        # rows of the token table: the decode requests, then the prefill chunks
+        self.idx_all = torch.arange(d.num_seqs + p.num_seqs, dtype=torch.int32, device=dev)
         self.max_dec = int(d.device_len.max())
         self.out_dec = torch.empty_like(self.q_dec)
         self.out_pre = torch.empty_like(self.q_pre)
         ws = pa.decode_workspace_size(self.q_dec.shape, self.k_cache, self.max_dec, kv_chunk=256)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
-        self.pt_dec = torch.empty((d.num_seqs, -(-self.max_dec // self.P)), dtype=torch.int32, device=dev)
-        self.pt_pre = torch.empty((p.num_seqs, -(-int(p.device_len.max()) // self.P)), dtype=torch.int32,
-                                  device=dev)
+        width = -(-max(self.max_dec, int(p.device_len.max())) // self.P)
+        self.pt_all = torch.empty((d.num_seqs + p.num_seqs, width), dtype=torch.int32, device=dev)
         # algorithmic work of one step
         ctx = d.device_len.astype(np.int64)
         self.decode_bytes = int(ctx.sum()) * self.Hkv * self.D * 2 * 2 + 2 * self.q_dec.numel() * 2
@@ -191,7 +190,7 @@ class MixedBatch:
         self.prefill_bytes = 2 * self.q_pre.numel() * 2 + 2 * p.num_new_tokens * self.Hkv * self.D * 2
         self.store_bytes = 2 * 2 * Tn * self.Hkv * self.D * 2
         self.step_bytes = self.decode_bytes + self.prefill_bytes + self.store_bytes
-        self.launches_per_step = 6   # store, 2 page tables, prefill, decode split + combine
+        self.launches_per_step = 5   # store, page table, prefill, decode split + combine
         self.num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
         self.prefill_sms = 12        # overlapped schedule (0: phases in sequence)
         # "overlap": prefill on prefill_sms SMs, decode as its programmatic
@@ -201,9 +200,9 @@ class MixedBatch:
         self.mixed_sched = torch.zeros(4, dtype=torch.int32, device=dev)
         self.fused_prefill_ctas = 12   # fused schedule: CTAs that take prefill tiles first (0 = automatic)
         self.fused_kv_chunk = 256      # fused schedule: the decode split layout's unit
-        from paged_kv_flashattention_gb300.metadata import MetadataBuilder
-        self.meta_dec = MetadataBuilder(dev, d.num_seqs)
-        self.meta_pre = MetadataBuilder(dev, p.num_seqs)
+        from paged_kv_flashattention_gb300.metadata import MixedMetadataBuilder
+        # both halves' lengths in one copy, both page tables in one launch
+        self.meta = MixedMetadataBuilder(dev, p.num_seqs, d.num_seqs)
 
     def step(self, timing: bool = False, concurrent: bool | None = None):
         """One pass of the path.  concurrent (the default unless timing):
@@ -220,10 +219,9 @@ class MixedBatch:
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
             ev[0].record()
         pa.store_kv(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache)
-        md = self.meta_dec.prepare(self.dec.cached_len, self.dec.extend_len, self.token_table,
-                                   self.idx_dec, self.P, page_table_out=self.pt_dec)
-        mp = self.meta_pre.prepare(self.pre.cached_len, self.pre.extend_len, self.token_table,
-                                   self.idx_pre, self.P, page_table_out=self.pt_pre)
+        mp, md = self.meta.prepare(self.pre.cached_len, self.pre.extend_len, self.dec.cached_len,
+                                   self.dec.extend_len, self.token_table, self.idx_all, self.P,
+                                   page_table_out=self.pt_all)
         if timing:
             ev[1].record()
         if fused:
@@ -396,7 +394,7 @@ def run_gpu(args):
     mb.fused_prefill_ctas = args.fused_prefill_ctas
     mb.fused_kv_chunk = args.fused_kv_chunk
     if mb.schedule == "fused":
-        mb.launches_per_step = 5     # store, 2 page tables, mixed prefill+decode, combine
+        mb.launches_per_step = 4     # store, page table, mixed prefill+decode, combine
     elif mb.schedule == "sequential":
         mb.prefill_sms = 0
     torch.cuda.synchronize()
@@ -541,7 +539,7 @@ def run_gpu(args):
     for n in names_in + names_out:                         # back to the first set
         setattr(mb, n, sets[0][n])
     ms_e2e = max_over_ranks(s2.elapsed_time(e2), world, dev) / args.steps
-    h2d += 3 * 4 * (mb.dec.num_seqs + 1 + mb.pre.num_seqs + 1)   # metadata copies of both batches
+    h2d += mb._keep[0].h2d_bytes + mb._keep[1].h2d_bytes          # the metadata copy of both halves
 
     dec_ms = statistics.mean(phase["decode"])
     pre_ms = statistics.mean(phase["prefill"])
@@ -557,7 +555,8 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (decode reads "
                    f"{mb.decode_bytes / 1e9:.2f} GB per step; no flush)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "step": "store_kv + metadata (2 batches) + prefill + decode(split+combine)",
+                   "step": "store_kv + metadata of both halves (one copy, one page-table launch) + prefill "
+                           "+ decode (split + combine)",
                    "schedule": schedule_text(mb),
                    "step_bytes": mb.step_bytes},
         "roofline": roofline_block(mb, fused_ms, dec_gbs, peaks, peak_src),

@@ -109,3 +109,40 @@ def test_mixed_batch_repeated_and_edges(cuda_device):
         assert sched.tolist() == [0, 0, 0, 0]
     m.check("edges")
     m.check("edges, prefill on one CTA", prefill_ctas=1)
+
+
+def test_mixed_metadata_builder(cuda_device):
+    """MixedMetadataBuilder (one copy of both halves' lengths, one page-table
+    launch for both halves' rows, two buffer sets used in turn): the same
+    lengths and page-table rows as preparing each half on its own, and the
+    same mixed-batch result, over repeated batches."""
+    import paged_kv_flashattention_gb300 as pa
+    from paged_kv_flashattention_gb300.metadata import MixedMetadataBuilder
+    dec_len = np.array([1, 33, 700, 2500, 16, 17, 4000], np.int64)
+    m = Mixed(670, [0, 300, 64], [129, 200, 1], dec_len, hq=32, hkv=8, d=128, page=16)
+    p, n = m.p, m.n_pre
+    tt = torch.from_numpy(p.token_table).to(cuda_device)
+    idx = torch.from_numpy(np.concatenate([p.table_idx[n:], p.table_idx[:n]]).astype(np.int32)).to(cuda_device)
+    builder = MixedMetadataBuilder(cuda_device, 4, 16)
+    ref = m.mixed()
+    sched = torch.zeros(4, dtype=torch.int32, device=cuda_device)
+    for rep in range(5):
+        mp, md = builder.prepare(p.cached_len[:n], p.extend_len[:n], p.cached_len[n:], p.extend_len[n:], tt, idx,
+                                 p.page_size)
+        for got, want in ((mp, m.mp), (md, m.md)):
+            assert (got.num_seqs, got.max_seqlen_q, got.max_seqlen_k) == (want.num_seqs, want.max_seqlen_q,
+                                                                           want.max_seqlen_k)
+            for f in ("cu_seqlens_q", "cu_seqlens_k", "cache_seqlens"):
+                assert torch.equal(getattr(got, f), getattr(want, f)), f
+            cols = want.page_table.shape[1]
+            assert torch.equal(got.page_table[:, :cols], want.page_table)
+        lse_p = torch.empty((p.num_q_heads, m.tp), dtype=torch.float32, device=cuda_device)
+        lse_d = torch.empty((m.q_dec.shape[0], p.num_q_heads), dtype=torch.float32, device=cuda_device)
+        out = pa.mixed_batch(m.q_pre, m.q_dec, m.k_cache, m.v_cache, mp.page_table, mp.cu_seqlens_q,
+                             mp.cu_seqlens_k, mp.max_seqlen_q, mp.max_seqlen_k, md.page_table, md.cache_seqlens,
+                             md.max_seqlen_k, scale=p.scale, lse_prefill=lse_p, lse_decode=lse_d, scheduler=sched)
+        torch.cuda.synchronize()
+        for a, b in zip((out[0], out[1], lse_p, lse_d), ref):
+            assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                               b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+    assert pa.device_error() == 0
