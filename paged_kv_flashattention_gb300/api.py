@@ -433,14 +433,17 @@ def mixed_batch(q_prefill: torch.Tensor, q_decode: torch.Tensor, k_cache: torch.
                 scale: float | None = None, out_prefill: torch.Tensor | None = None,
                 out_decode: torch.Tensor | None = None, lse_prefill: torch.Tensor | None = None,
                 lse_decode: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                kv_chunk: int = 0, scheduler: torch.Tensor | None = None, prefill_ctas: int = 0):
+                kv_chunk: int = 0, scheduler: torch.Tensor | None = None, prefill_ctas: int = 0,
+                decode_sliding_window: int = 0):
     """One continuous batch in one launch (``pa_mixed_batch``): prefill /
     extend of ``q_prefill`` [total_q, Hq, d] (cu_seqlens_q/k, its page table)
     and decode of ``q_decode`` [B, Hq, d] (cache_seqlens, its page table)
     over the same bf16 pools.  ``prefill_ctas`` > 0: that many CTAs take
     prefill tiles before decode key ranges (the others start on decode at
     once); 0: the kernel chooses the count from the work of both halves.
-    Returns (out_prefill, out_decode)."""
+    ``decode_sliding_window`` W > 0: each decode query sees its sequence's
+    last W keys only (the prefill half takes no window).  Returns
+    (out_prefill, out_decode)."""
     dev = q_prefill.device
     p, out_prefill = _prefill_params(q_prefill, k_cache, v_cache, page_table_prefill, cu_seqlens_q, cu_seqlens_k,
                                      max_seqlen_q, max_seqlen_k_prefill, causal, scale, None, out_prefill,
@@ -455,7 +458,8 @@ def mixed_batch(q_prefill: torch.Tensor, q_decode: torch.Tensor, k_cache: torch.
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     dp = _decode_params(q_decode, k_cache, v_cache, page_table_decode, cache_seqlens, max_seqlen_k_decode, scale,
-                        None, out_decode, lse_decode, workspace, kv_chunk)
+                        None, out_decode, lse_decode, workspace, kv_chunk,
+                        sliding_window=int(decode_sliding_window))
     lib = _lib.load()
     _check(lib.pa_mixed_batch(ctypes.byref(p), ctypes.byref(dp), _stream(q_prefill)), lib)
     return out_prefill, out_decode

@@ -146,3 +146,79 @@ def test_mixed_metadata_builder(cuda_device):
             assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
                                b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
     assert pa.device_error() == 0
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+def test_mixed_batch_one_kind_only(cuda_device):
+    """With no decode sequences the call is pa_prefill, with no prefill rows it
+    is pa_decode: the same bits as those calls."""
+    import paged_kv_flashattention_gb300 as pa
+    m = Mixed(680, [0, 300], [200, 40], np.array([10, 900, 3000]), hq=32, hkv=8, d=128, page=16)
+    mp, md = m.mp, m.md
+    sp, sd = m.separate()
+    op, od = pa.mixed_batch(m.q_pre, m.q_dec[:0], m.k_cache, m.v_cache, mp.page_table, mp.cu_seqlens_q,
+                            mp.cu_seqlens_k, mp.max_seqlen_q, mp.max_seqlen_k, md.page_table[:0],
+                            md.cache_seqlens[:0], 1, scale=m.p.scale)
+    torch.cuda.synchronize()
+    assert od.shape[0] == 0 and torch.equal(_bits(op), _bits(sp))
+    zero = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    op, od = pa.mixed_batch(m.q_pre[:0], m.q_dec, m.k_cache, m.v_cache, mp.page_table[:0], zero, zero, 0, 0,
+                            md.page_table, md.cache_seqlens, md.max_seqlen_k, scale=m.p.scale)
+    torch.cuda.synchronize()
+    assert op.shape[0] == 0 and torch.equal(_bits(od), _bits(sd))
+    assert pa.device_error() == 0
+
+
+def test_mixed_batch_decode_rows_without_keys(cuda_device):
+    """Decode sequences of length 0 in a mixed launch: O = 0 and lse = -inf for
+    them; the other rows still match the oracle."""
+    import paged_kv_flashattention_gb300 as pa
+    m = Mixed(690, [0, 100], [300, 60], np.array([50, 1200, 7, 2600, 300]), hq=32, hkv=8, d=128, page=16)
+    mp, md = m.mp, m.md
+    cs = md.cache_seqlens.clone()
+    empty = [0, 3]
+    cs[empty] = 0
+    lse_d = torch.empty((m.q_dec.shape[0], m.p.num_q_heads), dtype=torch.float32, device=cuda_device)
+    op, od = pa.mixed_batch(m.q_pre, m.q_dec, m.k_cache, m.v_cache, mp.page_table, mp.cu_seqlens_q,
+                            mp.cu_seqlens_k, mp.max_seqlen_q, mp.max_seqlen_k, md.page_table, cs,
+                            md.max_seqlen_k, scale=m.p.scale, lse_decode=lse_d)
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle_ref(m.p)
+    keep = [i for i in range(m.q_dec.shape[0]) if i not in empty]
+    assert torch.all(od[empty].float() == 0) and torch.all(lse_d[empty] == -float("inf"))
+    compare(od[keep], ref[m.tp:][keep], "decode rows with keys", lse_gpu=lse_d[keep], lse_ref=ref_lse[m.tp:][keep])
+    compare(op, ref[:m.tp], "prefill half beside empty decode rows")
+    assert pa.device_error() == 0
+
+
+def test_mixed_batch_decode_sliding_window(cuda_device):
+    """A sliding window on the decode half (its queries see their sequences'
+    last W keys) against the oracle with that window."""
+    import oracle
+    import paged_kv_flashattention_gb300 as pa
+    from oracle_pins import _meta, stored_caches
+    m = Mixed(700, [0, 64], [250, 100], np.array([40, 300, 1500, 5000, 257]), hq=32, hkv=8, d=128, page=16)
+    mp, md = m.mp, m.md
+    W = 256
+    lse_d = torch.empty((m.q_dec.shape[0], m.p.num_q_heads), dtype=torch.float32, device=cuda_device)
+    op, od = pa.mixed_batch(m.q_pre, m.q_dec, m.k_cache, m.v_cache, mp.page_table, mp.cu_seqlens_q,
+                            mp.cu_seqlens_k, mp.max_seqlen_q, mp.max_seqlen_k, md.page_table, md.cache_seqlens,
+                            md.max_seqlen_k, scale=m.p.scale, lse_decode=lse_d, decode_sliding_window=W)
+    torch.cuda.synchronize()
+    p = m.p
+    cu_q, cu_k, _, pt = _meta(p)
+    kc, vc = stored_caches(p)
+    rows = np.stack(np.meshgrid(np.arange(m.tp, p.q.shape[0]), np.arange(p.num_q_heads), indexing="ij"),
+                    -1).reshape(-1, 2).astype(np.int64)
+    ref, ref_lse = oracle.attention(p.q, kc, vc, pt, cu_q, cu_k, num_q_heads=p.num_q_heads,
+                                    num_kv_heads=p.num_kv_heads, head_dim=p.head_dim, page_size=p.page_size,
+                                    causal=p.causal, scale=p.scale, window_left=W - 1, rows=rows)
+    nd = m.q_dec.shape[0]
+    compare(od.reshape(nd * p.num_q_heads, -1), ref, "decode half, window 256", lse_gpu=lse_d.reshape(-1),
+            lse_ref=ref_lse)
+    ref_full, _ = oracle_ref(p)
+    compare(op, ref_full[:m.tp], "prefill half (no window)")
+    assert pa.device_error() == 0
