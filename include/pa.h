@@ -365,10 +365,11 @@ pa_status pa_decode(const pa_decode_params *p, void *stream);
  *  - pre->scheduler must hold PA_MIXED_SCHEDULER_INTS int32 (zero before its
  *    first use, left zero by every completed launch: [0..1] the prefill
  *    counters, [2..3] the decode ones); dec->workspace as for pa_decode.
- *  - Both halves: bf16 pools, the same k_cache / v_cache / num_pages /
- *    page_size / head counts / head_dim; an even GQA group and
- *    num_kv_heads % 4 == 0; no window or block mask on the prefill half (a
- *    decode window is fine); dec->overlap_previous = 0, max_ctas ignored.
+ *  - Both halves: the same k_cache / v_cache / num_pages / page_size / head
+ *    counts / head_dim and pool type (bf16, or FP8 with the same k_scale and
+ *    v_scale); an even GQA group and num_kv_heads % 4 == 0; no window or
+ *    block mask on the prefill half (a decode window is fine);
+ *    dec->overlap_previous = 0, dec->max_ctas ignored.
  *    Otherwise PA_ERR_UNSUPPORTED / PA_ERR_INVALID, nothing launched.
  *  - A batch with no prefill rows is pa_decode(dec); one with no decode
  *    sequences pa_prefill(pre).

@@ -434,7 +434,8 @@ def mixed_batch(q_prefill: torch.Tensor, q_decode: torch.Tensor, k_cache: torch.
                 out_decode: torch.Tensor | None = None, lse_prefill: torch.Tensor | None = None,
                 lse_decode: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                 kv_chunk: int = 0, scheduler: torch.Tensor | None = None, prefill_ctas: int = 0,
-                decode_sliding_window: int = 0):
+                decode_sliding_window: int = 0, k_scale: torch.Tensor | None = None,
+                v_scale: torch.Tensor | None = None):
     """One continuous batch in one launch (``pa_mixed_batch``): prefill /
     extend of ``q_prefill`` [total_q, Hq, d] (cu_seqlens_q/k, its page table)
     and decode of ``q_decode`` [B, Hq, d] (cache_seqlens, its page table)
@@ -442,12 +443,13 @@ def mixed_batch(q_prefill: torch.Tensor, q_decode: torch.Tensor, k_cache: torch.
     prefill tiles before decode key ranges (the others start on decode at
     once); 0: the kernel chooses the count from the work of both halves.
     ``decode_sliding_window`` W > 0: each decode query sees its sequence's
-    last W keys only (the prefill half takes no window).  Returns
-    (out_prefill, out_decode)."""
+    last W keys only (the prefill half takes no window).  FP8 (uint8 E4M3)
+    pools take their per-KV-head ``k_scale`` / ``v_scale`` for both halves.
+    Returns (out_prefill, out_decode)."""
     dev = q_prefill.device
     p, out_prefill = _prefill_params(q_prefill, k_cache, v_cache, page_table_prefill, cu_seqlens_q, cu_seqlens_k,
                                      max_seqlen_q, max_seqlen_k_prefill, causal, scale, None, out_prefill,
-                                     lse_prefill, None, None, 0, int(prefill_ctas), scheduler, None,
+                                     lse_prefill, k_scale, v_scale, 0, int(prefill_ctas), scheduler, None,
                                      PA_MIXED_SCHEDULER_INTS)
     _need(q_decode, "q_decode", torch.bfloat16, dev)
     _need(cache_seqlens, "cache_seqlens", torch.int32, dev)
@@ -458,7 +460,7 @@ def mixed_batch(q_prefill: torch.Tensor, q_decode: torch.Tensor, k_cache: torch.
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     dp = _decode_params(q_decode, k_cache, v_cache, page_table_decode, cache_seqlens, max_seqlen_k_decode, scale,
-                        None, out_decode, lse_decode, workspace, kv_chunk,
+                        None, out_decode, lse_decode, workspace, kv_chunk, k_scale, v_scale,
                         sliding_window=int(decode_sliding_window))
     lib = _lib.load()
     _check(lib.pa_mixed_batch(ctypes.byref(p), ctypes.byref(dp), _stream(q_prefill)), lib)

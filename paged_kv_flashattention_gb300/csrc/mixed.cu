@@ -53,15 +53,17 @@ struct MixedArgs {
 // when the decode does on the others; a quarter more (plus one CTA) covers
 // the prefill's slowdown beside the decode stream, and prefill CTAs that
 // finish early join the decode.
-constexpr float kPrefillFlopPerNs = 9.0e5f;
+constexpr float kPrefillFlopPerNs = 9.0e5f;      // bf16 pools
 constexpr float kDecodeBytePerNs = 6.9e3f;
+constexpr float kPrefillFlopPerNsFp8 = 8.0e5f;   // FP8 (E4M3) pools
+constexpr float kDecodeBytePerNsFp8 = 5.9e3f;
 // The automatic count is at most half the grid: CTAs past it start on decode
 // without computing it.
 constexpr int kAutoPrefillShareMax = 2;
 
 // Called by every thread of a CTA (synchronises the CTA); every CTA reaches
 // the same count from the same inputs (fp32 sums in a fixed order).
-template <int D>
+template <int D, bool F8>
 __device__ int auto_prefill_ctas(const PrefillArgs &a, const DecodeArgs &da, float *red) {
     float pairs = 0.f, keys = 0.f;
     for (int b = threadIdx.x; b < a.num_seqs; b += blockDim.x) {
@@ -91,8 +93,8 @@ __device__ int auto_prefill_ctas(const PrefillArgs &a, const DecodeArgs &da, flo
         keys += red[nw + w];
     }
     __syncthreads();                      // red is free again
-    const float t_pre = pairs * (4.f * D * a.num_q_heads) / kPrefillFlopPerNs;
-    const float t_dec = keys * (4.f * D * da.num_kv_heads) / kDecodeBytePerNs;
+    const float t_pre = pairs * (4.f * D * a.num_q_heads) / (F8 ? kPrefillFlopPerNsFp8 : kPrefillFlopPerNs);
+    const float t_dec = keys * ((F8 ? 2.f : 4.f) * D * da.num_kv_heads) / (F8 ? kDecodeBytePerNsFp8 : kDecodeBytePerNs);
     if (!(t_pre > 0.f)) return 0;
     const float r = t_pre / (t_pre + t_dec);
     const int cap = (int)gridDim.x / kAutoPrefillShareMax;
@@ -103,9 +105,9 @@ __device__ int auto_prefill_ctas(const PrefillArgs &a, const DecodeArgs &da, flo
 // Shared-memory layout of the decode phase (from offset 0 of the aligned
 // dynamic shared memory, below the prefill kernel's barriers, which are not
 // reused).
-template <int D>
+template <int D, bool F8>
 struct MixedSmem {
-    using DS = DecodeSmem<D, kMixedHpc, 2, 3>;
+    using DS = DecodeSmem<D, kMixedHpc, F8 ? 1 : 2, 3>;
     static constexpr int kStages = DS::kStages;
     static constexpr int kRing = (DS::kRingBytes + 1023) / 1024 * 1024;
     static constexpr int kBars = 2 * kRing;                           // per stream: full, empty, chunk ring
@@ -116,10 +118,11 @@ struct MixedSmem {
     static int total(int num_seqs) { return kPrefix + (num_seqs + 1) * 4; }
 };
 
-template <int D, int G>
+template <int D, int G, bool F8>
 __global__ void __launch_bounds__(384, 1)
     mixed_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ DecodeArgs da, const MixedArgs m) {
-    using M = MixedSmem<D>;
+    using M = MixedSmem<D, F8>;
+    constexpr int EB = F8 ? 1 : 2;
     constexpr int HPC = kMixedHpc;
     constexpr int kStages = M::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -132,10 +135,10 @@ __global__ void __launch_bounds__(384, 1)
     int prefill_ctas = m.prefill_ctas;
     if (prefill_ctas <= 0) {
         const bool candidate = kStaticSixteenths > 0 || (int)blockIdx.x < (int)gridDim.x / kAutoPrefillShareMax;
-        prefill_ctas = candidate ? auto_prefill_ctas<D>(a, da, reinterpret_cast<float *>(smem)) : 0;
+        prefill_ctas = candidate ? auto_prefill_ctas<D, F8>(a, da, reinterpret_cast<float *>(smem)) : 0;
     }
     if ((int)blockIdx.x < prefill_ctas) {
-        prefill_body<D, 2, false, false>(a, prefill_ctas);   // ends with a CTA-wide barrier; TMEM freed
+        prefill_body<D, 2, F8, false>(a, prefill_ctas);   // ends with a CTA-wide barrier; TMEM freed
         // undo the prefill phase's register split: every warp back to the
         // launch's count (the host checked that the kernel was given it)
         if (warp < 8)
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (c0 < 0) break;
             const int64_t g0 = (int64_t)c0 * T, g1 = min((int64_t)c1 * T, total);
-            if (!decode_produce<D, HPC, 2, kStages>(da, prefix, T, g0, g1, ring, full, empty, stage_ctr, lane)) break;
+            if (!decode_produce<D, HPC, EB, kStages>(da, prefix, T, g0, g1, ring, full, empty, stage_ctr, lane)) break;
         }
         // the last stream to finish resets the counters for the next launch
         if (lane == 0) {
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0) mbar_arrive(&cempty[slot]);
             if (c0 < 0) break;
             const int64_t g0 = (int64_t)c0 * T, g1 = min((int64_t)c1 * T, total);
-            if (!decode_consume<D, G, HPC, false, kStages>(da, prefix, T, g0, g1, ring, full, empty, pbuf, stage_ctr, cw,
+            if (!decode_consume<D, G, HPC, F8, kStages>(da, prefix, T, g0, g1, ring, full, empty, pbuf, stage_ctr, cw,
                                                  lane))
                 break;
         }
@@ -273,20 +276,32 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
 }
 
-template <int D, int G>
+template <int D, int G, bool F8>
 cudaError_t launch_mixed_t(const PrefillArgs &a, const DecodeArgs &da, const MixedArgs &m, int grid,
                            cudaStream_t stream) {
-    using PS = PrefillSmem<D, 2, false>;
+    using PS = PrefillSmem<D, 2, F8>;
     // the decode phase's layout must end below the prefill barriers
-    if (MixedSmem<D>::total(da.num_seqs) > PS::kBars) return cudaErrorNotSupported;
+    if (MixedSmem<D, F8>::total(da.num_seqs) > PS::kBars) return cudaErrorNotSupported;
     const int smem = PS::kTotal + 1024;
-    auto kern = mixed_kernel<D, G>;
+    auto kern = mixed_kernel<D, G, F8>;
     static const cudaError_t regs = check_register_split(kern);
     if (regs != cudaSuccess) return regs;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, 384, smem, stream>>>(a, da, m);
     return cudaGetLastError();
+}
+
+template <bool F8>
+cudaError_t dispatch_mixed(const PrefillArgs &a, const DecodeArgs &da, const MixedArgs &m, int grid, int d, int g,
+                           cudaStream_t stream) {
+    if (d == 128)
+        return g == 2 ? launch_mixed_t<128, 2, F8>(a, da, m, grid, stream)
+             : g == 4 ? launch_mixed_t<128, 4, F8>(a, da, m, grid, stream)
+                      : launch_mixed_t<128, 8, F8>(a, da, m, grid, stream);
+    return g == 2 ? launch_mixed_t<64, 2, F8>(a, da, m, grid, stream)
+         : g == 4 ? launch_mixed_t<64, 4, F8>(a, da, m, grid, stream)
+                  : launch_mixed_t<64, 8, F8>(a, da, m, grid, stream);
 }
 
 }  // namespace
@@ -314,14 +329,8 @@ cudaError_t launch_mixed(const pa_prefill_params &pp, const pa_decode_params &dp
     a.num_ctas = 0;
     MixedArgs m{pp.scheduler + 2, kChunksPerSm * sms, pre_ctas};
     const int g = dp.num_q_heads / dp.num_kv_heads;
-    if (dp.head_dim == 128)
-        e = g == 2 ? launch_mixed_t<128, 2>(a, da, m, sms, stream)
-          : g == 4 ? launch_mixed_t<128, 4>(a, da, m, sms, stream)
-                   : launch_mixed_t<128, 8>(a, da, m, sms, stream);
-    else
-        e = g == 2 ? launch_mixed_t<64, 2>(a, da, m, sms, stream)
-          : g == 4 ? launch_mixed_t<64, 4>(a, da, m, sms, stream)
-                   : launch_mixed_t<64, 8>(a, da, m, sms, stream);
+    e = dp.kv_dtype == PA_KV_FP8_E4M3 ? dispatch_mixed<true>(a, da, m, sms, dp.head_dim, g, stream)
+                                      : dispatch_mixed<false>(a, da, m, sms, dp.head_dim, g, stream);
     if (e != cudaSuccess) return e;
     return launch_lse_combine(da.o_part, da.lse_part, nullptr, da.ws_header, da.ws_prefix, da.head_groups,
                               g * plan.heads_per_cta, dp.num_q_heads, dp.num_seqs * dp.num_q_heads,

@@ -390,8 +390,9 @@ pa_status pa_mixed_batch(const pa_prefill_params *pre, const pa_decode_params *d
         pre->page_size != dec->page_size || pre->num_q_heads != dec->num_q_heads ||
         pre->num_kv_heads != dec->num_kv_heads || pre->head_dim != dec->head_dim)
         return fail(PA_ERR_INVALID, "prefill and decode halves must share the pools and the head geometry");
-    if (pre->kv_dtype != PA_KV_BF16 || dec->kv_dtype != PA_KV_BF16)
-        return fail(PA_ERR_UNSUPPORTED, "the mixed-batch launch takes bf16 pools; call pa_prefill and pa_decode");
+    if (pre->kv_dtype != dec->kv_dtype || (pre->kv_dtype == PA_KV_FP8_E4M3 &&
+                                           (pre->k_scale != dec->k_scale || pre->v_scale != dec->v_scale)))
+        return fail(PA_ERR_INVALID, "prefill and decode halves must share the pool type and its scales");
     if (pre->sliding_window != 0 || pre->block_mask != nullptr)
         return fail(PA_ERR_UNSUPPORTED, "the mixed-batch launch's prefill half takes no window or block mask");
     if ((pre->num_q_heads / pre->num_kv_heads) % 2 != 0 || pre->num_kv_heads % 4 != 0)

@@ -89,8 +89,9 @@ MIXED_DECODE = dict(DECODE_BASE, num_q_heads=32, num_kv_heads=8, page_table_stri
 MIXED_CASES = [
     ("other_pools", dict(k_cache=0x9100), {}, INVALID),
     ("other_head_dim", {}, dict(head_dim=64), INVALID),
-    ("fp8_pools", dict(kv_dtype=1, k_scale=0xA000, v_scale=0xA100), dict(kv_dtype=1, k_scale=0xA000, v_scale=0xA100),
-     UNSUPPORTED),
+    ("fp8_other_scales", dict(kv_dtype=1, k_scale=0xA000, v_scale=0xA100), dict(kv_dtype=1, k_scale=0xA200, v_scale=0xA100),
+     INVALID),
+    ("mixed_pool_types", dict(kv_dtype=1, k_scale=0xA000, v_scale=0xA100), {}, INVALID),
     ("prefill_window", dict(sliding_window=64), {}, UNSUPPORTED),
     ("odd_group", dict(num_q_heads=8, num_kv_heads=8), dict(num_q_heads=8, num_kv_heads=8), UNSUPPORTED),
     ("kv_heads_not_4", dict(num_q_heads=12, num_kv_heads=6), dict(num_q_heads=12, num_kv_heads=6), UNSUPPORTED),

@@ -222,3 +222,45 @@ def test_mixed_batch_decode_sliding_window(cuda_device):
     ref_full, _ = oracle_ref(p)
     compare(op, ref_full[:m.tp], "prefill half (no window)")
     assert pa.device_error() == 0
+
+
+@pytest.mark.parametrize("d,hq,hkv,page", [(128, 32, 8, 16), (64, 16, 4, 1)])
+def test_mixed_batch_fp8(cuda_device, d, hq, hkv, page):
+    """One mixed launch over FP8 (E4M3) pools with per-KV-head scales: both
+    halves against the fp64 oracle on the same codes, the prefill half
+    bit-identical to pa_prefill over the same pools."""
+    import oracle
+    import paged_kv_flashattention_gb300 as pa
+    from paged_kv_flashattention_gb300 import metadata
+    from oracle_pins import _meta
+    from test_fp8_gpu import FP8Problem
+    rng = np.random.default_rng(710 + d + page)
+    dec_len = rng.integers(1, 3000, size=12)
+    pre_c, pre_e = [0, 500], [300, 77]
+    p = W.small_problem(711 + d + page, pre_c + [int(L) - 1 for L in dec_len], pre_e + [1] * len(dec_len),
+                        num_q_heads=hq, num_kv_heads=hkv, head_dim=d, page_size=page)
+    f = FP8Problem(p, cuda_device, 712 + d)
+    n = len(pre_c)
+    tp = int(p.extend_len[:n].sum())
+    tt = torch.from_numpy(p.token_table).to(cuda_device)
+    idx = torch.from_numpy(p.table_idx).to(cuda_device)
+    mp = metadata.prepare(p.cached_len[:n], p.extend_len[:n], tt, idx[:n], page)
+    md = metadata.prepare(p.cached_len[n:], p.extend_len[n:], tt, idx[n:], page)
+    lse_p = torch.empty((hq, tp), dtype=torch.float32, device=cuda_device)
+    lse_d = torch.empty((len(dec_len), hq), dtype=torch.float32, device=cuda_device)
+    sc = dict(k_scale=f.k_scale, v_scale=f.v_scale)
+    op, od = pa.mixed_batch(f.q[:tp], f.q[tp:], f.k_cache, f.v_cache, mp.page_table, mp.cu_seqlens_q,
+                            mp.cu_seqlens_k, mp.max_seqlen_q, mp.max_seqlen_k, md.page_table, md.cache_seqlens,
+                            md.max_seqlen_k, scale=p.scale, lse_prefill=lse_p, lse_decode=lse_d, **sc)
+    torch.cuda.synchronize()
+    cu_q, cu_k, _, pt = _meta(p)
+    ref, ref_lse = oracle.attention(p.q, f.kc, f.vc, pt, cu_q, cu_k, num_q_heads=hq, num_kv_heads=hkv,
+                                    head_dim=d, page_size=page, causal=True, scale=p.scale, k_scale=f.ks,
+                                    v_scale=f.vs)
+    compare(op, ref[:tp], f"fp8 mixed d{d} P{page}: prefill half", lse_gpu=lse_p.T.contiguous(), lse_ref=ref_lse[:tp])
+    compare(od, ref[tp:], f"fp8 mixed d{d} P{page}: decode half", lse_gpu=lse_d, lse_ref=ref_lse[tp:])
+    sp = pa.prefill(f.q[:tp], f.k_cache, f.v_cache, mp.page_table, mp.cu_seqlens_q, mp.cu_seqlens_k,
+                    mp.max_seqlen_q, mp.max_seqlen_k, causal=True, scale=p.scale, **sc)
+    torch.cuda.synchronize()
+    assert torch.equal(op.view(torch.int16), sp.view(torch.int16))
+    assert pa.device_error() == 0
