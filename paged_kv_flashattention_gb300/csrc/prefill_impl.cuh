@@ -287,9 +287,19 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// The mbarrier counts one more pending arrival until every cp.async this
+// thread issued so far has landed (a regular arrive must follow).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 // Page size 1: warps that gather K/V rows (the producer and the two warps of
 // the control warpgroup that have no other role, fewer if the ring is
-// shorter), loads dealt out round robin; each keeps one copy group in flight.
+// shorter), loads dealt out round robin.  bf16: each warp waits for its
+// copies, fences and signals the load.  FP8 (the producer gathers alone): a
+// load's barrier completes when its copies have landed and the warp goes on
+// to its next load at once (410 us against 446 on the FP8 extend workload;
+// with three bf16 gather warps the same measured no gain, and the proxy fence
+// it moves into the MMA thread cost page size 16 about 2 %).
 // Measured on the extend workload with page size 1 (5 ring slots): 1 warp
 // 698 us, 2 warps 393 us, 3 warps 282 us.
 constexpr int kGatherWarpsMax = 3;
@@ -330,9 +340,8 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs &a, int sched_cta
     uint8_t *sQ = smem + S::kQ;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBars);
     constexpr int NS = S::kSlots;
-    // each gather warp has at most one load in flight and signals it when it
-    // is complete, so G < NS leaves the MMA a slot; with FP8 pools the two
-    // spare warps widen tiles instead
+    // G < NS gather warps leave the MMA a slot; with FP8 pools the two spare
+    // warps widen tiles instead
     constexpr int kGatherWarps = F8 ? 1 : (NS - 1 < kGatherWarpsMax ? NS - 1 : kGatherWarpsMax);
     constexpr int NC = F8 ? S::kCSlots : NS;  // slots the MMA reads from
     constexpr int kConverters = F8 ? 2 : 0;
@@ -472,9 +481,9 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs &a, int sched_cta
     };
     // The loads of one item that gather warp g issues (page size 1): loads
     // g, g + kGatherWarps, ... of the CTA.  Each waits for its ring slot, is
-    // copied, and is signalled as soon as its copies are complete; the next
-    // load's page-table entries are read while the copies are in flight.
-    // False on a timeout.
+    // copied and signalled (see above; the regular arrive releases the zero
+    // rows written for keys past the end); the next load's page-table entries
+    // are read while the copies are in flight.  False on a timeout.
     auto gather_item = [&](const PrefillItem &it, int gl0, int g) {
         const int n = 2 * it.n_kv;
         int c = ((g - gl0) % kGatherWarps + kGatherWarps) % kGatherWarps;
@@ -491,8 +500,12 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs &a, int sched_cta
                 st = cur.at<EXT>(a, it, (c + kGatherWarps) >> 1);
                 gather_rows(it, st, rows);
             }
-            cp_async_wait_all();
-            fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA
+            if constexpr (F8) {        // the widening warps read the rows with generic loads
+                cp_async_mbar_arrive(&full[gl % NS]);
+            } else {
+                cp_async_wait_all();
+                fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA
+            }
             mbar_arrive(&full[gl % NS]);
         }
         return true;
