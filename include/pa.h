@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 2
+#define PA_ABI_VERSION 3
 
 typedef enum {
     PA_OK = 0,
@@ -81,6 +81,7 @@ typedef enum {
 #define PA_DEVERR_SEQLENS 2      /* cu_seqlens / cache_seqlens inconsistent */
 #define PA_DEVERR_TIMEOUT 4      /* a bounded wait in a kernel gave up */
 #define PA_DEVERR_POSITION 8     /* a RoPE position outside the cos/sin table */
+#define PA_DEVERR_TABLE_INDEX 16 /* a table_idx entry outside the token table's rows */
 
 int pa_abi_version(void);
 const char *pa_status_string(int status);
@@ -206,11 +207,15 @@ pa_status pa_build_seqlens(const int32_t *cached_len, const int32_t *extend_len,
  *   page_table[b * page_table_stride + c] =
  *       floor(token_table[table_idx[b] * token_table_stride + c * page_size] / page_size)
  *   for c < ceil(max_seqlen_k / page_size).
- * token_table, table_idx, page_table: device int32.  Columns at and beyond
- * ceil(max_seqlen_k / page_size) are not written.
+ * token_table, table_idx, page_table: device int32; token_table holds
+ * token_table_rows rows.  Columns at and beyond ceil(max_seqlen_k /
+ * page_size) are not written.  A table_idx entry outside [0,
+ * token_table_rows) (device data: checked in the kernel) writes -1 across its
+ * row, which the attention kernels skip as a page outside the pool, and
+ * raises PA_DEVERR_TABLE_INDEX.
  */
 pa_status pa_build_page_table(const int32_t *token_table, int64_t token_table_stride,
-                              const int32_t *table_idx, int32_t num_seqs,
+                              int64_t token_table_rows, const int32_t *table_idx, int32_t num_seqs,
                               int32_t max_seqlen_k, int32_t page_size, int32_t *page_table,
                               int32_t page_table_stride, void *stream);
 

@@ -72,7 +72,7 @@ SIGNATURES = {
     "pa_rope_cos_sin_table": (ctypes.c_int, [c_p, c_i32, c_i32, ctypes.c_double]),
     "pa_rope_store_kv": (ctypes.c_int, [ctypes.POINTER(RopeStoreParams), c_p]),
     "pa_build_seqlens": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p]),
-    "pa_build_page_table": (ctypes.c_int, [c_p, c_i64, c_p, c_i32, c_i32, c_i32, c_p, c_i32, c_p]),
+    "pa_build_page_table": (ctypes.c_int, [c_p, c_i64, c_i64, c_p, c_i32, c_i32, c_i32, c_p, c_i32, c_p]),
     "pa_prefill": (ctypes.c_int, [ctypes.POINTER(PrefillParams), c_p]),
     "pa_decode_workspace_size": (c_size, [ctypes.POINTER(DecodeParams)]),
     "pa_decode_kv_chunk": (c_i32, [ctypes.POINTER(DecodeParams)]),

@@ -217,11 +217,16 @@ def build_page_table(token_table: torch.Tensor, table_idx: torch.Tensor, max_seq
     _need(table_idx, "table_idx", torch.int32, dev)
     B = table_idx.numel()
     ncols = -(-int(max_seqlen_k) // int(page_size))
+    if token_table.dim() != 2 or token_table.stride(1) != 1:
+        raise ValueError("token_table must be 2-D with unit column stride")
     if out is None:
         out = torch.empty((B, max(ncols, 1)), dtype=torch.int32, device=dev)
-    _need(out, "out", torch.int32, dev)
+    _need(out, "out", torch.int32, dev, contiguous=False)
+    if out.dim() != 2 or out.stride(1) != 1 or out.shape[0] < B or out.shape[1] < ncols:
+        raise ValueError(f"out must be 2-D with unit column stride and at least [{B}, {ncols}]")
     lib = _lib.load()
-    _check(lib.pa_build_page_table(_ptr(token_table), token_table.stride(0), _ptr(table_idx), B,
+    _check(lib.pa_build_page_table(_ptr(token_table), token_table.stride(0), token_table.shape[0],
+                                   _ptr(table_idx), B,
                                    int(max_seqlen_k), int(page_size), _ptr(out), out.stride(0),
                                    _stream(token_table)), lib)
     return out

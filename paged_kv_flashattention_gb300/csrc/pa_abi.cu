@@ -219,11 +219,12 @@ pa_status pa_build_seqlens(const int32_t *cached_len, const int32_t *extend_len,
 }
 
 pa_status pa_build_page_table(const int32_t *token_table, int64_t token_table_stride,
-                              const int32_t *table_idx, int32_t num_seqs, int32_t max_seqlen_k,
-                              int32_t page_size, int32_t *page_table, int32_t page_table_stride,
-                              void *stream) {
+                              int64_t token_table_rows, const int32_t *table_idx, int32_t num_seqs,
+                              int32_t max_seqlen_k, int32_t page_size, int32_t *page_table,
+                              int32_t page_table_stride, void *stream) {
     g_last_error[0] = 0;
     if (num_seqs < 0 || max_seqlen_k < 0) return fail(PA_ERR_INVALID, "negative num_seqs or max_seqlen_k");
+    if (token_table_rows < 0) return fail(PA_ERR_INVALID, "token_table_rows < 0");
     if (page_size <= 0) return fail(PA_ERR_INVALID, "page_size must be positive");
     const int64_t ncols = ((int64_t)max_seqlen_k + page_size - 1) / page_size;
     if (ncols > page_table_stride) return fail(PA_ERR_INVALID, "page_table_stride %d < %lld columns", page_table_stride, (long long)ncols);
@@ -231,7 +232,7 @@ pa_status pa_build_page_table(const int32_t *token_table, int64_t token_table_st
         return fail(PA_ERR_INVALID, "token_table_stride %lld too small for max_seqlen_k %d", (long long)token_table_stride, max_seqlen_k);
     if (num_seqs == 0 || ncols == 0) return PA_OK;
     if (!token_table || !table_idx || !page_table) return fail(PA_ERR_INVALID, "NULL pointer");
-    cudaError_t e = launch_build_page_table(token_table, token_table_stride, table_idx, num_seqs,
+    cudaError_t e = launch_build_page_table(token_table, token_table_stride, token_table_rows, table_idx, num_seqs,
                                             (int32_t)ncols, page_size, page_table, page_table_stride,
                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "build_page_table launch");

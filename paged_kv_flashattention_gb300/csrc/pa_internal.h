@@ -20,7 +20,7 @@ cudaError_t launch_store_kv_fp8(const void *k, const void *v, const int32_t *slo
 
 cudaError_t launch_rope_store(const pa_rope_store_params &p, cudaStream_t stream);
 
-cudaError_t launch_build_page_table(const int32_t *token_table, int64_t tt_stride,
+cudaError_t launch_build_page_table(const int32_t *token_table, int64_t tt_stride, int64_t tt_rows,
                                     const int32_t *table_idx, int32_t num_seqs, int32_t ncols,
                                     int32_t page_size, int32_t *page_table, int32_t pt_stride,
                                     cudaStream_t stream);

@@ -271,15 +271,20 @@ __global__ void __launch_bounds__(256) rope_store_kernel(const RopeStoreArgs a) 
 }
 
 __global__ void build_page_table_kernel(const int32_t *__restrict__ token_table, int64_t tt_stride,
-                                        const int32_t *__restrict__ table_idx, int32_t num_seqs,
-                                        int32_t ncols, int32_t page_size, int32_t *page_table,
-                                        int32_t pt_stride) {
+                                        int64_t tt_rows, const int32_t *__restrict__ table_idx,
+                                        int32_t num_seqs, int32_t ncols, int32_t page_size,
+                                        int32_t *page_table, int32_t pt_stride) {
     const int64_t n = (int64_t)num_seqs * ncols;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x) {
         const int32_t b = (int32_t)(e / ncols);
         const int32_t c = (int32_t)(e % ncols);
         const int64_t row = table_idx[b];
+        if (row < 0 || row >= tt_rows) {     // never read outside the token table
+            if (c == 0) raise_error(PA_DEVERR_TABLE_INDEX);
+            page_table[(int64_t)b * pt_stride + c] = -1;
+            continue;
+        }
         const int32_t slot = token_table[row * tt_stride + (int64_t)c * page_size];
         // floor division (slots of real tokens are >= 0)
         int32_t q = slot / page_size;
@@ -353,7 +358,7 @@ cudaError_t launch_store_kv(const void *k, const void *v, const int32_t *slot_ma
     return cudaGetLastError();
 }
 
-cudaError_t launch_build_page_table(const int32_t *token_table, int64_t tt_stride,
+cudaError_t launch_build_page_table(const int32_t *token_table, int64_t tt_stride, int64_t tt_rows,
                                     const int32_t *table_idx, int32_t num_seqs, int32_t ncols,
                                     int32_t page_size, int32_t *page_table, int32_t pt_stride,
                                     cudaStream_t stream) {
@@ -362,7 +367,7 @@ cudaError_t launch_build_page_table(const int32_t *token_table, int64_t tt_strid
     int64_t blocks = (n + 255) / 256;
     if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
     build_page_table_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-        token_table, tt_stride, table_idx, num_seqs, ncols, page_size, page_table, pt_stride);
+        token_table, tt_stride, tt_rows, table_idx, num_seqs, ncols, page_size, page_table, pt_stride);
     return cudaGetLastError();
 }
 

@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libpa.so does not export {name}"
         assert name in _lib.SIGNATURES, f"binding has no signature for {name}"
-    assert lib.pa_abi_version() == 2
+    assert lib.pa_abi_version() == 3
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
@@ -138,3 +138,18 @@ def test_graph_bucket_selection():
     assert bucket_for((1, 2, 4), 4) == 4
     with pytest.raises(ValueError):
         bucket_for((1, 2, 4), 5)
+
+
+def test_page_table_binding_checks_shapes():
+    """The binding rejects a page-table output too small for the rows and
+    columns it would write, on the host, before any call into the library."""
+    import torch
+    from paged_kv_flashattention_gb300 import api
+    tt = torch.zeros((4, 64), dtype=torch.int32)
+    idx = torch.arange(3, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        api.build_page_table(tt, idx, 64, 16, out=torch.zeros((2, 4), dtype=torch.int32))
+    with pytest.raises(ValueError):
+        api.build_page_table(tt, idx, 64, 16, out=torch.zeros((3, 3), dtype=torch.int32))
+    with pytest.raises(ValueError):
+        api.build_page_table(tt.t(), idx, 64, 16, out=torch.zeros((3, 4), dtype=torch.int32))

@@ -24,7 +24,7 @@ def _cuda_home():
 
 def test_c_program_abi_closed_form(cuda_device, tmp_path):
     import paged_kv_flashattention_gb300 as pa     # the in-tree libpa.so is built
-    assert pa.abi_version() == 2
+    assert pa.abi_version() == 3
     gcc = shutil.which("gcc") or shutil.which("cc")
     if gcc is None:
         pytest.skip("no C compiler")

@@ -95,3 +95,22 @@ def test_page_table_row_selection(cuda_device):
                               torch.from_numpy(ti).to(cuda_device), mk, 16).cpu().numpy()
     want = oracle.page_table_from_token_table(p.token_table, ti, mk, 16)
     assert np.array_equal(got, want)
+
+
+def test_page_table_index_out_of_range(cuda_device):
+    """A table_idx entry outside the token table's rows (device data) reads
+    nothing: its row becomes -1 (a page the attention kernels skip) and
+    PA_DEVERR_TABLE_INDEX is raised; the other rows are still exact."""
+    import paged_kv_flashattention_gb300 as pa
+    p = W.small_problem(32, [40, 3, 17], [1, 1, 1], page_size=16)
+    rows = p.token_table.shape[0]
+    ti = np.array([1, rows, 0, -1, 2], np.int32)
+    mk = 41
+    pa.device_error()                                   # clear earlier bits
+    got = pa.build_page_table(torch.from_numpy(p.token_table).to(cuda_device),
+                              torch.from_numpy(ti).to(cuda_device), mk, 16).cpu().numpy()
+    assert pa.device_error() & 16
+    ok = [0, 2, 4]
+    want = oracle.page_table_from_token_table(p.token_table, ti[ok], mk, 16)
+    assert np.array_equal(got[ok], want)
+    assert np.all(got[[1, 3]] == -1)
