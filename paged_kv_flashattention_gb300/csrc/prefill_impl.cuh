@@ -113,6 +113,7 @@ struct PrefillArgs {
     int32_t window;               // sliding window W (0 = none): keys >= position - (W - 1)
     const uint8_t *bmask;         // block-sparse mask [num_seqs][bm_q][bm_k] over 128 x 128 blocks, or null
     int32_t bm_q, bm_k;
+    int32_t max_q, max_k;         // the call's max_seqlen_q / max_seqlen_k (bounds of the device lengths)
     int32_t num_ctas;             // CTAs that run the work loop (the last of them resets sched);
                                   // 0: the count passed to prefill_body
 };
@@ -160,6 +161,14 @@ __device__ __forceinline__ bool prefill_item(const PrefillArgs &a, int v, Prefil
     const int k = rest / a.num_seqs;
     const int q0 = a.cu_q[b];
     const int Lq = a.cu_q[b + 1] - q0;
+    const int Lk = a.cu_k[b + 1] - a.cu_k[b];
+    // device lengths outside the call's bounds: the request is skipped (its
+    // rows are not written) rather than read or written out of bounds
+    if (q0 < 0 || Lq < 0 || q0 + Lq > a.total_q || Lq > a.max_q || Lk < 0 || Lk > a.max_k ||
+        (Lk > 0 && Lq > Lk)) {
+        raise_error(PA_DEVERR_SEQLENS);
+        return false;
+    }
     const int tiles = (Lq + kBM - 1) / kBM;
     if (k >= tiles) return false;
     it.b = b;
@@ -167,7 +176,7 @@ __device__ __forceinline__ bool prefill_item(const PrefillArgs &a, int v, Prefil
     it.h0 = hp * T;
     it.kvh = it.h0 / (a.num_q_heads / a.num_kv_heads);
     it.q0 = q0;
-    it.Lk = a.cu_k[b + 1] - a.cu_k[b];
+    it.Lk = Lk;
     it.off = it.Lk - Lq;                                  // cached prefix length
     it.rows_here = min(kBM, Lq - it.tile * kBM);
     int kv_end = it.Lk;                                   // keys the tile's last row sees
@@ -1062,6 +1071,8 @@ cudaError_t prefill_setup(const pa_prefill_params &p, PrefillArgs &a, int &T) {
     a.lse_stride = p.lse_stride;
     a.num_seqs = p.num_seqs;
     a.total_q = p.total_q;
+    a.max_q = p.max_seqlen_q;
+    a.max_k = p.max_seqlen_k;
     a.num_q_heads = p.num_q_heads;
     a.num_kv_heads = p.num_kv_heads;
     a.page_size = p.page_size;

@@ -223,3 +223,34 @@ def test_prefill_and_decode_overlapped(cuda_device):
     compare(out_p, ref_p, "prefill on 12 SMs")
     compare(out_d, ref_d, "decode overlapped with prefill")
     compare(small, ref_d, "decode on 5 CTAs")
+
+
+def test_prefill_device_lengths_out_of_bounds(cuda_device):
+    """cu_seqlens on the device that break the call's bounds (rows past
+    total_q, more keys than max_seqlen_k) skip that request: nothing is read
+    or written out of bounds, PA_DEVERR_SEQLENS is raised, and the other
+    requests are still exact."""
+    import paged_kv_flashattention_gb300 as pa
+    p = W.small_problem(940, [100, 0, 40, 7], [50, 130, 20, 9], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                        page_size=16)
+    d = DeviceProblem(p, cuda_device)
+    d.store()
+    m = d.metadata()
+    ref, _ = oracle_ref(p)
+    cu_q, cu_k = m.cu_seqlens_q.clone(), m.cu_seqlens_k.clone()
+    # request 1: 200 more keys than max_seqlen_k allows (request 2 keeps its length)
+    cu_k[2:] += 200
+    # request 3: its rows run past total_q
+    cu_q[4] += 64
+    Tq = d.q.shape[0]
+    out = torch.zeros_like(d.q)
+    pa.device_error()
+    pa.prefill(d.q, d.k_cache, d.v_cache, m.page_table, cu_q, cu_k, m.max_seqlen_q, m.max_seqlen_k, causal=True,
+               scale=p.scale, out=out)
+    torch.cuda.synchronize()
+    assert pa.device_error() & 2
+    cq = np.concatenate([[0], np.cumsum(p.extend_len)])
+    for b in (0, 2):
+        rows = slice(int(cq[b]), int(cq[b + 1]))
+        compare(out[rows], ref[rows], f"request {b} beside out-of-bounds lengths")
+    assert torch.all(out[int(cq[1]):int(cq[2])] == 0) and torch.all(out[int(cq[3]):Tq] == 0)
