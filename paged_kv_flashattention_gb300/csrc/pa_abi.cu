@@ -399,6 +399,11 @@ pa_status pa_mixed_batch(const pa_prefill_params *pre, const pa_decode_params *d
     if ((pre->num_q_heads / pre->num_kv_heads) % 2 != 0 || pre->num_kv_heads % 4 != 0)
         return fail(PA_ERR_UNSUPPORTED, "the mixed-batch launch needs an even GQA group and num_kv_heads %% 4 == 0");
     if (dec->overlap_previous != 0) return fail(PA_ERR_INVALID, "overlap_previous must be 0 in a mixed-batch launch");
+    // the mixed launch splits the decode rows by groups of 4 KV heads, which
+    // can outnumber the standalone decode's groups checked above
+    if ((int64_t)dec->num_seqs * dec->max_seqlen_k * (dec->num_kv_heads / 4) > INT32_MAX)
+        return fail(PA_ERR_UNSUPPORTED, "the mixed-batch decode rows (num_seqs x max_seqlen_k x KV-head groups of 4) "
+                                        "exceed 32-bit arithmetic; call pa_prefill and pa_decode");
     cudaError_t e = launch_mixed(*pre, *dec, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "mixed-batch configuration not supported (too many decode sequences for one CTA's shared memory?)");
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "mixed-batch launch");

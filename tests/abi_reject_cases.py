@@ -97,6 +97,11 @@ MIXED_CASES = [
     ("kv_heads_not_4", dict(num_q_heads=12, num_kv_heads=6), dict(num_q_heads=12, num_kv_heads=6), UNSUPPORTED),
     ("overlap_previous", {}, dict(overlap_previous=1), INVALID),
     ("no_scheduler", dict(scheduler=0), {}, INVALID),
+    # FP8 at d = 64: the standalone decode groups 8 KV heads (2^30 rows pass its
+    # check), the mixed launch groups 4 (2^31 rows do not)
+    ("decode_rows_overflow", dict(kv_dtype=1, k_scale=0xA000, v_scale=0xA100, head_dim=64, num_pages=1 << 20),
+     dict(kv_dtype=1, k_scale=0xA000, v_scale=0xA100, head_dim=64, num_seqs=16384, max_seqlen_k=1 << 16,
+          page_table_stride=1 << 12, num_pages=1 << 20, kv_chunk=1 << 15, workspace_bytes=1 << 50), UNSUPPORTED),
 ]
 
 ROPE_CASES = [
