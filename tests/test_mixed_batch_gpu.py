@@ -1,7 +1,9 @@
 """Parity at full size on the benchmark's own workload and launch path: the
 mixed continuous batch (256 decode sequences with contexts log-uniform in
 [512, 32768] and two 2048-token prefill chunks over a 40 GB pool), run by
-bench.MixedBatch.step() exactly as bench.py times it.  Sampled outputs are
+bench.MixedBatch.step() exactly as bench.py times it: the headline's single
+mixed-batch launch (12 prefill CTAs, 256-key T-ranges), and the PDL overlap
+schedule its schedule comparison also times.  Sampled outputs are
 checked one by one against the oracle: for a handful of sequences the pages
 they read are copied to the host before the step, the oracle applies the
 step's KV store to them and computes those rows."""
@@ -46,9 +48,11 @@ def _oracle_rows(prob, k_pages, v_pages, page_ids, seqs, q_rows, new_k, new_v, n
                             scale=prob.scale, rows=rows)
 
 
-def test_mixed_batch_full_size_sampled(cuda_device):
+@pytest.mark.parametrize("schedule", ["fused", "overlap"])
+def test_mixed_batch_full_size_sampled(cuda_device, schedule):
     import bench
     mb = bench.MixedBatch(cuda_device)
+    mb.schedule = schedule
     dec, pre = mb.dec, mb.pre
     L = dec.device_len
     order = np.argsort(L)
@@ -70,7 +74,7 @@ def test_mixed_batch_full_size_sampled(cuda_device):
     knew, vnew = _bits(mb.k_new), _bits(mb.v_new)
     ref, _ = _oracle_rows(dec, kd, vd, pages_d, dseqs, _bits(mb.q_dec)[dseqs], knew[dseqs],
                           vnew[dseqs], dec.slot_mapping[dseqs], decode=True)
-    compare(mb.out_dec[torch.tensor(dseqs, device=cuda_device)], ref, "mixed batch decode (sampled)")
+    compare(mb.out_dec[torch.tensor(dseqs, device=cuda_device)], ref, f"{schedule}: decode (sampled)")
 
     # prefill rows: a sample of each chunk's rows (first, last, random), all heads
     rng = np.random.default_rng(3)
@@ -81,4 +85,6 @@ def test_mixed_batch_full_size_sampled(cuda_device):
     ref_rows, _ = _oracle_rows(pre, kp, vp, pages_p, pseqs, _bits(mb.q_pre), knew[nd:], vnew[nd:],
                                pre.slot_mapping, decode=False, rows=pairs)
     got = mb.out_pre[torch.from_numpy(pairs[:, 0]).to(cuda_device), torch.from_numpy(pairs[:, 1]).to(cuda_device)]
-    compare(got, ref_rows, "mixed batch prefill (sampled rows)")
+    compare(got, ref_rows, f"{schedule}: prefill (sampled rows)")
+    del mb
+    torch.cuda.empty_cache()
