@@ -329,7 +329,8 @@ def _pct(sorted_vals, q):
 # The other workloads of the path, each timed on its own in the default run
 # (config name -> microbenchmark cases): tiny decode, Llama-3.2-1B-shaped
 # decode, varlen causal prefill 16 x 512, extend with a partial prefix hit at
-# page size 16 and 1, the store of the 16 x 512 batch, and the FP8 variants.
+# page size 16 and 1, the store of the 16 x 512 batch, a smaller mixed batch
+# in one launch, and the FP8 variants.
 CONFIG_CASES = {
     "tiny_decode": ["tiny_decode"],
     "llama32_1b_decode": ["llama32_1b_decode", "llama32_1b_decode_fp8"],
@@ -338,6 +339,7 @@ CONFIG_CASES = {
     "extend_partial_hit": ["extend_partial_hit_p16", "extend_partial_hit_p1", "extend_partial_hit_p16_fp8",
                            "extend_partial_hit_p1_fp8", "extend_partial_hit_p16_mask50"],
     "decode_64seq_logu": ["decode_64seq_logu", "decode_64seq_logu_fp8"],
+    "mixed_64seq_logu": ["mixed_64seq_logu", "mixed_64seq_logu_fp8"],
 }
 
 
@@ -733,6 +735,7 @@ MICRO_CASES = {
     # decode_64seq_logu's sequences and two 2048-token prefill chunks over one
     # pool, in one mixed-batch launch (automatic prefill share, 256-key T-ranges)
     "mixed_64seq_logu": (None, None, "mixed"),
+    "mixed_64seq_logu_fp8": (None, None, "mixed"),
 }
 
 
@@ -834,7 +837,7 @@ def prepare_case(name, dev):
         fn = lambda: pa.mixed_batch(qp, qd, kc, vc, mp.page_table, mp.cu_seqlens_q, mp.cu_seqlens_k,
                                     mp.max_seqlen_q, mp.max_seqlen_k, md.page_table, md.cache_seqlens,
                                     md.max_seqlen_k, scale=p.scale, out_prefill=op, out_decode=od, workspace=ws,
-                                    scheduler=sched, kv_chunk=256)
+                                    scheduler=sched, kv_chunk=256, **scales)
         kv_row = Hkv * D * 2 * kc.element_size()
         work = (int(p.device_len[:nd].astype(np.int64).sum()) * kv_row + 2 * qd.numel() * 2 +
                 int(p.device_len[nd:].astype(np.int64).sum()) * kv_row + 2 * qp.numel() * 2)

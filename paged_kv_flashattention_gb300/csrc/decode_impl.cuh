@@ -190,10 +190,15 @@ __device__ __forceinline__ void decode_prefix(const DecodeArgs &a, int32_t *pref
 // 16-token stages into the ring (per token one bulk copy of the K row and
 // one of the V row), continuing the stage count of earlier ranges.  False
 // on a timeout.
+// part 0: this warp issues the K and the V rows of every stage (lanes 0-15
+// K, 16-31 V); part 1: only the K rows; part 2: only the V rows (a second
+// producer warp on the same ranges and stages: twice the copy-issue rate).
+// Each producer warp arrives on a stage's full barrier once, expecting the
+// bytes it copies itself (the barrier counts one arrival per producer warp).
 template <int D, int HPC, int EB, int STAGES = stages_for<D, EB, HPC>()>
 __device__ bool decode_produce(const DecodeArgs &a, const int32_t *prefix, int64_t T, int64_t g0,
                                int64_t g1, uint8_t *ring, uint64_t *full, uint64_t *empty, int &stage_ctr,
-                               int lane) {
+                               int lane, int part = 0) {
     using S = DecodeSmem<D, HPC, EB, STAGES>;
     constexpr int kStages = S::kStages;
     const int B = a.num_seqs, HG = a.head_groups;
@@ -214,10 +219,10 @@ __device__ bool decode_produce(const DecodeArgs &a, const int32_t *prefix, int64
             const int round = stage_ctr / kStages;
             if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) return false;
             const int n = min(kStageTok, k1 - t0);
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * n * S::kRowBytes);
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], (part == 0 ? 2u : 1u) * n * S::kRowBytes);
             __syncwarp();
             const int tok = lane & 15;
-            if (tok < n) {
+            if (tok < n && (part == 0 || (part == 1) == (lane < 16))) {
                 const int j = s0 + t0 + tok;
                 int64_t page = pt[j / a.page_size];
                 if (page < 0 || page >= a.num_pages) {   // never read outside the pool

@@ -20,9 +20,12 @@
 // The log-sum-exp combine of the decode partials follows as a second launch
 // (a programmatic dependent, as after the decode kernel).
 //
-// Roles in the decode phase (384 threads): stream 0 = producer warp 8,
-// consumers 0-3; stream 1 = producer warp 10, consumers 4-7; warps 9 and 11
-// wait at the final barrier.
+// Roles in the decode phase (384 threads): stream 0 = producer warps 8 (it
+// takes the key ranges and copies the K rows) and 9 (the V rows), consumers
+// 0-3; stream 1 = producer warps 10 and 11, consumers 4-7.  Two producer
+// warps per stream: at two streams per SM one warp's copy issue caps the
+// rate of 512-byte FP8 rows (about 4.7 TB/s measured with one issuing warp
+// per stream).
 #include "decode_impl.cuh"
 #include "prefill_impl.cuh"
 
@@ -155,12 +158,12 @@ __global__ void __launch_bounds__(384, 1)
         for (int s = 0; s < 2; ++s) {
             uint64_t *bars = reinterpret_cast<uint64_t *>(smem + M::kBars) + s * M::kBarsPerStream;
             for (int i = 0; i < kStages; ++i) {
-                mbar_init(&bars[i], 1);                      // stage full (producer's expect-tx)
+                mbar_init(&bars[i], 2);                      // stage full (each producer warp's expect-tx)
                 mbar_init(&bars[kStages + i], HPC);          // stage empty (one arrive per consumer warp)
             }
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&bars[2 * kStages + i], 1);        // key range published
-                mbar_init(&bars[2 * kStages + 2 + i], HPC);  // key range read by every consumer warp
+                mbar_init(&bars[2 * kStages + 2 + i], HPC + 1);  // key range read by the consumers and the V producer
             }
         }
         fence_mbar_init();
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(384, 1)
     int64_t T = (total + m.num_chunks - 1) / m.num_chunks;   // rows per T-range
     T = (T + 15) / 16 * 16;
     if (T < da.min_split) T = da.min_split;
-    const int stream = (warp >= 4 && warp < 8) || warp == 10 ? 1 : 0;
+    const int stream = warp < 8 ? warp >> 2 : (warp - 8) >> 1;   // warps 0-3, 8, 9: 0; 4-7, 10, 11: 1
     // T-ranges [0, N) of the decode rows, cut into one slice of Q ranges per
     // stream of the CTAs without prefill items (of all CTAs when all have
     // some).  Each such stream first walks the first K = 7/8 of its slice:
@@ -246,7 +249,8 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (c0 < 0) break;
             const int64_t g0 = (int64_t)c0 * T, g1 = min((int64_t)c1 * T, total);
-            if (!decode_produce<D, HPC, EB, kStages>(da, prefix, T, g0, g1, ring, full, empty, stage_ctr, lane)) break;
+            if (!decode_produce<D, HPC, EB, kStages>(da, prefix, T, g0, g1, ring, full, empty, stage_ctr, lane, 1))
+                break;
         }
         // the last stream to finish resets the counters for the next launch
         if (lane == 0) {
@@ -255,6 +259,20 @@ __global__ void __launch_bounds__(384, 1)
                 atomicExch(&m.dsched[0], 0);
                 atomicExch(&m.dsched[1], 0);
             }
+        }
+    } else if (warp == 9 || warp == 11) {
+        // ------------------------------ stream V producer (same ranges) ----
+        int stage_ctr = 0;
+        for (int n = 0;; ++n) {
+            const int slot = n & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&cfull[slot], (n >> 1) & 1))) break;
+            const int c0 = cidx[2 * slot], c1 = cidx[2 * slot + 1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cempty[slot]);
+            if (c0 < 0) break;
+            const int64_t g0 = (int64_t)c0 * T, g1 = min((int64_t)c1 * T, total);
+            if (!decode_produce<D, HPC, EB, kStages>(da, prefix, T, g0, g1, ring, full, empty, stage_ctr, lane, 2))
+                break;
         }
     } else if (warp < 8) {
         // -------------------------------------------- stream consumers ----
