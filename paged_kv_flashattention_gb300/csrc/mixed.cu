@@ -5,18 +5,18 @@
 //
 // The first prefill_ctas CTAs (one CTA per SM; the caller's count, else
 // chosen in the kernel from the work of both halves) first run the prefill
-// kernel's persistent work loop (prefill_impl.cuh): they
-// take 128-row query tiles from the prefill work counter until none are
-// left, drain their pipelines and free TMEM.  Every CTA then turns into two
-// decode streams over the same shared memory, each a producer warp and four
-// consumer warps running the split-KV decode of decode_impl.cuh: the streams
-// take key ranges of the decode batch (equal numbers of (sequence, head
-// group, key) rows): each stream of the CTAs without prefill work first walks
-// most of its own slice of the rows, and the slices' tails are handed out one
-// short range at a time from a second device counter.  The CTAs without prefill work start on decode at
-// once and the prefill CTAs join as they finish, so the tensor-bound prefill
-// runs under the HBM-bound decode read and the decode work still spreads
-// over every SM at the end.
+// kernel's persistent work loop (prefill_impl.cuh): they take 128-row query
+// tiles from the prefill work counter until none are left, drain their
+// pipelines and free TMEM.  Every CTA then turns into two decode streams over
+// the same shared memory, each two producer warps and four consumer warps
+// running the split-KV decode of decode_impl.cuh.  The streams take key
+// ranges of the decode batch (equal numbers of (sequence, head group, key)
+// rows): each stream of the CTAs without prefill work first walks most of its
+// own slice of the rows, and the slices' tails are handed out from a second
+// device counter in runs that shrink with the work left.  The CTAs without
+// prefill work start on decode at once and the prefill CTAs join as they
+// finish, so the tensor-bound prefill runs under the HBM-bound decode read
+// and the decode work still spreads over every SM at the end.
 // The log-sum-exp combine of the decode partials follows as a second launch
 // (a programmatic dependent, as after the decode kernel).
 //
