@@ -3,7 +3,8 @@
 with pa_decode within the parity tolerance on two calls in a row (the shared
 scratch keeps the previous call's contents), and with the fp64 oracle.  Its
 rejection of sizes beyond the fixed 32 MiB scratch is checked without a GPU
-(tests/abi_reject_cases.py).  This file is collected last on purpose."""
+(tests/abi_reject_cases.py), so nothing here depends on the order in which
+the test files run."""
 import pytest
 import torch
 
