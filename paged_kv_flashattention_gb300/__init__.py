@@ -7,7 +7,9 @@ split-KV decode and the log-sum-exp combine, and both attention halves of a
 mixed batch in one launch; this package is its thin torch binding.  PyTorch
 provides device memory and streams only.
 """
-from .api import (PA_KV_BF16, PA_KV_FP8_E4M3, PA_MIXED_SCHEDULER_INTS, PagedAttentionError, abi_version,
+from .api import (PA_DEVERR_PAGE_RANGE, PA_DEVERR_POSITION, PA_DEVERR_SEQLENS, PA_DEVERR_TABLE_INDEX,
+                  PA_DEVERR_TIMEOUT, PA_KV_BF16, PA_KV_FP8_E4M3, PA_MIXED_SCHEDULER_INTS, PagedAttentionError,
+                  abi_version,
                   build_page_table,
                   build_seqlens, decode, decode_noalloc, decode_kv_chunk, decode_workspace_size,
                   device_error, lse_combine, mixed_batch, prefill, prefill_scheduler, rope_cos_sin_table,
@@ -23,4 +25,6 @@ __all__ = [
     "DecodeGraphRunner", "bucket_for",
     "store_kv", "store_kv_fp8", "PA_KV_BF16", "PA_KV_FP8_E4M3", "PA_MIXED_SCHEDULER_INTS",
     "rope_cos_sin_table", "rope_store_kv",
+    "PA_DEVERR_PAGE_RANGE", "PA_DEVERR_SEQLENS", "PA_DEVERR_TIMEOUT", "PA_DEVERR_POSITION",
+    "PA_DEVERR_TABLE_INDEX",
 ]

@@ -81,11 +81,26 @@ def abi_version() -> int:
     return int(_lib.load().pa_abi_version())
 
 
+# Device error bits (include/pa.h, PA_DEVERR_*).
+PA_DEVERR_PAGE_RANGE = 1
+PA_DEVERR_SEQLENS = 2
+PA_DEVERR_TIMEOUT = 4
+PA_DEVERR_POSITION = 8
+PA_DEVERR_TABLE_INDEX = 16
+
+
 def device_error() -> int:
-    """Read and clear the device error word (synchronises the current stream)."""
+    """Read and clear the device error word (synchronises the current stream).
+
+    A launch whose bounded wait gave up (PA_DEVERR_TIMEOUT) may leave its
+    scheduler counters non-zero, and the next launch sharing the array would
+    skip work items: the scheduler arrays cached by ``prefill_scheduler``
+    are cleared then (after the device has drained)."""
     lib = _lib.load()
     bits = ctypes.c_int32(0)
     _check(lib.pa_device_error(ctypes.byref(bits), _stream()), lib)
+    if bits.value & PA_DEVERR_TIMEOUT:
+        _reset_schedulers()
     return int(bits.value)
 
 
@@ -257,6 +272,18 @@ _sched_lock = threading.Lock()
 _sched_arrays: dict = {}
 PA_PREFILL_SCHEDULER_INTS = 2
 PA_MIXED_SCHEDULER_INTS = 4
+
+
+def _reset_schedulers() -> None:
+    """Zero every cached scheduler array once the work in flight has ended."""
+    with _sched_lock:
+        arrays = list(_sched_arrays.values())
+    for t in arrays:
+        if t.is_cuda:
+            torch.cuda.synchronize(t.device)
+        t.zero_()
+        if t.is_cuda:
+            torch.cuda.synchronize(t.device)
 
 
 def prefill_scheduler(device=None, stream=None) -> torch.Tensor:

@@ -153,3 +153,42 @@ def test_page_table_binding_checks_shapes():
         api.build_page_table(tt, idx, 64, 16, out=torch.zeros((3, 3), dtype=torch.int32))
     with pytest.raises(ValueError):
         api.build_page_table(tt.t(), idx, 64, 16, out=torch.zeros((3, 4), dtype=torch.int32))
+
+
+def test_device_error_bits_match_header():
+    """The binding's PA_DEVERR_* constants are the header's."""
+    import paged_kv_flashattention_gb300 as pa
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    defs = dict(re.findall(r"#define (PA_DEVERR_\w+) (\d+)", text))
+    assert defs, "no PA_DEVERR_* defines found"
+    for name, value in defs.items():
+        assert getattr(pa, name) == int(value), name
+
+
+def test_timeout_clears_cached_schedulers(monkeypatch):
+    """After a device error word with PA_DEVERR_TIMEOUT, the cached scheduler
+    arrays are zero again (a timed-out launch may leave its counters set);
+    other error bits leave them alone.  The library call is a fake that
+    reports the bits, so nothing runs on a device."""
+    import torch
+    from paged_kv_flashattention_gb300 import api
+
+    class FakeLib:
+        bits = 0
+
+        def pa_device_error(self, out, stream):
+            ctypes.cast(out, ctypes.POINTER(ctypes.c_int32))[0] = self.bits
+            return 0
+
+    fake = FakeLib()
+    monkeypatch.setattr(api._lib, "load", lambda: fake)
+    monkeypatch.setattr(api, "_stream", lambda t=None: 0)
+    arrays = {("cpu", 1): torch.tensor([5, 3, 0, 0], dtype=torch.int32),
+              ("cpu", 2): torch.tensor([0, 0, 7, 1], dtype=torch.int32)}
+    monkeypatch.setattr(api, "_sched_arrays", arrays)
+    fake.bits = api.PA_DEVERR_PAGE_RANGE
+    assert api.device_error() == api.PA_DEVERR_PAGE_RANGE
+    assert int(arrays[("cpu", 1)].sum()) == 8 and int(arrays[("cpu", 2)].sum()) == 8
+    fake.bits = api.PA_DEVERR_TIMEOUT | api.PA_DEVERR_SEQLENS
+    assert api.device_error() == api.PA_DEVERR_TIMEOUT | api.PA_DEVERR_SEQLENS
+    assert all(int(t.abs().sum()) == 0 for t in arrays.values())
