@@ -593,6 +593,9 @@ def run_gpu(args):
         line["device_error"] |= device_error()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(mb, args.cpu_seconds)
+        if "configs" in line:
+            for cfg, r in config_cpu_baselines(args.config_cpu_seconds).items():
+                line["configs"][cfg]["cpu_baseline"] = r
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -666,6 +669,80 @@ def cpu_baseline(mb: MixedBatch, target_s: float):
             "kind": "oracle",
             "sample": f"fp64 oracle decode of {len(seqs)} of the 256 decode sequences "
                       f"({total_b / reps / 1e9:.2f} GB of K/V) x {reps} repetitions, {total_t:.1f} s"}
+
+
+# The oracle on the other workloads, each in the unit of its GPU case: the
+# config name, the config number and the case it stands beside.
+CONFIG_CPU_CASES = {"tiny_decode": 1, "llama32_1b_decode": 2, "varlen_prefill_16x512": 3,
+                    "extend_partial_hit": 4}
+
+
+def oracle_config_rate(p: W.Problem, budget_s: float, threads: int | None = None):
+    """The fp64 oracle on host workload p (its new K/V stored first): whole
+    requests in a seeded order, one oracle call each (the oracle computes
+    only the requested rows), cycling through them until about budget_s
+    seconds are spent (at least one request).  Decode workloads are rated in
+    GB/s of the K/V the sampled sequences read, prefill workloads in TFLOP/s
+    of 4 d Hq per visible (query, key) pair; both also in query tokens per
+    second."""
+    import oracle
+    row = p.num_kv_heads * p.head_dim
+    kc, vc = p.k_cache.copy(), p.v_cache.copy()
+    oracle.store_kv(p.k_new.reshape(-1, row), p.v_new.reshape(-1, row), p.slot_mapping,
+                    kc.reshape(-1, row), vc.reshape(-1, row))
+    cu_q, cu_k, _, mq, mk = oracle.seqlens(p.cached_len, p.extend_len)
+    pt = oracle.page_table_from_token_table(p.token_table, p.table_idx, max(mk, 1), p.page_size)
+    decode = bool(np.all(p.extend_len == 1))
+    saved = oracle.num_threads()
+    if threads is not None:
+        oracle.set_threads(threads)
+    try:
+        spent, tokens, work, calls = 0.0, 0, 0, 0
+        order = [int(b) for b in np.random.default_rng(11).permutation(p.num_seqs) if cu_q[b + 1] > cu_q[b]]
+        seen = set()
+        for n in range(1000 * len(order)):
+            b = order[n % len(order)]
+            q0, q1 = int(cu_q[b]), int(cu_q[b + 1])
+            Lk = int(cu_k[b + 1] - cu_k[b])
+            tok = np.arange(q0, q1, dtype=np.int64)
+            rows = np.stack([np.repeat(tok, p.num_q_heads),
+                             np.tile(np.arange(p.num_q_heads, dtype=np.int64), q1 - q0)], axis=1)
+            t0 = time.perf_counter()
+            oracle.attention(p.q, kc, vc, pt, cu_q, cu_k, num_q_heads=p.num_q_heads,
+                             num_kv_heads=p.num_kv_heads, head_dim=p.head_dim, page_size=p.page_size,
+                             causal=p.causal, scale=p.scale, rows=rows)
+            spent += time.perf_counter() - t0
+            tokens += q1 - q0
+            calls += 1
+            seen.add(b)
+            if decode:
+                work += Lk * row * 2 * 2
+            else:                    # visible pairs of the end-aligned causal rows
+                off = Lk - (q1 - q0)
+                work += 4 * p.head_dim * p.num_q_heads * sum(min(Lk, off + i + 1) for i in range(q1 - q0))
+            if spent >= budget_s:
+                break
+        cores = oracle.num_threads()
+    finally:
+        oracle.set_threads(saved)
+    value = work / spent / (1e9 if decode else 1e12)
+    return {"value": round(value, 4), "unit": "GB/s" if decode else "TFLOP/s",
+            "tokens_per_s": round(tokens / spent, 1), "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle on {len(seen)} of {p.num_seqs} requests, {calls} request calls "
+                      f"({tokens} query tokens), {spent:.2f} s"}
+
+
+def config_cpu_baselines(budget_s: float):
+    """The oracle on each workload of CONFIG_CPU_CASES with every host
+    thread, and with one thread on the two decode workloads."""
+    out = {}
+    for name, cfg in CONFIG_CPU_CASES.items():
+        p = W.config(cfg)
+        r = oracle_config_rate(p, budget_s)
+        if cfg in (1, 2):
+            r["single_thread"] = oracle_config_rate(p, budget_s, threads=1)
+        out[name] = r
+    return out
 
 
 def run_reference(args):
@@ -920,6 +997,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target wall time of the CPU-oracle baseline sample")
+    ap.add_argument("--config-cpu-seconds", type=float, default=2.0,
+                    help="oracle time per workload of the configs block's CPU baselines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-sms", type=int, default=12,
                     help="SMs the prefill gets while decode runs beside it (0 = one after the other)")
