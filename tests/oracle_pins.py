@@ -329,6 +329,31 @@ def check_permutation_invariance(lib=None):
     _assert_close(l, l2, 0.0, "permutation lse")
 
 
+def check_threads_and_rows_invariance(lib=None):
+    """The oracle computes every (token, head) row on its own, so neither the
+    number of threads nor computing a sample of rows may change a value: one
+    thread and every thread give the same bits, and the rows mode returns the
+    same bits as the full call at those rows (the sampled parity tests and the
+    bench's CPU baselines use it)."""
+    p = W.small_problem(21, [0, 37, 130, 5], [19, 64, 150, 1], num_q_heads=8, num_kv_heads=2, head_dim=64,
+                        page_size=16)
+    full_o, full_l = run_oracle(p, lib)
+    saved = oracle.num_threads()
+    try:
+        oracle.set_threads(1)
+        one_o, one_l = run_oracle(p, lib)
+    finally:
+        oracle.set_threads(saved)
+    assert np.array_equal(one_o, full_o) and np.array_equal(one_l, full_l), "thread count changed the oracle"
+    rng = np.random.default_rng(5)
+    tok = rng.integers(0, full_o.shape[0], size=40)
+    head = rng.integers(0, p.num_q_heads, size=40)
+    rows = np.stack([tok, head], axis=1).astype(np.int64)
+    ro, rl = run_oracle(p, lib, rows=rows)
+    assert np.array_equal(ro, full_o[tok, head]) and np.array_equal(rl, full_l[tok, head]), \
+        "rows mode differs from the full call"
+
+
 def check_shared_prefix(lib=None):
     """Two requests whose tables share physical prefix pages give the same
     result as two requests holding private copies of those pages."""
@@ -788,4 +813,5 @@ ALL_CHECKS = [check_block_mask_brute_force, check_block_mask_closed_forms,
               check_single_key, check_dominant_key, check_empty, check_sdpa_library,
               check_decode_is_last_prefill_row, check_extend_is_prefill_tail,
               check_gqa_equals_repeated_mha, check_page_size_equivalence,
-              check_permutation_invariance, check_shared_prefix, check_online_and_split_merge]
+              check_permutation_invariance, check_shared_prefix, check_online_and_split_merge,
+              check_threads_and_rows_invariance]
